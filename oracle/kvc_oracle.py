@@ -1,0 +1,606 @@
+"""Plain CPU oracle of the budgeted KV-cache compaction pass.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, the smoke check and the CPU
+baseline leg of the benchmark import this module; the library and its
+Python binding never do, and nothing here calls the library.
+
+Sources (page title, then the section / equation):
+  * PASK  = "Parser Transitions Already Reveal Structural Responsibility: KV
+            Persistence for Structured Generation" (arXiv 2608.28276)
+  * PACE  = "PACE: Keeping the Right Tokens in the KV Cache Is Not Enough for
+            Long-Horizon LLM Agents" (arXiv 2611.10240)
+  * CommitKV = "CommitKV: Lifecycle-Aware KV Cache Compression via Commit
+            Transitions for Multi-Turn Agents" (arXiv 2608.07855)
+
+Floating point is fp64 except where the result decides an integer or a
+stored bit pattern: re-rotation and quantisation follow a fixed fp32
+operation order (each product, sum, square root and quotient rounded once,
+no fused multiply-add), the precision the CUDA kernels use, so that the
+stored bf16 keys and the int8/int4 codes can be compared bit for bit.
+
+Every function below is pinned by a `-m "not gpu"` test against values the
+pages print, closed forms, library routines or brute force; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+
+ACT_RELEASE, ACT_INT4, ACT_INT8, ACT_BF16 = 0, 1, 2, 3
+FLAG_PROTECT, FLAG_EXCLUDE = 1, 2
+QUANT_G32_BF16, QUANT_ROW_FP16 = 0, 1
+UNIT_OK, UNIT_OVER_BUDGET, UNIT_BAD_INDEX, UNIT_BAD_FLAGS = 0, 1, 2, 3
+
+BF16_MIN_POSITIVE = 2.0 ** -133      # smallest bf16 subnormal
+FP16_MIN_POSITIVE = 2.0 ** -24       # smallest fp16 subnormal
+FP16_MAX = 65504.0
+
+# ----------------------------------------------------------------------------
+# number formats
+# ----------------------------------------------------------------------------
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp32 values (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def f32_to_bf16_bits(x) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest even; NaN stays NaN."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint32)
+    nan = np.isnan(x)
+    if nan.any():
+        r = np.where(nan, ((u >> np.uint64(16)) | np.uint64(0x40)).astype(np.uint32), r)
+    return r.astype(np.uint16)
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round fp32 values to the nearest bf16 and return them as fp32."""
+    return bf16_bits_to_f32(f32_to_bf16_bits(x))
+
+
+# ----------------------------------------------------------------------------
+# layer groups -- PASK, App. A.2
+# ----------------------------------------------------------------------------
+
+
+def layer_group_bounds(n_layers: int, n_groups: int) -> list:
+    """Group boundaries b_k = floor((k*L + G - 1) / G), k = 0..G.
+
+    For G = 3 this is PASK's b1 = floor((L+2)/3), b2 = floor((2L+2)/3); the
+    same rule is used for any number of groups.
+    """
+    return [(k * n_layers + n_groups - 1) // n_groups if 0 < k < n_groups
+            else (0 if k == 0 else n_layers) for k in range(n_groups + 1)]
+
+
+def layer_group(layer: int, n_layers: int, n_groups: int) -> int:
+    b = layer_group_bounds(n_layers, n_groups)
+    for c in range(n_groups):
+        if b[c] <= layer < b[c + 1]:
+            return c
+    raise ValueError("layer out of range")
+
+
+# ----------------------------------------------------------------------------
+# a1/a2: observation-window attention mass -- PASK Eq. 1; the SnapKV window
+# scorer described in PASK App. C.3 and CommitKV Sec. 3.1; the bonus of PACE
+# Sec. 3.1 is added to the score and the top-B are kept by the sum.
+# ----------------------------------------------------------------------------
+
+
+def window_mass(k, q, scale: float, row_block: int = 8) -> np.ndarray:
+    """Attention mass that the window rows put on each cached key.
+
+    k : [T][d] keys (already rotated at their physical positions)
+    q : [G][W][d] window queries of the G query heads that share this KV
+        head; row w of every head sits at cache index T - W + w and, by
+        causality, sees keys j <= T - W + w.
+    Returns mass[j] = sum over heads h and rows w of softmax_j(q_hw . k_j * scale),
+    in fp64.
+    """
+    k = np.asarray(k, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    T = k.shape[0]
+    G, W, d = q.shape
+    rows = q.reshape(G * W, d)
+    last_visible = np.tile(T - W + np.arange(W), G)          # per row
+    mass = np.zeros(T, dtype=np.float64)
+    j = np.arange(T)
+    for r0 in range(0, G * W, row_block):
+        r1 = min(G * W, r0 + row_block)
+        z = (rows[r0:r1] @ k.T) * scale                        # [rb][T]
+        z = np.where(j[None, :] <= last_visible[r0:r1, None], z, -np.inf)
+        m = z.max(axis=1, keepdims=True)
+        e = np.exp(z - m)
+        a = e / e.sum(axis=1, keepdims=True)
+        mass += a.sum(axis=0)
+    return mass
+
+
+def unit_scores(k_bits, q_bits, scale: float, bonus=None, acc=None) -> np.ndarray:
+    """score_j = fp32(mass_j + bonus_j + acc_j) for one unit (bf16 inputs as bits)."""
+    k = bf16_bits_to_f32(k_bits)
+    q = bf16_bits_to_f32(q_bits)
+    s = window_mass(k, q, scale)
+    if bonus is not None:
+        s = s + np.asarray(bonus, dtype=np.float32).astype(np.float64)
+    if acc is not None:
+        s = s + np.asarray(acc, dtype=np.float32).astype(np.float64)
+    return s.astype(np.float32)
+
+
+def page_max(scores, page_size: int) -> np.ndarray:
+    """Page score = maximum token score over each page (max pooling)."""
+    s = np.asarray(scores, dtype=np.float32)
+    return s.reshape(-1, page_size).max(axis=1)
+
+
+# ----------------------------------------------------------------------------
+# a3/a4: masks and deterministic selection
+# ----------------------------------------------------------------------------
+
+
+def canonical(scores) -> np.ndarray:
+    """-0 -> +0 and NaN -> -inf, so that the order of scores is total."""
+    s = np.asarray(scores, dtype=np.float32).copy()
+    s[np.isnan(s)] = -np.inf
+    s[s == 0] = 0.0
+    return s
+
+
+def rank_order(scores, idx) -> np.ndarray:
+    """Positions of `idx` sorted by (score descending, index ascending)."""
+    s = canonical(scores).astype(np.float64)
+    return np.lexsort((np.asarray(idx), -s))
+
+
+def item_masks(n_items: int, sink_items: int, recent_items: int, flags):
+    """forced / excluded / bad-flag masks over selection items (tokens or pages).
+
+    Sinks (the first `sink_items`) and the recent window (the last
+    `recent_items`) are always kept; PROTECT adds to the kept set (CommitKV
+    Eq. 13, N is a subset of I); EXCLUDE removes an item unless it is a sink
+    or recent item.  An item flagged both PROTECT and EXCLUDE is an error.
+    """
+    i = np.arange(n_items)
+    window = (i < sink_items) | (i >= n_items - recent_items)
+    fl = np.zeros(n_items, dtype=np.uint8) if flags is None else np.asarray(flags, np.uint8)
+    protect = (fl & FLAG_PROTECT) != 0
+    exclude = (fl & FLAG_EXCLUDE) != 0
+    bad = bool((protect & exclude).any())
+    forced = window | protect
+    excluded = exclude & ~window
+    return forced, excluded, bad
+
+
+def select_top(scores, budget: int, forced, excluded):
+    """Kept items (ascending) and unit status for token / page mode.
+
+    Forced items are kept; if they alone exceed the budget the unit is
+    OVER_BUDGET and nothing is kept (CommitKV Eq. 4: |I| <= B).  Otherwise
+    the k = min(budget - |F|, |E|) eligible items that rank first by
+    (score descending, index ascending) are added.
+    """
+    forced = np.asarray(forced, bool)
+    excluded = np.asarray(excluded, bool)
+    n_forced = int(forced.sum())
+    if n_forced > budget:
+        return np.zeros(0, dtype=np.int64), UNIT_OVER_BUDGET
+    elig = np.nonzero(~forced & ~excluded)[0]
+    k = min(budget - n_forced, elig.size)
+    order = rank_order(np.asarray(scores)[elig], elig)
+    take = elig[order[:k]]
+    kept = np.sort(np.concatenate([np.nonzero(forced)[0], take]))
+    return kept.astype(np.int64), UNIT_OK
+
+
+def sink_recent_pages(n_tokens: int, page_size: int, n_sink: int, n_recent: int):
+    """Pages holding any sink or recent token: (first pages, last pages)."""
+    n_pages = n_tokens // page_size
+    first = -(-n_sink // page_size)
+    last_start = (n_tokens - n_recent) // page_size
+    return first, n_pages - last_start
+
+
+def select_tokens(scores, n_tokens: int, budget: int, n_sink: int, n_recent: int,
+                  flags=None, page_size: int = 1):
+    """Token mode (page_size = 1) or page mode (scores are page scores).
+
+    Returns (kept token indices ascending, status).
+    """
+    if page_size == 1:
+        forced, excluded, bad = item_masks(n_tokens, n_sink, n_recent, flags)
+        if bad:
+            return np.zeros(0, dtype=np.int64), UNIT_BAD_FLAGS
+        return select_top(scores, budget, forced, excluded)
+    n_pages = n_tokens // page_size
+    sp, rp = sink_recent_pages(n_tokens, page_size, n_sink, n_recent)
+    forced, excluded, bad = item_masks(n_pages, sp, rp, flags)
+    if bad:
+        return np.zeros(0, dtype=np.int64), UNIT_BAD_FLAGS
+    pages, st = select_top(scores, budget // page_size, forced, excluded)
+    toks = (pages[:, None] * page_size + np.arange(page_size)[None, :]).reshape(-1)
+    return toks.astype(np.int64), st
+
+
+# ----------------------------------------------------------------------------
+# byte mode -- PASK App. B.3 (payload), App. B.4 (floors first, priority
+# order, floor excess recorded), Sec. 3.5 (floors take precedence)
+# ----------------------------------------------------------------------------
+
+
+def row_bytes(action: int, head_dim: int, quant_mode: int = QUANT_G32_BF16) -> int:
+    """Bytes stored for one token of one unit (its K row plus its V row)."""
+    d = head_dim
+    if action == ACT_RELEASE:
+        return 0
+    if action == ACT_BF16:
+        return 2 * 2 * d
+    scales = 2 * (d // 32) if quant_mode == QUANT_G32_BF16 else 2
+    code = d if action == ACT_INT8 else d // 2
+    return 2 * (code + scales)
+
+
+def select_bytes(scores, floors, budget_bytes: int, n_sink: int, n_recent: int,
+                 head_dim: int, quant_mode: int = QUANT_G32_BF16, flags=None):
+    """Byte-budget selection of one unit.
+
+    floors : per-token floor action from the (tag, layer-group) table.
+    Sink/recent and PROTECT tokens are held at bf16; EXCLUDE releases.
+    The remainder budget - sum(cost(floor)) is spent by promoting to bf16 the
+    longest prefix of the (score desc, index asc) order of the remaining
+    non-bf16 tokens whose summed upgrade costs fit.  A negative remainder is
+    recorded as floor excess and nothing is promoted.
+    Returns (action per token, floor_excess, status).
+    """
+    T = len(floors)
+    forced, excluded, bad = item_masks(T, n_sink, n_recent, flags)
+    if bad:
+        return np.zeros(T, dtype=np.uint8), 0, UNIT_BAD_FLAGS
+    act = np.asarray(floors, dtype=np.uint8).copy()
+    act[forced] = ACT_BF16
+    act[excluded] = ACT_RELEASE
+    cost = np.array([row_bytes(a, head_dim, quant_mode) for a in range(4)], dtype=np.int64)
+    rem = int(budget_bytes) - int(cost[act].sum())
+    if rem < 0:
+        return act, -rem, UNIT_OK
+    cand = np.nonzero(~forced & ~excluded & (act != ACT_BF16))[0]
+    order = cand[rank_order(np.asarray(scores)[cand], cand)]
+    delta = cost[ACT_BF16] - cost[act[order]]
+    n_up = int(np.searchsorted(np.cumsum(delta), rem, side="right"))
+    act[order[:n_up]] = ACT_BF16
+    return act, 0, UNIT_OK
+
+
+# ----------------------------------------------------------------------------
+# a5/a6: renumber, exact re-rotation -- PACE Sec. 3.2 (bounded positions,
+# Proposition 1); CommitKV Eq. 4 (apply one index set to K, V, positions)
+# ----------------------------------------------------------------------------
+
+
+def rope_angles(pos, head_dim: int, theta: float) -> np.ndarray:
+    """pos * theta^(-2i/d) for i < d/2, fp64."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.asarray(pos, dtype=np.float64)[..., None] * theta ** (-2.0 * i / head_dim)
+
+
+def rope_rotate(x, pos, head_dim: int, theta: float) -> np.ndarray:
+    """Split-half rotary rotation R_pos of x in fp64 (PACE Eq. 1)."""
+    x = np.asarray(x, dtype=np.float64)
+    h = head_dim // 2
+    a = rope_angles(pos, head_dim, theta)
+    c, s = np.cos(a), np.sin(a)
+    lo, hi = x[..., :h], x[..., h:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def rerotate_bits(k_bits, p: int, p_new: int, cos_tab, sin_tab) -> np.ndarray:
+    """Re-rotate one stored bf16 key from position p to p_new (fp32 spec).
+
+    cos/sin of (p_new - p) theta_i come from the engine's own tables through
+    the angle-difference identities and are normalised to unit length
+    (PACE Sec. 3.2); every product, sum, root and quotient is rounded to fp32
+    once, in this order, and the rotated halves are rounded to bf16.
+    If p_new == p the stored bits are returned unchanged.
+    """
+    k_bits = np.asarray(k_bits, dtype=np.uint16)
+    if p_new == p:
+        return k_bits.copy()
+    f = np.float32
+    c0 = np.asarray(cos_tab[p], dtype=f)
+    s0 = np.asarray(sin_tab[p], dtype=f)
+    c1 = np.asarray(cos_tab[p_new], dtype=f)
+    s1 = np.asarray(sin_tab[p_new], dtype=f)
+    C = (c1 * c0) + (s1 * s0)
+    S = (s1 * c0) - (c1 * s0)
+    n = np.sqrt((C * C) + (S * S))
+    C = C / n
+    S = S / n
+    h = k_bits.shape[-1] // 2
+    x = bf16_bits_to_f32(k_bits[..., :h])
+    y = bf16_bits_to_f32(k_bits[..., h:])
+    xr = (x * C) - (y * S)
+    yr = (y * C) + (x * S)
+    return f32_to_bf16_bits(np.concatenate([xr, yr], axis=-1))
+
+
+def new_positions(kept_sorted, pos_in, renumber: bool) -> np.ndarray:
+    """p' = rank among the kept rows in logical order if renumbering, else p."""
+    kept_sorted = np.asarray(kept_sorted)
+    if renumber:
+        return np.arange(kept_sorted.size, dtype=np.int64)
+    return np.asarray(pos_in)[kept_sorted].astype(np.int64)
+
+
+def smallest_pow2_limit(budget: int, interval: int, chunk: int) -> int:
+    """Smallest power of two L with L > B_max + H, B_max = budget + interval."""
+    need = budget + interval + chunk
+    L = 1
+    while L <= need:
+        L *= 2
+    return L
+
+
+def renumber_due(next_pos: int, limit: int, headroom: int) -> bool:
+    """PACE Sec. 3.2 trigger: next physical position within H of the limit L."""
+    return next_pos > limit - headroom
+
+
+# ----------------------------------------------------------------------------
+# quantisation -- PASK App. B.5 (symmetric, scale = max|x| / qmax rounded to
+# the scale format and floored at its smallest positive value, codes rounded
+# to nearest and clipped, zero groups -> zero codes and unit scale, two
+# signed nibbles per byte)
+# ----------------------------------------------------------------------------
+
+
+def _round_scale(s32: np.ndarray, quant_mode: int) -> np.ndarray:
+    if quant_mode == QUANT_G32_BF16:
+        s = bf16_round(s32)
+        return np.maximum(s, np.float32(BF16_MIN_POSITIVE))
+    s = s32.astype(np.float16)
+    s = np.minimum(s.astype(np.float32), np.float32(FP16_MAX))
+    return np.maximum(s, np.float32(FP16_MIN_POSITIVE))
+
+
+def quantize(x, qmax: int, quant_mode: int = QUANT_G32_BF16):
+    """Quantise rows x [..., d] (fp32 values of bf16 keys/values).
+
+    Groups are 32 consecutive elements (QUANT_G32_BF16, bf16 scale) or the
+    whole row (QUANT_ROW_FP16, fp16 scale).  Returns (codes int8 [..., d],
+    scales fp32 [..., n_groups]) with scales exactly representable in the
+    scale format.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    gs = 32 if quant_mode == QUANT_G32_BF16 else d
+    xg = x.reshape(x.shape[:-1] + (d // gs, gs))
+    a = np.abs(xg).max(axis=-1)
+    zero = a == 0
+    s = _round_scale(a / np.float32(qmax), quant_mode)
+    s = np.where(zero, np.float32(1.0), s).astype(np.float32)
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore"):
+        r = np.rint(xg / s[..., None])
+    codes = np.clip(r, -qmax, qmax).astype(np.int8)
+    codes[zero] = 0
+    return codes.reshape(x.shape), s
+
+
+def dequantize(codes, scales, quant_mode: int = QUANT_G32_BF16) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.int8)
+    d = codes.shape[-1]
+    gs = 32 if quant_mode == QUANT_G32_BF16 else d
+    cg = codes.reshape(codes.shape[:-1] + (d // gs, gs)).astype(np.float32)
+    return (cg * np.asarray(scales, np.float32)[..., None]).reshape(codes.shape)
+
+
+def pack_int4(codes) -> np.ndarray:
+    """Byte j holds element 2j in its low nibble and 2j+1 in its high nibble."""
+    c = np.asarray(codes, dtype=np.int8).astype(np.uint8)
+    lo = c[..., 0::2] & 0xF
+    hi = c[..., 1::2] & 0xF
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def unpack_int4(packed) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.uint8)
+    lo = (p & 0xF).astype(np.int8)
+    hi = (p >> 4).astype(np.int8)
+    lo = np.where(lo > 7, lo - 16, lo).astype(np.int8)
+    hi = np.where(hi > 7, hi - 16, hi).astype(np.int8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def scale_bits(scales, quant_mode: int) -> np.ndarray:
+    """Stored scale bit patterns: bf16 (g32 mode) or fp16 (row mode)."""
+    s = np.asarray(scales, dtype=np.float32)
+    if quant_mode == QUANT_G32_BF16:
+        return f32_to_bf16_bits(s)
+    return s.astype(np.float16).view(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# a7: consumer decode step -- PASK Eq. 1 over all kept rows; Eq. 15 merge
+# ----------------------------------------------------------------------------
+
+
+def attend(q, keys, values, scale: float) -> np.ndarray:
+    """softmax(keys q * scale)-weighted sum of values, fp64 (one query)."""
+    q = np.asarray(q, np.float64)
+    keys = np.asarray(keys, np.float64)
+    values = np.asarray(values, np.float64)
+    if keys.shape[0] == 0:
+        return np.zeros(values.shape[-1])
+    z = keys @ q * scale
+    m = z.max()
+    e = np.exp(z - m)
+    return (e[:, None] * values).sum(axis=0) / e.sum()
+
+
+def partition_stats(q, keys, values, scale: float):
+    """(max score v_j, exp-sum l_j, unnormalised value sum u_j) of one partition."""
+    q = np.asarray(q, np.float64)
+    z = np.asarray(keys, np.float64) @ q * scale
+    v = z.max()
+    e = np.exp(z - v)
+    return v, e.sum(), (e[:, None] * np.asarray(values, np.float64)).sum(axis=0)
+
+
+def merge_partitions(parts) -> np.ndarray:
+    """PASK Eq. 15: o = sum_j e^{v_j - v} u_j / sum_j e^{v_j - v} l_j; empty parts skipped."""
+    parts = [p for p in parts if p is not None]
+    v = max(p[0] for p in parts)
+    num = sum(math.exp(p[0] - v) * p[2] for p in parts)
+    den = sum(math.exp(p[0] - v) * p[1] for p in parts)
+    return num / den
+
+
+# ----------------------------------------------------------------------------
+# one unit end to end
+# ----------------------------------------------------------------------------
+
+
+@dataclass
+class Pool:
+    """Kept rows of one storage class of one unit, ascending by index."""
+    action: int
+    idx: np.ndarray
+    pos: np.ndarray = None          # new physical position p'
+    orig_pos: np.ndarray = None     # position before compaction
+    k: np.ndarray = None            # bf16 bits [n][d], or codes [n][d] / packed [n][d/2]
+    v: np.ndarray = None
+    k_scale: np.ndarray = None      # fp32 [n][groups]
+    v_scale: np.ndarray = None
+
+
+@dataclass
+class UnitResult:
+    scores: np.ndarray = None
+    page_scores: np.ndarray = None
+    status: int = UNIT_OK
+    floor_excess: int = 0
+    actions: np.ndarray = None
+    pools: dict = field(default_factory=dict)
+
+
+@dataclass
+class PassParams:
+    """Policy of one compaction pass (what the C-ABI's select parameters hold)."""
+    budget_tokens: int = 0
+    budget_bytes: int = 0
+    n_sink: int = 4
+    n_recent: int = 32
+    page_size: int = 1
+    renumber: bool = True
+    quant_mode: int = QUANT_G32_BF16
+    n_layer_groups: int = 3
+    softmax_scale: float = 0.0
+
+
+def select_unit(scores, page_scores, n_tokens, head_dim, params: PassParams,
+                flags=None, tags=None, table=None, group=0):
+    """Selection of one unit: returns (actions per token, floor_excess, status)."""
+    T = n_tokens
+    act = np.zeros(T, dtype=np.uint8)
+    if params.budget_bytes > 0:
+        floors = np.asarray(table, np.uint8)[np.asarray(tags, np.int64), group]
+        return select_bytes(scores, floors, params.budget_bytes, params.n_sink,
+                            params.n_recent, head_dim, params.quant_mode, flags)
+    src = scores if params.page_size == 1 else page_scores
+    kept, st = select_tokens(src, T, params.budget_tokens, params.n_sink, params.n_recent,
+                             flags, params.page_size)
+    act[kept] = ACT_BF16
+    return act, 0, st
+
+
+def compact_unit(k_bits, v_bits, pos_in, actions, params: PassParams, cos_tab, sin_tab):
+    """Gather, re-rotate and quantise the kept rows of one unit into pools."""
+    actions = np.asarray(actions)
+    kept_all = np.nonzero(actions != ACT_RELEASE)[0]
+    p_new_all = new_positions(kept_all, pos_in, params.renumber)
+    new_of = dict(zip(kept_all.tolist(), p_new_all.tolist()))
+    pools = {}
+    for a in (ACT_INT4, ACT_INT8, ACT_BF16):
+        idx = np.nonzero(actions == a)[0]
+        pool = Pool(action=a, idx=idx)
+        pool.orig_pos = np.asarray(pos_in)[idx].astype(np.int64)
+        pool.pos = np.array([new_of[int(i)] for i in idx], dtype=np.int64)
+        d = k_bits.shape[-1]
+        kr = np.zeros((idx.size, d), dtype=np.uint16)
+        for n, (i, p, p2) in enumerate(zip(idx, pool.orig_pos, pool.pos)):
+            kr[n] = rerotate_bits(k_bits[i], int(p), int(p2), cos_tab, sin_tab)
+        vr = np.asarray(v_bits)[idx]
+        if a == ACT_BF16:
+            pool.k, pool.v = kr, vr
+        else:
+            qmax = 7 if a == ACT_INT4 else 127
+            kc, ks = quantize(bf16_bits_to_f32(kr), qmax, params.quant_mode)
+            vc, vs = quantize(bf16_bits_to_f32(vr), qmax, params.quant_mode)
+            if a == ACT_INT4:
+                kc, vc = pack_int4(kc), pack_int4(vc)
+            pool.k, pool.v, pool.k_scale, pool.v_scale = kc, vc, ks, vs
+        pools[a] = pool
+    return pools
+
+
+def pool_rows_f32(pool: Pool, quant_mode: int):
+    """Dequantised (K, V) rows of a pool as fp32."""
+    if pool.action == ACT_BF16:
+        return bf16_bits_to_f32(pool.k), bf16_bits_to_f32(pool.v)
+    kc, vc = pool.k, pool.v
+    if pool.action == ACT_INT4:
+        kc, vc = unpack_int4(kc), unpack_int4(vc)
+    return (dequantize(kc, pool.k_scale, quant_mode), dequantize(vc, pool.v_scale, quant_mode))
+
+
+def decode_unit(q_bits, pools: dict, scale: float, quant_mode: int) -> np.ndarray:
+    """Decode-step outputs [G][d] (fp64) of the G query heads of one unit."""
+    ks, vs = [], []
+    for a in (ACT_INT4, ACT_INT8, ACT_BF16):
+        if a in pools and pools[a].idx.size:
+            k, v = pool_rows_f32(pools[a], quant_mode)
+            ks.append(k)
+            vs.append(v)
+    q = bf16_bits_to_f32(q_bits)
+    if not ks:
+        return np.zeros(q.shape)
+    K = np.concatenate(ks)
+    V = np.concatenate(vs)
+    return np.stack([attend(q[h], K, V, scale) for h in range(q.shape[0])])
+
+
+def run_unit(k_bits, v_bits, q_bits, pos_in, params: PassParams, cos_tab, sin_tab,
+             bonus=None, acc=None, flags=None, tags=None, table=None, group=0,
+             scores=None) -> UnitResult:
+    """Score, select and compact one unit.  `scores` may be given to skip scoring."""
+    T, d = k_bits.shape
+    scale = params.softmax_scale or 1.0 / math.sqrt(d)
+    res = UnitResult()
+    res.scores = unit_scores(k_bits, q_bits, scale, bonus, acc) if scores is None \
+        else np.asarray(scores, np.float32)
+    if params.page_size > 1:
+        res.page_scores = page_max(res.scores, params.page_size)
+    res.actions, res.floor_excess, res.status = select_unit(
+        res.scores, res.page_scores, T, d, params, flags, tags, table, group)
+    if res.status != UNIT_OK:
+        res.actions = np.zeros(T, dtype=np.uint8)
+    res.pools = compact_unit(k_bits, v_bits, pos_in, res.actions, params, cos_tab, sin_tab)
+    return res
+
+
+def cache_bytes(n_tokens: int, n_layers: int, n_kv_heads: int, head_dim: int,
+                action: int = ACT_BF16, quant_mode: int = QUANT_G32_BF16) -> int:
+    """Bytes of K and V payload for n_tokens tokens across all layers and KV heads."""
+    return n_tokens * n_layers * n_kv_heads * row_bytes(action, head_dim, quant_mode)

@@ -1,0 +1,482 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test ties one oracle function to something other than itself: values
+printed on the pages (tests/golden), closed forms, library routines
+(torch's bf16 cast and scaled-dot-product attention) or brute force on tiny
+inputs.  All run on the CPU.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# --------------------------------------------------------------------------- formats
+
+def test_bf16_rounding_matches_torch_cast():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * 10,
+        rng.standard_normal(2000).astype(np.float32) * 1e-39,        # subnormals
+        np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, 3.4e38, -3.4e38], np.float32),
+        # exact ties between two bf16 neighbours: even and odd lower mantissa
+        (np.arange(1, 200, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
+    ])
+    ours = o.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    back = o.bf16_bits_to_f32(ours)
+    ref_back = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(back, ref_back)
+
+
+# --------------------------------------------------------------------------- printed numbers
+
+def test_layer_groups_printed_by_pask():
+    for model, L, *ranges in _rows("pask_layer_groups.txt"):
+        b = o.layer_group_bounds(int(L), 3)
+        got = [f"{b[c]}-{b[c + 1] - 1}" for c in range(3)]
+        assert got == ranges, model
+        for c, r in enumerate(ranges):
+            lo, hi = map(int, r.split("-"))
+            assert all(o.layer_group(l, int(L), 3) == c for l in range(lo, hi + 1))
+
+
+def test_layer_groups_four_groups_cover_and_balance():
+    b = o.layer_group_bounds(32, 4)
+    assert b == [0, 8, 16, 24, 32]
+    for L in range(1, 80):
+        for G in range(1, 6):
+            if G > L:
+                continue
+            b = o.layer_group_bounds(L, G)
+            sizes = np.diff(b)
+            assert b[0] == 0 and b[-1] == L and sizes.min() >= 1
+            assert sizes.max() - sizes.min() <= 1
+
+
+def test_kv_accounting_printed_by_pace():
+    d, L, H = 128, 36, 8           # Qwen3-8B
+    for q, toks, val, unit, dec in _rows("kv_accounting.txt"):
+        toks, val, dec = int(toks), float(val), int(dec)
+        if q == "bytes_per_token":
+            assert o.cache_bytes(toks, L, H, d) == val * 1024
+        elif q == "key_store_keys_only":
+            got = o.cache_bytes(toks, L, H, d) / 2 / 1e9
+            assert round(got, dec) == val
+        else:
+            got = o.cache_bytes(toks, L, H, d) / 1e9
+            # the pages print the leading digits (14.75 GB is printed as 14.7)
+            assert math.floor(got * 10 ** dec) / 10 ** dec == val or round(got, dec) == val
+
+
+def test_payload_bits_of_pask_eq14():
+    for d, mR, mH, mL in _rows("pask_payload_bits.txt"):
+        d = int(d)
+        assert o.row_bytes(o.ACT_RELEASE, d) * 8 == int(mR)
+        assert o.row_bytes(o.ACT_BF16, d) * 8 == int(mH)
+        assert o.row_bytes(o.ACT_INT4, d, o.QUANT_ROW_FP16) * 8 == int(mL)
+
+
+def test_row_bytes_group32_layout():
+    # per K (or V) row at d = 128: bf16 256 B, int8 g32 128 + 4*2 = 136 B,
+    # int4 g32 64 + 8 = 72 B, row-mode int4 64 + 2 = 66 B
+    assert o.row_bytes(o.ACT_BF16, 128) == 2 * 256
+    assert o.row_bytes(o.ACT_INT8, 128) == 2 * 136
+    assert o.row_bytes(o.ACT_INT4, 128) == 2 * 72
+    assert o.row_bytes(o.ACT_INT4, 128, o.QUANT_ROW_FP16) == 2 * 66
+
+
+def test_pace_limit_rule():
+    for B, itv, H, Lim in _rows("pace_limit.txt"):
+        assert o.smallest_pow2_limit(int(B), int(itv), int(H)) == int(Lim)
+    assert o.renumber_due(8192 - 4096 + 1, 8192, 4096)
+    assert not o.renumber_due(8192 - 4096, 8192, 4096)
+
+
+# --------------------------------------------------------------------------- scoring
+
+def _sdpa_mass(k, q, scale):
+    """Window mass through torch's attention with V = identity (library routine)."""
+    T, d = k.shape
+    G, W, _ = q.shape
+    K = torch.from_numpy(np.asarray(k, np.float64))
+    eye = torch.eye(T, dtype=torch.float64)
+    vis = torch.arange(T)[None, :] <= (T - W + torch.arange(W))[:, None]
+    tot = torch.zeros(T, dtype=torch.float64)
+    for h in range(G):
+        Q = torch.from_numpy(np.asarray(q[h], np.float64))
+        a = torch.nn.functional.scaled_dot_product_attention(
+            Q[None], K[None], eye[None], attn_mask=vis[None], scale=scale)[0]
+        tot += a.sum(0)
+    return tot.numpy()
+
+
+@pytest.mark.parametrize("T,W,G,d", [(40, 8, 2, 16), (97, 16, 4, 32), (64, 64, 1, 8)])
+def test_window_mass_matches_library_attention(T, W, G, d):
+    rng = np.random.default_rng(T + W)
+    k = rng.standard_normal((T, d))
+    q = rng.standard_normal((G, W, d)) * 2
+    scale = 1 / math.sqrt(d)
+    ours = o.window_mass(k, q, scale)
+    ref = _sdpa_mass(k, q, scale)
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_window_mass_zero_query_closed_form():
+    T, W, G, d = 300, 24, 3, 16
+    k = np.random.default_rng(1).standard_normal((T, d))
+    q = np.zeros((G, W, d))
+    mass = o.window_mass(k, q, 0.25)
+    tw = T - W + np.arange(W)
+    closed = np.array([G * sum(1.0 / (t + 1) for t in tw if t >= j) for j in range(T)])
+    np.testing.assert_allclose(mass, closed, rtol=1e-12)
+
+
+def test_window_mass_conservation_and_dominant_key():
+    T, W, G, d = 257, 32, 4, 32
+    rng = np.random.default_rng(2)
+    k = rng.standard_normal((T, d))
+    q = rng.standard_normal((G, W, d))
+    mass = o.window_mass(k, q, 1 / math.sqrt(d))
+    assert abs(mass.sum() - W * G) < 1e-9
+    # a key aligned with every query and 50x longer takes all the mass of every row
+    k[5] = 50 * q.reshape(-1, d).mean(0) / np.linalg.norm(q.reshape(-1, d).mean(0)) * math.sqrt(d)
+    q2 = np.broadcast_to(k[5] / np.linalg.norm(k[5]), (G, W, d)) * 10
+    mass = o.window_mass(k, q2, 1.0)
+    assert mass[5] > W * G * (1 - 1e-9)
+
+
+def test_scores_add_bonus_and_accumulator():
+    w = wl.tiny().replace(n_tokens=200, window=16)
+    x = wl.make_inputs(w, with_tables=False)
+    kb = x["k_cache"][0, 0, 0].view(torch.int16).numpy().view(np.uint16)
+    qb = x["q_window"][0, 0, 0:2].view(torch.int16).numpy().view(np.uint16)
+    bonus = np.zeros(200, np.float32)
+    bonus[10:20] = 10.0
+    acc = np.linspace(0, 1, 200).astype(np.float32)
+    s0 = o.unit_scores(kb, qb, 0.125)
+    s1 = o.unit_scores(kb, qb, 0.125, bonus, acc)
+    np.testing.assert_allclose(s1, s0.astype(np.float64) + bonus + acc, rtol=1e-6, atol=1e-6)
+
+
+def test_page_max_brute_force():
+    s = np.random.default_rng(3).standard_normal(64).astype(np.float32)
+    pm = o.page_max(s, 16)
+    assert [pm[p] for p in range(4)] == [max(s[16 * p:16 * p + 16]) for p in range(4)]
+
+
+# --------------------------------------------------------------------------- selection
+
+def _beats(sa, ia, sb, ib):
+    """(score desc, index asc): does item a rank before item b?"""
+    ca, cb = o.canonical([sa])[0], o.canonical([sb])[0]
+    return ca > cb or (ca == cb and ia < ib)
+
+
+def _brute_top(scores, budget, forced, excluded):
+    n = len(scores)
+    F = [i for i in range(n) if forced[i]]
+    if len(F) > budget:
+        return [], o.UNIT_OVER_BUDGET
+    E = [i for i in range(n) if not forced[i] and not excluded[i]]
+    k = min(budget - len(F), len(E))
+    take = [e for e in E if sum(_beats(scores[x], x, scores[e], e) for x in E) < k]
+    return sorted(F + take), o.UNIT_OK
+
+
+def test_select_matches_pairwise_definition_with_ties():
+    rng = np.random.default_rng(4)
+    vals = np.array([-1.0, 0.0, -0.0, 0.5, 2.0, np.nan, -np.inf, np.inf], np.float32)
+    for trial in range(400):
+        T = int(rng.integers(1, 24))
+        s = rng.choice(vals, size=T)
+        budget = int(rng.integers(0, T + 3))
+        sink, recent = int(rng.integers(0, 3)), int(rng.integers(0, 3))
+        flags = rng.choice([0, 0, 0, o.FLAG_PROTECT, o.FLAG_EXCLUDE], size=T).astype(np.uint8)
+        forced, excluded, bad = o.item_masks(T, sink, recent, flags)
+        assert not bad
+        got, st = o.select_tokens(s, T, budget, sink, recent, flags)
+        ref, rst = _brute_top(s, budget, forced, excluded)
+        assert st == rst and list(got) == ref, (trial, s, budget)
+        if st == o.UNIT_OK:
+            assert len(got) == min(budget, int(forced.sum()) + int((~forced & ~excluded).sum()))
+
+
+def test_select_exhaustive_equal_scores_take_lowest_indices():
+    for T in range(1, 9):
+        for budget in range(0, T + 1):
+            got, st = o.select_tokens(np.ones(T, np.float32), T, budget, 0, 0)
+            assert list(got) == list(range(budget)) and st == o.UNIT_OK
+
+
+def test_select_budget_at_least_T_keeps_every_non_excluded_row():
+    T = 50
+    s = np.random.default_rng(5).standard_normal(T).astype(np.float32)
+    flags = np.zeros(T, np.uint8)
+    flags[[7, 9, 30]] = o.FLAG_EXCLUDE
+    flags[0] = o.FLAG_EXCLUDE              # sink: exclusion ignored
+    got, st = o.select_tokens(s, T, T + 5, 2, 3, flags)
+    assert list(got) == [i for i in range(T) if i not in (7, 9, 30)]
+
+
+def test_select_over_budget_and_bad_flags():
+    T = 20
+    s = np.zeros(T, np.float32)
+    got, st = o.select_tokens(s, T, 5, 4, 4)
+    assert st == o.UNIT_OVER_BUDGET and got.size == 0
+    flags = np.zeros(T, np.uint8)
+    flags[10] = o.FLAG_PROTECT | o.FLAG_EXCLUDE
+    got, st = o.select_tokens(s, T, 15, 1, 1, flags)
+    assert st == o.UNIT_BAD_FLAGS and got.size == 0
+
+
+def test_page_select_matches_token_level_definition():
+    rng = np.random.default_rng(6)
+    for trial in range(100):
+        P = int(rng.choice([2, 4, 8]))
+        n_pages = int(rng.integers(2, 12))
+        T = P * n_pages
+        s = rng.standard_normal(T).astype(np.float32)
+        s[rng.integers(0, T, 3)] = 1.0
+        budget = P * int(rng.integers(0, n_pages + 1))
+        sink, recent = int(rng.integers(0, P + 2)), int(rng.integers(0, P + 2))
+        pflags = rng.choice([0, 0, 0, o.FLAG_PROTECT, o.FLAG_EXCLUDE], size=n_pages).astype(np.uint8)
+        ps = o.page_max(s, P)
+        got, st = o.select_tokens(ps, T, budget, sink, recent, pflags, page_size=P)
+        # a page is forced iff one of its tokens is a sink or recent token
+        tok_window = (np.arange(T) < sink) | (np.arange(T) >= T - recent)
+        forced = tok_window.reshape(n_pages, P).any(1) | ((pflags & o.FLAG_PROTECT) != 0)
+        excluded = ((pflags & o.FLAG_EXCLUDE) != 0) & ~tok_window.reshape(n_pages, P).any(1)
+        ref_pages, rst = _brute_top(ps, budget // P, forced, excluded)
+        ref = [p * P + i for p in ref_pages for i in range(P)]
+        assert st == rst and list(got) == ref
+
+
+def _brute_bytes(scores, floors, budget, sink, recent, d, qm, flags):
+    T = len(scores)
+    forced, excluded, _ = o.item_masks(T, sink, recent, flags)
+    act = np.array(floors, np.uint8)
+    act[forced] = o.ACT_BF16
+    act[excluded] = o.ACT_RELEASE
+    cost = lambda a: o.row_bytes(int(a), d, qm)
+    rem = budget - sum(cost(a) for a in act)
+    if rem < 0:
+        return act, -rem
+    cand = [t for t in range(T) if not forced[t] and not excluded[t] and act[t] != o.ACT_BF16]
+    order = sorted(cand, key=lambda t: sum(_beats(scores[x], x, scores[t], t) for x in cand))
+    used = 0
+    for t in order:                      # longest prefix that fits
+        dlt = cost(o.ACT_BF16) - cost(act[t])
+        if used + dlt > rem:
+            break
+        used += dlt
+        act[t] = o.ACT_BF16
+    return act, 0
+
+
+def test_byte_mode_matches_prefix_knapsack_brute_force():
+    rng = np.random.default_rng(7)
+    for trial in range(200):
+        T = int(rng.integers(1, 32))
+        d = int(rng.choice([64, 128]))
+        qm = int(rng.choice([o.QUANT_G32_BF16, o.QUANT_ROW_FP16]))
+        s = rng.choice(np.array([0.1, 0.2, 0.3, 5.0], np.float32), size=T)
+        floors = rng.integers(0, 4, T).astype(np.uint8)
+        full = T * o.row_bytes(o.ACT_BF16, d)
+        budget = int(rng.integers(0, full + 1))
+        flags = rng.choice([0, 0, 0, 0, o.FLAG_PROTECT, o.FLAG_EXCLUDE], size=T).astype(np.uint8)
+        sink, recent = int(rng.integers(0, 3)), int(rng.integers(0, 3))
+        act, excess, st = o.select_bytes(s, floors, budget, sink, recent, d, qm, flags)
+        ref, rex = _brute_bytes(s, floors, budget, sink, recent, d, qm, flags)
+        assert st == o.UNIT_OK and excess == rex and np.array_equal(act, ref)
+        used = sum(o.row_bytes(int(a), d, qm) for a in act)
+        if excess == 0:
+            assert used <= budget
+        else:
+            assert used == budget + excess
+
+
+# --------------------------------------------------------------------------- rotation
+
+def test_rope_relative_identity_and_composition():
+    rng = np.random.default_rng(8)
+    d, th = 64, 1e4
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    for m, n in [(0, 0), (5, 3), (1000, 17), (8191, 40000)]:
+        lhs = o.rope_rotate(q, m, d, th) @ o.rope_rotate(k, n, d, th)
+        rhs = q @ o.rope_rotate(k, n - m, d, th)
+        assert abs(lhs - rhs) < 1e-9 * (1 + abs(lhs))
+        ab = o.rope_rotate(o.rope_rotate(k, m, d, th), n, d, th)
+        np.testing.assert_allclose(ab, o.rope_rotate(k, m + n, d, th), atol=1e-9)
+    # rotation preserves the norm of every split-half pair
+    r = o.rope_rotate(k, 123, d, th)
+    np.testing.assert_allclose(np.hypot(r[:32], r[32:]), np.hypot(k[:32], k[32:]), rtol=1e-12)
+
+
+@pytest.mark.parametrize("d,theta", [(64, 1e4), (128, 1e6)])
+def test_rerotation_equals_rotating_the_prerotation_key(d, theta):
+    """PACE Prop. 1: re-rotating k~ = R_p k by p'-p gives R_p' k (up to two bf16 roundings)."""
+    rng = np.random.default_rng(9)
+    cos, sin = wl.rope_tables(50000, d, theta)
+    cos, sin = cos.numpy(), sin.numpy()
+    h = d // 2
+    for _ in range(200):
+        k = rng.standard_normal(d)
+        p, p2 = int(rng.integers(0, 50000)), int(rng.integers(0, 50000))
+        stored = o.f32_to_bf16_bits(o.rope_rotate(k, p, d, theta).astype(np.float32))
+        got = o.bf16_bits_to_f32(o.rerotate_bits(stored, p, p2, cos, sin)).astype(np.float64)
+        want = o.rope_rotate(k, p2, d, theta)
+        err = np.hypot(got[:h] - want[:h], got[h:] - want[h:])
+        mag = np.hypot(want[:h], want[h:])
+        # each bf16 rounding moves a pair by at most 2^-8 of its length
+        assert np.all(err <= 2 * 2.0 ** -8 * mag * (1 + 1e-3) + 1e-30)
+        assert np.linalg.norm(got - want) <= 1e-2 * np.linalg.norm(want)
+
+
+def test_renumbered_score_depends_only_on_new_distance():
+    rng = np.random.default_rng(10)
+    d, theta = 128, 1e6
+    cos, sin = wl.rope_tables(40000, d, theta)
+    cos, sin = cos.numpy(), sin.numpy()
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    m_hat = 2048
+    for p, p2 in [(30000, 100), (12345, 2000), (7, 7)]:
+        stored = o.f32_to_bf16_bits(o.rope_rotate(k, p, d, theta).astype(np.float32))
+        kr = o.bf16_bits_to_f32(o.rerotate_bits(stored, p, p2, cos, sin))
+        lhs = o.rope_rotate(q, m_hat, d, theta) @ kr
+        rhs = q @ o.rope_rotate(k, p2 - m_hat, d, theta)
+        assert abs(lhs - rhs) <= 1e-2 * np.linalg.norm(q) * np.linalg.norm(k)
+
+
+def test_rerotation_identity_position_is_bitwise_copy():
+    bits = np.random.default_rng(11).integers(0, 65535, 128).astype(np.uint16)
+    cos, sin = wl.rope_tables(10, 128, 1e6)
+    assert np.array_equal(o.rerotate_bits(bits, 3, 3, cos.numpy(), sin.numpy()), bits)
+
+
+# --------------------------------------------------------------------------- quantisation
+
+@pytest.mark.parametrize("qmax", [7, 127])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_quant_error_at_most_half_scale(qmax, mode):
+    rng = np.random.default_rng(12)
+    x = o.bf16_round(rng.standard_normal((500, 128)).astype(np.float32) *
+                     np.exp(rng.standard_normal((500, 1))).astype(np.float32))
+    x[0, :32] = 0
+    x[1, 5] = 300.0
+    codes, s = o.quantize(x, qmax, mode)
+    xh = o.dequantize(codes, s, mode)
+    gs = 32 if mode == 0 else 128
+    s_el = np.repeat(s, gs, axis=-1)
+    assert np.all(np.abs(x - xh) <= s_el / 2)
+    assert np.all(np.abs(codes) <= qmax)
+
+
+def test_quant_zero_group_and_exact_codes():
+    codes, s = o.quantize(np.zeros((2, 64), np.float32), 7)
+    assert np.all(codes == 0) and np.all(s == 1.0)
+    rng = np.random.default_rng(13)
+    for qmax in (7, 127):
+        n = rng.integers(-qmax, qmax + 1, (50, 128))
+        n[:, ::32] = qmax                       # every group reaches the maximum
+        x = (n * 2.0 ** -3).astype(np.float32)   # exactly representable
+        codes, s = o.quantize(x, qmax)
+        assert np.array_equal(codes, n) and np.all(s == 2.0 ** -3)
+
+
+def test_quant_ties_round_to_even_and_scale_floor():
+    # scale 1 (max 7 -> 7/7), codes of 2.5 and 3.5 and -0.5 are 2, 4, -0
+    x = np.zeros(32, np.float32)
+    x[:4] = [7.0, 2.5, 3.5, -0.5]
+    codes, s = o.quantize(x, 7)
+    assert s[0] == 1.0 and list(codes[:4]) == [7, 2, 4, 0]
+    tiny = np.full(32, 2.0 ** -140, np.float32)      # max/7 rounds below bf16's minimum
+    codes, s = o.quantize(tiny, 7)
+    assert s[0] == 2.0 ** -133 and np.all(codes == 0)
+    codes, s = o.quantize(tiny, 7, o.QUANT_ROW_FP16)
+    assert s[0] == 2.0 ** -24
+
+
+def test_int4_pack_round_trip_low_nibble_first():
+    codes = np.array(list(itertools.product(range(-7, 8), repeat=2)), np.int8).reshape(-1)
+    packed = o.pack_int4(codes)
+    assert packed[0] == ((-7 & 0xF) | ((-7 & 0xF) << 4))
+    assert np.array_equal(o.unpack_int4(packed), codes)
+    assert o.pack_int4(np.array([1, 2], np.int8))[0] == 0x21
+
+
+# --------------------------------------------------------------------------- decode
+
+def test_partition_merge_eq15_equals_single_softmax():
+    rng = np.random.default_rng(14)
+    q = rng.standard_normal(64)
+    K, V = rng.standard_normal((300, 64)) * 3, rng.standard_normal((300, 64))
+    whole = o.attend(q, K, V, 0.125)
+    parts = [o.partition_stats(q, K[a:b], V[a:b], 0.125) for a, b in [(0, 7), (7, 200), (200, 300)]]
+    np.testing.assert_allclose(o.merge_partitions(parts + [None]), whole, rtol=1e-12)
+
+
+def test_attend_matches_library_attention():
+    rng = np.random.default_rng(15)
+    q = rng.standard_normal(32)
+    K, V = rng.standard_normal((50, 32)), rng.standard_normal((50, 32))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None, None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        scale=0.3)[0, 0].numpy()
+    np.testing.assert_allclose(o.attend(q, K, V, 0.3), ref, rtol=1e-12, atol=1e-14)
+
+
+# --------------------------------------------------------------------------- end to end
+
+def _unit_np(x, w, u):
+    b, l, g = wl.unit_coords(w, u)
+    G = w.group
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    return (bits(x["k_cache"][b, l, g]), bits(x["v_cache"][b, l, g]),
+            bits(x["q_window"][b, l, g * G:(g + 1) * G]), x["pos_in"][u].numpy())
+
+
+def test_inactive_pass_reproduces_the_cache_bytewise():
+    """PACE Sec. 5.7: with nothing evicted and no renumbering the cache is unchanged."""
+    w = wl.tiny().replace(n_tokens=300, budget_tokens=300, renumber=False)
+    x = wl.make_inputs(w)
+    k, v, q, pos = _unit_np(x, w, 1)
+    p = o.PassParams(budget_tokens=300, n_sink=4, n_recent=32, renumber=False)
+    r = o.run_unit(k, v, q, pos, p, x["rope_cos"].numpy(), x["rope_sin"].numpy())
+    pool = r.pools[o.ACT_BF16]
+    assert np.array_equal(pool.idx, np.arange(300))
+    assert np.array_equal(pool.k, k) and np.array_equal(pool.v, v)
+    assert np.array_equal(pool.pos, pos)
+
+
+def test_tiny_workload_end_to_end_invariants():
+    w = wl.tiny()
+    x = wl.make_inputs(w)
+    cos, sin = x["rope_cos"].numpy(), x["rope_sin"].numpy()
+    p = o.PassParams(budget_tokens=256, n_sink=4, n_recent=32, renumber=True)
+    for u in range(w.n_units):
+        k, v, q, pos = _unit_np(x, w, u)
+        r = o.run_unit(k, v, q, pos, p, cos, sin)
+        pool = r.pools[o.ACT_BF16]
+        assert r.status == o.UNIT_OK and pool.idx.size == 256
+        assert set(range(4)) <= set(pool.idx) and set(range(1024 - 32, 1024)) <= set(pool.idx)
+        assert np.array_equal(pool.pos, np.arange(256))
+        # the kept non-window rows are exactly the 220 best by score
+        rest = np.setdiff1d(np.arange(4, 1024 - 32), pool.idx)
+        assert r.scores[np.setdiff1d(pool.idx, list(range(4)) + list(range(992, 1024)))].min() \
+            >= r.scores[rest].max()
+        np.testing.assert_array_equal(pool.v, v[pool.idx])
