@@ -1,0 +1,386 @@
+"""Benchmark of the budgeted KV-cache compaction pass on GB300.
+
+One step = one full compaction pass (kvc_score -> kvc_select ->
+kvc_compact_rerotate_quant) over every (layer, KV head) unit of the
+Qwen3-8B-shaped single-session workload: 36 layers x 8 KV heads, 32 query
+heads, head_dim 128, T = 32,768 cached tokens, window 64, budget 2,048
+(4 sinks + 128 recent + top-k), bounded positions (renumber + re-rotation),
+foresight bonus on 4 spans.  Inputs are seeded synthetic tensors.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  Multi-GPU (torchrun, one rank per GPU): every rank
+compacts its own session of the same shape (weak scaling, no collective on
+the data path); the timed region is bracketed by barriers and the slowest
+rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or TC util)"
+UNIT = "tokens/s (summed over layer x KV-head units)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(w, kept_per_unit: int) -> dict:
+    """Bytes the method must move once per pass (counted per stage)."""
+    U, T, d, R = w.n_units, w.n_tokens, w.head_dim, w.rows_per_unit
+    score = U * T * 2 * d + U * R * 2 * d + U * T * 4 + (w.batch * T * 4 if w.bonus_spans else 0)
+    select = U * T * 4 + 3 * U * kept_per_unit * 4
+    row_io = 2 * 2 * d                                  # K and V row, bf16
+    compact = U * kept_per_unit * (row_io + row_io + 4 + 4 + 4 + 4)
+    if w.renumber:
+        compact += min(w.max_pos, T) * d * 4            # cos + sin rows touched (fp32, d/2 each)
+    return dict(score=score, select=select, compact=compact, total=score + select + compact)
+
+
+def algorithmic_flops(w) -> int:
+    return 2 * w.n_units * w.rows_per_unit * w.n_tokens * w.head_dim
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(w, x_host, seconds: float, max_units: int):
+    """Time the CPU oracle (score + select + compact) on whole units until `seconds` pass."""
+    import oracle as o
+    cos, sin = x_host["rope_cos"].numpy(), x_host["rope_sin"].numpy()
+    prm = o.PassParams(budget_tokens=w.budget_tokens, budget_bytes=w.budget_bytes,
+                       n_sink=w.n_sink, n_recent=w.n_recent, page_size=w.page_size,
+                       renumber=w.renumber, quant_mode=w.quant_mode,
+                       n_layer_groups=w.n_layer_groups)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    done, t0 = 0, time.perf_counter()
+    rng = np.random.default_rng(0)
+    units = rng.permutation(w.n_units)
+    while done < max_units:
+        u = int(units[done % w.n_units])
+        b, l, g = wl.unit_coords(w, u)
+        G = w.group
+        o.run_unit(bits(x_host["k_cache"][b, l, g]), bits(x_host["v_cache"][b, l, g]),
+                   bits(x_host["q_window"][b, l, g * G:(g + 1) * G]), x_host["pos_in"][u].numpy(),
+                   prm, cos, sin, bonus=x_host["bonus"][b].numpy() if "bonus" in x_host else None)
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:       # BLAS uses every host core by default
+        threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return done, dt, threads
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    # the oracle's own inputs: a one-layer, one-KV-head slice of the workload
+    ws = w.replace(n_layers=1, n_kv_heads=1, n_q_heads=w.group)
+    x = wl.make_inputs(ws, device="cpu")
+    per_step = []
+    n_rows = 0
+    threads = 1
+    for step in range(args.warmup + args.steps):
+        done, dt, threads = oracle_sample(ws, x, seconds=0.0, max_units=1)
+        if step >= args.warmup:
+            per_step.append(dt)
+            n_rows += done * ws.n_tokens
+    total = sum(per_step)
+    value = n_rows / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "units_per_step": 1, "n_tokens": w.n_tokens,
+                   "budget": w.budget_tokens, "window": w.window, "head_dim": w.head_dim},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"1 of {w.n_units} (layer, KV head) units per step, "
+                                   f"score+select+compact, numpy fp64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w, world, rank, local):
+    import budgeted_kv_cache_gb300 as kvc
+    from budgeted_kv_cache_gb300 import build
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    if rank == 0 or not os.path.exists(build.LIB):
+        build.build()
+    barrier(world)
+    kvc.library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    # each rank compacts its own session (different seed)
+    wr = w.replace(seed=w.seed + 1000 * rank)
+    x = wl.make_inputs(wr, device=dev)
+    p = pass_for_workload(wr, inputs=x, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"],
+              x["rope_sin"], x.get("bonus"), stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(p.unit_status.abs().sum()) == 0 and int(p.score_status.abs().sum()) == 0
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    marks = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.fill_(float(s))                     # L2 flush outside the timed events
+        m = marks[s]
+        m[0].record(stream)
+        p.score(x["k_cache"], x["q_window"], x.get("bonus"), stream=stream)
+        m[1].record(stream)
+        p.select(stream=stream)
+        m[2].record(stream)
+        p.compact(x["k_cache"], x["v_cache"], x["pos_in"], x["rope_cos"], x["rope_sin"],
+                  stream=stream)
+        m[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    t_score = [m[0].elapsed_time(m[1]) for m in marks]
+    t_select = [m[1].elapsed_time(m[2]) for m in marks]
+    t_compact = [m[2].elapsed_time(m[3]) for m in marks]
+    t_pass = [a + b + c for a, b, c in zip(t_score, t_select, t_compact)]
+    total_ms = max_over_ranks(sum(t_pass), world)
+
+    # decode step, timed separately (consumer check, not part of the pass)
+    d0, d1 = ev(), ev()
+    d0.record(stream)
+    p.decode(x["q_decode"], stream=stream)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    t_decode = d0.elapsed_time(d1)
+
+    # end to end through the C-ABI with host buffers: pinned host inputs are
+    # copied in, the pass runs, the compacted cache comes back, every step
+    e2e = None
+    if not args.no_e2e:
+        names = ["k_cache", "v_cache", "q_window", "pos_in", "rope_cos", "rope_sin", "bonus"]
+        host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
+        for n in names:
+            host[n].copy_(x[n])
+        dev_in = {n: torch.empty_like(x[n]) for n in names}
+        outs = [p.pools.k_bf16, p.pools.v_bf16, p.pools.pos_out, p.kept_idx, p.kept_count,
+                p.unit_status]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+
+        def e2e_step():
+            for n in names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            p.run(dev_in["k_cache"], dev_in["v_cache"], dev_in["q_window"], dev_in["pos_in"],
+                  dev_in["rope_cos"], dev_in["rope_sin"], dev_in["bonus"], stream=stream)
+            for h, t in zip(host_out, outs):
+                h.copy_(t, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(1, min(args.steps, 5))
+        barrier(world)
+        e0, e1 = ev(), ev()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
+        e2e = {"value": world * wr.n_units * wr.n_tokens / (t_e2e * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e,
+               "steps": n_e2e}
+        del host, dev_in, host_out
+
+    if rank != 0:
+        return
+    hbm, tc, src = _peaks()
+    kept = wr.budget_tokens
+    ab = algorithmic_bytes(wr, kept)
+    flops = algorithmic_flops(wr)
+    ms_step = total_ms / args.steps
+    score_ms = statistics.mean(t_score)
+    achieved = ab["score"] / (score_ms * 1e-3) / 1e9
+    t_roof = max(ab["total"] / (hbm * 1e9), flops / (tc * 1e12))
+    value = world * wr.n_units * wr.n_tokens / (ms_step * 1e-3)
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        ws = wr.replace(n_layers=1, n_kv_heads=1, n_q_heads=wr.group)
+        xh = wl.make_inputs(ws, device="cpu")
+        done, dt, threads = oracle_sample(ws, xh, seconds=args.cpu_seconds, max_units=64)
+        cpu = {"value": done * ws.n_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{done} whole (layer, KV head) unit(s) of {wr.name} "
+                         f"(score+select+compact, numpy fp64), {dt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wr.name, "units": wr.n_units, "n_tokens": wr.n_tokens,
+                   "budget": wr.budget_tokens, "window": wr.window, "head_dim": wr.head_dim,
+                   "q_heads": wr.n_q_heads, "kv_heads": wr.n_kv_heads, "layers": wr.n_layers,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "256 MiB buffer written between timed steps; K/V inputs (2.4 GB each) exceed L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "kernel": "score_kernel",
+                     "peak_source": src,
+                     "algorithmic_bytes_per_launch": ab["score"],
+                     "tc_tflops_algorithmic": flops / (score_ms * 1e-3) / 1e12},
+        "stages_ms": {"score": score_ms, "select": statistics.mean(t_select),
+                      "compact": statistics.mean(t_compact), "decode": t_decode},
+        "pass_roofline": {"t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step,
+                          "algorithmic_bytes": ab["total"], "algorithmic_flops": flops},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 3 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.qwen3_8b_32k().name, choices=sorted(wl.ALL))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+    w = wl.ALL[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+    else:
+        run_gpu(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+"""Python binding of libkvc (budgeted KV-cache compaction on GB300).
+
+Argument marshalling only: every function here forwards to the C-ABI entry
+point of the same name in libkvc.so (declared in include/kvc.h), passing
+device pointers of torch tensors and the current CUDA stream.  There is no
+fallback: if the library is missing or a call fails, a KvcError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+KVC_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+                3: "workspace missing or too small", 4: "CUDA error", 5: "no usable sm_103 device"}
+UNIT_OK, UNIT_OVER_BUDGET, UNIT_BAD_INDEX, UNIT_BAD_FLAGS, UNIT_TIMEOUT = 0, 1, 2, 3, 4
+ACT_RELEASE, ACT_INT4, ACT_INT8, ACT_BF16 = 0, 1, 2, 3
+POOL_INT4, POOL_INT8, POOL_BF16, N_POOLS = 0, 1, 2, 3
+FLAG_PROTECT, FLAG_EXCLUDE = 1, 2
+QUANT_G32_BF16, QUANT_ROW_FP16 = 0, 1
+SCORE_ACCUMULATE = 1
+
+
+class KvcError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)} ({code})")
+        self.code = code
+
+
+class kvc_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_tokens", ctypes.c_int64)]
+
+
+class kvc_policy(ctypes.Structure):
+    _fields_ = [("budget_tokens", ctypes.c_int32), ("budget_bytes", ctypes.c_int64),
+                ("n_sink", ctypes.c_int32), ("n_recent", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("renumber", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("quant_mode", ctypes.c_int32),
+                ("n_tags", ctypes.c_int32), ("n_layer_groups", ctypes.c_int32),
+                ("flags", ctypes.c_void_p), ("tags", ctypes.c_void_p),
+                ("action_table", ctypes.c_void_p)]
+
+
+class kvc_pools(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "k_bf16", "v_bf16", "k_i8", "v_i8", "k_i8_scale", "v_i8_scale",
+        "k_i4", "v_i4", "k_i4_scale", "v_i4_scale", "pos_out", "orig_pos_out")]
+
+
+_LIB = None
+
+
+def _load():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise KvcError("load libkvc.so (not built: run budgeted_kv_cache_gb300.build.build())", -1)
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, U32, F32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                     ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t)
+        SH, PO, PL = ctypes.POINTER(kvc_shape), ctypes.POINTER(kvc_policy), ctypes.POINTER(kvc_pools)
+        sig = {
+            "kvc_score_workspace_bytes": (SZ, [SH, I32]),
+            "kvc_score": (ctypes.c_int, [SH, P, P, I32, F32, P, I32, U32, P, P, P, P, SZ, P]),
+            "kvc_select_workspace_bytes": (SZ, [SH, PO]),
+            "kvc_select": (ctypes.c_int, [SH, PO, P, P, P, P, P, P, SZ, P]),
+            "kvc_compact_rerotate_quant": (ctypes.c_int, [SH, PO, P, P, P, P, P, P, P, I64, PL, P, P]),
+            "kvc_decode_workspace_bytes": (SZ, [SH, PO]),
+            "kvc_decode_attn": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P, SZ, P]),
+            "kvc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype, f.argtypes = res, args
+        _LIB = lib
+    return _LIB
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libkvc.so (raises KvcError if it is not built)."""
+    return _load()
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, code: int):
+    if code != KVC_OK:
+        raise KvcError(fn, code)
+
+
+# ----------------------------------------------------------------------------- structs
+
+def make_shape(batch, n_layers, n_q_heads, n_kv_heads, head_dim, n_tokens) -> kvc_shape:
+    return kvc_shape(batch, n_layers, n_q_heads, n_kv_heads, head_dim, n_tokens)
+
+
+@dataclasses.dataclass
+class Policy:
+    budget_tokens: int = 0
+    budget_bytes: int = 0
+    n_sink: int = 4
+    n_recent: int = 32
+    page_size: int = 1
+    renumber: bool = True
+    capacity: int = 0
+    quant_mode: int = QUANT_G32_BF16
+    n_tags: int = 0
+    n_layer_groups: int = 1
+    flags: Optional[torch.Tensor] = None
+    tags: Optional[torch.Tensor] = None
+    action_table: Optional[torch.Tensor] = None
+
+    def c(self) -> kvc_policy:
+        return kvc_policy(self.budget_tokens, self.budget_bytes, self.n_sink, self.n_recent,
+                          self.page_size, int(bool(self.renumber)), self.capacity, self.quant_mode,
+                          self.n_tags, self.n_layer_groups, _p(self.flags), _p(self.tags),
+                          _p(self.action_table))
+
+    @property
+    def byte_mode(self) -> bool:
+        return self.budget_bytes > 0
+
+
+@dataclasses.dataclass
+class Pools:
+    """Output arrays of kvc_compact_rerotate_quant (torch tensors)."""
+    k_bf16: torch.Tensor
+    v_bf16: torch.Tensor
+    pos_out: torch.Tensor
+    orig_pos_out: Optional[torch.Tensor] = None
+    k_i8: Optional[torch.Tensor] = None
+    v_i8: Optional[torch.Tensor] = None
+    k_i8_scale: Optional[torch.Tensor] = None
+    v_i8_scale: Optional[torch.Tensor] = None
+    k_i4: Optional[torch.Tensor] = None
+    v_i4: Optional[torch.Tensor] = None
+    k_i4_scale: Optional[torch.Tensor] = None
+    v_i4_scale: Optional[torch.Tensor] = None
+
+    def c(self) -> kvc_pools:
+        return kvc_pools(*[_p(getattr(self, n)) for n, _ in kvc_pools._fields_])
+
+    @staticmethod
+    def allocate(shape: kvc_shape, policy: Policy, device="cuda", orig_pos: bool = True) -> "Pools":
+        U = shape.batch * shape.n_layers * shape.n_kv_heads
+        cap, d = policy.capacity, shape.head_dim
+        e = lambda *s, dt: torch.empty(s, dtype=dt, device=device)
+        p = Pools(k_bf16=e(U, cap, d, dt=torch.bfloat16), v_bf16=e(U, cap, d, dt=torch.bfloat16),
+                  pos_out=e(N_POOLS, U, cap, dt=torch.int32),
+                  orig_pos_out=e(N_POOLS, U, cap, dt=torch.int32) if orig_pos else None)
+        if policy.byte_mode:
+            ns = d // 32 if policy.quant_mode == QUANT_G32_BF16 else 1
+            sdt = torch.bfloat16 if policy.quant_mode == QUANT_G32_BF16 else torch.float16
+            p.k_i8, p.v_i8 = e(U, cap, d, dt=torch.int8), e(U, cap, d, dt=torch.int8)
+            p.k_i4, p.v_i4 = e(U, cap, d // 2, dt=torch.uint8), e(U, cap, d // 2, dt=torch.uint8)
+            p.k_i8_scale, p.v_i8_scale = e(U, cap, ns, dt=sdt), e(U, cap, ns, dt=sdt)
+            p.k_i4_scale, p.v_i4_scale = e(U, cap, ns, dt=sdt), e(U, cap, ns, dt=sdt)
+        return p
+
+
+# ----------------------------------------------------------------------------- entry points
+
+def kvc_status_string(code: int) -> str:
+    return _load().kvc_status_string(code).decode()
+
+
+def kvc_score_workspace_bytes(shape: kvc_shape, window: int) -> int:
+    return _load().kvc_score_workspace_bytes(ctypes.byref(shape), window)
+
+
+def kvc_score(shape, k_cache, q_window, window, softmax_scale, bonus, page_size, flags, scores,
+              page_scores, unit_status, workspace, workspace_bytes=None, stream=None):
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check("kvc_score", _load().kvc_score(
+        ctypes.byref(shape), _p(k_cache), _p(q_window), window, float(softmax_scale), _p(bonus),
+        page_size, flags, _p(scores), _p(page_scores), _p(unit_status), _p(workspace), wb,
+        _stream(stream)))
+
+
+def kvc_select_workspace_bytes(shape: kvc_shape, policy: Policy) -> int:
+    cp = policy.c()
+    return _load().kvc_select_workspace_bytes(ctypes.byref(shape), ctypes.byref(cp))
+
+
+def kvc_select(shape, policy: Policy, scores, kept_idx, kept_count, unit_status, floor_excess=None,
+               workspace=None, workspace_bytes=0, stream=None):
+    cp = policy.c()
+    _check("kvc_select", _load().kvc_select(
+        ctypes.byref(shape), ctypes.byref(cp), _p(scores), _p(kept_idx), _p(kept_count),
+        _p(unit_status), _p(floor_excess), _p(workspace), workspace_bytes, _stream(stream)))
+
+
+def kvc_compact_rerotate_quant(shape, policy: Policy, k_cache, v_cache, pos_in, kept_idx,
+                               kept_count, rope_cos, rope_sin, rope_max_pos, pools: Pools,
+                               unit_status=None, stream=None):
+    cp, cpools = policy.c(), pools.c()
+    _check("kvc_compact_rerotate_quant", _load().kvc_compact_rerotate_quant(
+        ctypes.byref(shape), ctypes.byref(cp), _p(k_cache), _p(v_cache), _p(pos_in),
+        _p(kept_idx), _p(kept_count), _p(rope_cos), _p(rope_sin), int(rope_max_pos),
+        ctypes.byref(cpools), _p(unit_status), _stream(stream)))
+
+
+def kvc_decode_workspace_bytes(shape, policy: Policy) -> int:
+    cp = policy.c()
+    return _load().kvc_decode_workspace_bytes(ctypes.byref(shape), ctypes.byref(cp))
+
+
+def kvc_decode_attn(shape, policy: Policy, q, pools: Pools, kept_count, softmax_scale, out,
+                    workspace=None, workspace_bytes=None, stream=None):
+    cp, cpools = policy.c(), pools.c()
+    wb = 0 if workspace is None else (workspace.numel() * workspace.element_size()
+                                      if workspace_bytes is None else workspace_bytes)
+    _check("kvc_decode_attn", _load().kvc_decode_attn(
+        ctypes.byref(shape), ctypes.byref(cp), _p(q), ctypes.byref(cpools), _p(kept_count),
+        float(softmax_scale), _p(out), _p(workspace), wb, _stream(stream)))

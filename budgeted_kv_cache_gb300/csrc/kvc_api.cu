@@ -1,0 +1,449 @@
+// C-ABI entry points of libkvc: argument validation, launch configuration,
+// tensor-map encoding and workspace layout.  Every step of the pass runs in
+// the kernels of score_tc.cu, select.cu, compact.cu and decode.cu.
+#include <math.h>
+#include <stdlib.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kvc_internal.cuh"
+
+using namespace kvc;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DevInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+  bool ok = false;
+};
+
+// Properties of the current device, cached per device ordinal.
+bool device_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  static DevInfo cache[64];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev].ok) {
+    DevInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return false;
+    d.ok = true;
+    cache[dev] = d;
+  }
+  *out = cache[dev];
+  return true;
+}
+
+kvc_status check_device(DevInfo* info) {
+  if (!device_info(info)) return KVC_ERR_NO_DEVICE;
+  if (info->major != 10 || info->minor != 3) return KVC_ERR_NO_DEVICE;   // built for sm_103a only
+  return KVC_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kvc_status check_shape(const kvc_shape* s) {
+  if (!s) return KVC_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->n_layers < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1) return KVC_ERR_INVALID_ARG;
+  if (s->n_q_heads % s->n_kv_heads) return KVC_ERR_INVALID_ARG;
+  if (s->n_tokens < 1 || s->n_tokens > 0x7fffffffLL) return KVC_ERR_INVALID_ARG;
+  if (s->head_dim != 64 && s->head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  const int64_t units = static_cast<int64_t>(s->batch) * s->n_layers * s->n_kv_heads;
+  if (units > (1 << 24)) return KVC_ERR_UNSUPPORTED;
+  return KVC_OK;
+}
+
+int64_t n_units(const kvc_shape* s) {
+  return static_cast<int64_t>(s->batch) * s->n_layers * s->n_kv_heads;
+}
+
+// ---------------------------------------------------------------- scoring plan
+struct ScorePlan {
+  int grid = 0;
+  int n_tiles = 0, chunk_tiles = 0, S = 0;
+  int R = 0, q_rows = 0, n_stages = 0;
+  size_t smem = 0;
+  size_t ws_counters = 0, ws_stats = 0, ws_total = 0;
+};
+
+kvc_status plan_score(const kvc_shape* s, int32_t window, ScorePlan* p) {
+  kvc_status st = check_shape(s);
+  if (st != KVC_OK) return st;
+  if (window < 1 || window > s->n_tokens) return KVC_ERR_INVALID_ARG;
+  const int G = s->n_q_heads / s->n_kv_heads;
+  const int64_t R = static_cast<int64_t>(window) * G;
+  if (R % 32 != 0 || R > 256) return KVC_ERR_UNSUPPORTED;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  p->grid = info.sms;
+  p->R = static_cast<int>(R);
+  p->n_tiles = static_cast<int>((s->n_tokens + kTileTokens - 1) / kTileTokens);
+  int chunk = 16;
+  if (const char* e = getenv("KVC_SCORE_CHUNK_TILES")) {
+    const int v = atoi(e);
+    if (v >= 1 && v <= 1 << 20) chunk = v;
+  }
+  chunk = std::max(chunk, (p->n_tiles + p->grid - 1) / p->grid);   // S <= grid (co-resident unit)
+  p->chunk_tiles = std::min(chunk, p->n_tiles);
+  p->S = (p->n_tiles + p->chunk_tiles - 1) / p->chunk_tiles;
+  const int64_t items = n_units(s) * p->S;
+  if (items > 0x7fffffffLL) return KVC_ERR_UNSUPPORTED;
+  p->q_rows = static_cast<int>((R + 127) / 128 * 128);
+  const size_t max_smem = 232448;       // 227 KB per block on sm_103
+  const size_t stage = static_cast<size_t>(s->head_dim / 64) * 128 * 128;
+  const size_t fixed = score_smem_bytes(s->head_dim, p->q_rows, 0);
+  int stages = static_cast<int>((max_smem - fixed - 16 * 8) / (stage + 16));
+  stages = std::min(stages, 8);
+  if (stages < 2) return KVC_ERR_UNSUPPORTED;
+  p->n_stages = stages;
+  // at least 120 KB so that exactly one CTA (and one 512-column TMEM
+  // allocation) lives on each SM
+  p->smem = std::max(score_smem_bytes(s->head_dim, p->q_rows, stages), static_cast<size_t>(120 * 1024));
+  p->ws_counters = (static_cast<size_t>(n_units(s)) * 4 + 255) / 256 * 256;
+  p->ws_stats = static_cast<size_t>(items) * R * sizeof(float2);
+  p->ws_total = p->ws_counters + (p->ws_stats + 255) / 256 * 256;
+  return KVC_OK;
+}
+
+kvc_status encode_3d(CUtensorMap* map, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                     uint32_t b0, uint32_t b1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KVC_ERR_CUDA;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KVC_OK : KVC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- policy checks
+struct SelectPlan {
+  bool byte_mode = false;
+  int P = 1;
+  int64_t n_items = 0;
+  int sink_items = 0, recent_items = 0;
+  int budget_items = 0;
+};
+
+kvc_status plan_select(const kvc_shape* s, const kvc_policy* pol, SelectPlan* sp) {
+  kvc_status st = check_shape(s);
+  if (st != KVC_OK) return st;
+  if (!pol) return KVC_ERR_INVALID_ARG;
+  const bool tok = pol->budget_tokens > 0, byt = pol->budget_bytes > 0;
+  if (tok == byt) return KVC_ERR_INVALID_ARG;                  // exactly one budget
+  if (pol->budget_tokens < 0 || pol->budget_bytes < 0) return KVC_ERR_INVALID_ARG;
+  if (pol->n_sink < 0 || pol->n_recent < 0) return KVC_ERR_INVALID_ARG;
+  if (pol->quant_mode != KVC_QUANT_G32_BF16 && pol->quant_mode != KVC_QUANT_ROW_FP16)
+    return KVC_ERR_INVALID_ARG;
+  if (pol->renumber != 0 && pol->renumber != 1) return KVC_ERR_INVALID_ARG;
+  const int64_t T = s->n_tokens;
+  const int P = pol->page_size;
+  if (P < 1 || P > 32 || (P & (P - 1))) return KVC_ERR_INVALID_ARG;
+  sp->byte_mode = byt;
+  sp->P = P;
+  if (byt) {
+    if (P != 1) return KVC_ERR_UNSUPPORTED;
+    if (!pol->tags || !pol->action_table || pol->n_tags < 1 || pol->n_layer_groups < 1 ||
+        pol->n_layer_groups > s->n_layers)
+      return KVC_ERR_INVALID_ARG;
+    if (pol->capacity < T) return KVC_ERR_INVALID_ARG;
+    if (T * 4 * s->head_dim >= (1LL << 32)) return KVC_ERR_UNSUPPORTED;
+    sp->n_items = T;
+    sp->sink_items = static_cast<int>(std::min<int64_t>(pol->n_sink, T));
+    sp->recent_items = static_cast<int>(std::min<int64_t>(pol->n_recent, T));
+  } else {
+    if (pol->capacity < pol->budget_tokens) return KVC_ERR_INVALID_ARG;
+    if (P > 1 && (T % P != 0 || pol->budget_tokens % P != 0)) return KVC_ERR_INVALID_ARG;
+    sp->n_items = T / P;
+    sp->budget_items = pol->budget_tokens / P;
+    if (P == 1) {
+      sp->sink_items = static_cast<int>(std::min<int64_t>(pol->n_sink, T));
+      sp->recent_items = static_cast<int>(std::min<int64_t>(pol->n_recent, T));
+    } else {
+      const int64_t first = (static_cast<int64_t>(pol->n_sink) + P - 1) / P;
+      const int64_t rstart = std::max<int64_t>(0, T - pol->n_recent) / P;
+      sp->sink_items = static_cast<int>(std::min<int64_t>(first, sp->n_items));
+      sp->recent_items = static_cast<int>(sp->n_items - rstart);
+    }
+  }
+  if (pol->capacity < 1 && (pol->budget_tokens > 0 || byt)) return KVC_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(KVC_N_POOLS) * n_units(s) * pol->capacity > (1LL << 40)) return KVC_ERR_UNSUPPORTED;
+  return KVC_OK;
+}
+
+int decode_splits(const kvc_shape* s, const kvc_policy* pol, int sms) {
+  const int64_t U = n_units(s);
+  const int64_t rows = static_cast<int64_t>(pol->capacity) * (pol->budget_bytes > 0 ? 3 : 1);
+  int64_t want = (2LL * sms + U - 1) / U;
+  const int64_t most = std::max<int64_t>(1, (rows + 255) / 256);
+  want = std::min<int64_t>(std::min<int64_t>(want, most), 32);
+  return static_cast<int>(std::max<int64_t>(want, 1));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvc_status_string(kvc_status status) {
+  switch (status) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID_ARG: return "invalid argument";
+    case KVC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVC_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVC_ERR_CUDA: return "CUDA error";
+    case KVC_ERR_NO_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+size_t kvc_score_workspace_bytes(const kvc_shape* shape, int32_t window) {
+  ScorePlan p;
+  if (plan_score(shape, window, &p) != KVC_OK) return 0;
+  return p.ws_total;
+}
+
+kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_window,
+                     int32_t window, float softmax_scale, const float* bonus, int32_t page_size,
+                     uint32_t flags, float* scores, float* page_scores, int32_t* unit_status,
+                     void* workspace, size_t workspace_bytes, kvc_stream stream) {
+  ScorePlan p;
+  kvc_status st = plan_score(shape, window, &p);
+  if (st != KVC_OK) return st;
+  if (!k_cache || !q_window || !scores) return KVC_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(q_window, 16)) return KVC_ERR_INVALID_ARG;
+  if (flags & ~static_cast<uint32_t>(KVC_SCORE_ACCUMULATE)) return KVC_ERR_INVALID_ARG;
+  if (page_size < 1 || page_size > 32 || (page_size & (page_size - 1))) return KVC_ERR_INVALID_ARG;
+  if (page_size > 1 && (shape->n_tokens % page_size != 0 || !page_scores)) return KVC_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < p.ws_total || !aligned(workspace, 256)) return KVC_ERR_WORKSPACE;
+  if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / sqrtf(static_cast<float>(shape->head_dim));
+
+  ScoreArgs a = {};
+  a.U = static_cast<int32_t>(n_units(shape));
+  a.L = shape->n_layers;
+  a.Hkv = shape->n_kv_heads;
+  a.B = shape->batch;
+  a.T = shape->n_tokens;
+  a.d = shape->head_dim;
+  a.W = window;
+  a.G = shape->n_q_heads / shape->n_kv_heads;
+  a.R = p.R;
+  a.n_tiles = p.n_tiles;
+  a.chunk_tiles = p.chunk_tiles;
+  a.items_per_unit = p.S;
+  a.n_items = a.U * p.S;
+  a.page_size = page_size;
+  a.accumulate = (flags & KVC_SCORE_ACCUMULATE) ? 1 : 0;
+  a.n_stages = p.n_stages;
+  a.q_rows = p.q_rows;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.bonus = bonus;
+  a.scores = scores;
+  a.page_scores = page_size > 1 ? page_scores : nullptr;
+  a.unit_status = unit_status;
+  a.counters = static_cast<uint32_t*>(workspace);
+  a.stats = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + p.ws_counters);
+
+  CUtensorMap mk, mq;
+  if ((st = encode_3d(&mk, k_cache, shape->head_dim, shape->n_tokens, a.U, 64, kTileTokens)) != KVC_OK)
+    return st;
+  if ((st = encode_3d(&mq, q_window, shape->head_dim, p.R, a.U, 64, p.R)) != KVC_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(a.counters, 0, p.ws_counters, s) != cudaSuccess) return KVC_ERR_CUDA;
+  if (launch_score(a, mk, mq, p.grid, p.smem, s) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+size_t kvc_select_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy) {
+  (void)shape;
+  (void)policy;
+  return 0;
+}
+
+kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const float* scores,
+                      int32_t* kept_idx, int32_t* kept_count, int32_t* unit_status,
+                      int64_t* floor_excess, void* workspace, size_t workspace_bytes,
+                      kvc_stream stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  SelectPlan sp;
+  kvc_status st = plan_select(shape, policy, &sp);
+  if (st != KVC_OK) return st;
+  if (!scores || !kept_idx || !kept_count || !unit_status) return KVC_ERR_INVALID_ARG;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  SelectArgs a = {};
+  a.U = static_cast<int32_t>(n_units(shape));
+  a.L = shape->n_layers;
+  a.Hkv = shape->n_kv_heads;
+  a.B = shape->batch;
+  a.T = shape->n_tokens;
+  a.d = shape->head_dim;
+  a.n_items = sp.n_items;
+  a.page_size = sp.P;
+  a.budget_items = sp.budget_items;
+  a.budget_bytes = policy->budget_bytes;
+  a.sink_items = sp.sink_items;
+  a.recent_items = sp.recent_items;
+  a.capacity = policy->capacity;
+  a.byte_mode = sp.byte_mode ? 1 : 0;
+  a.quant_mode = policy->quant_mode;
+  a.n_tags = policy->n_tags;
+  a.n_groups = policy->n_layer_groups;
+  a.flags = policy->flags;
+  a.tags = policy->tags;
+  a.table = policy->action_table;
+  a.scores = scores;
+  a.kept_idx = kept_idx;
+  a.kept_count = kept_count;
+  a.unit_status = unit_status;
+  a.floor_excess = floor_excess;
+  const size_t cache_bytes = static_cast<size_t>(sp.n_items) * 5;
+  a.cache_items = cache_bytes <= 200 * 1024 ? 1 : 0;
+  const size_t smem = a.cache_items ? (cache_bytes + 15) / 16 * 16 : 0;
+  if (launch_select(a, static_cast<cudaStream_t>(stream), smem) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+kvc_status kvc_compact_rerotate_quant(const kvc_shape* shape, const kvc_policy* policy,
+                                      const void* k_cache, const void* v_cache,
+                                      const int32_t* pos_in, const int32_t* kept_idx,
+                                      const int32_t* kept_count, const float* rope_cos,
+                                      const float* rope_sin, int64_t rope_max_pos,
+                                      const kvc_pools* pools, int32_t* unit_status,
+                                      kvc_stream stream) {
+  SelectPlan sp;
+  kvc_status st = plan_select(shape, policy, &sp);
+  if (st != KVC_OK) return st;
+  if (!k_cache || !v_cache || !pos_in || !kept_idx || !kept_count || !pools || !pools->pos_out)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return KVC_ERR_INVALID_ARG;
+  if (policy->renumber) {
+    if (!rope_cos || !rope_sin || rope_max_pos < 1) return KVC_ERR_INVALID_ARG;
+    if (!aligned(rope_cos, 16) || !aligned(rope_sin, 16)) return KVC_ERR_INVALID_ARG;
+    if (rope_max_pos < policy->capacity) return KVC_ERR_INVALID_ARG;
+  }
+  if (!pools->k_bf16 || !pools->v_bf16 || !aligned(pools->k_bf16, 16) || !aligned(pools->v_bf16, 16))
+    return KVC_ERR_INVALID_ARG;
+  if (sp.byte_mode) {
+    const void* need[8] = {pools->k_i8, pools->v_i8, pools->k_i8_scale, pools->v_i8_scale,
+                           pools->k_i4, pools->v_i4, pools->k_i4_scale, pools->v_i4_scale};
+    for (const void* q : need)
+      if (!q) return KVC_ERR_INVALID_ARG;
+    if (!aligned(pools->k_i8, 8) || !aligned(pools->v_i8, 8) || !aligned(pools->k_i4, 4) ||
+        !aligned(pools->v_i4, 4))
+      return KVC_ERR_INVALID_ARG;
+  }
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  CompactArgs a = {};
+  a.U = static_cast<int32_t>(n_units(shape));
+  a.d = shape->head_dim;
+  a.T = shape->n_tokens;
+  a.capacity = policy->capacity;
+  a.renumber = policy->renumber;
+  a.quant_mode = policy->quant_mode;
+  a.rope_max_pos = rope_max_pos;
+  a.k = static_cast<const __nv_bfloat16*>(k_cache);
+  a.v = static_cast<const __nv_bfloat16*>(v_cache);
+  a.pos_in = pos_in;
+  a.kept_idx = kept_idx;
+  a.kept_count = kept_count;
+  a.cos = rope_cos;
+  a.sin = rope_sin;
+  a.pools = *pools;
+  a.unit_status = unit_status;
+  a.pool_lo = sp.byte_mode ? KVC_POOL_INT4 : KVC_POOL_BF16;
+  a.pool_hi = KVC_N_POOLS;
+  if (launch_compact(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+size_t kvc_decode_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy) {
+  SelectPlan sp;
+  if (plan_select(shape, policy, &sp) != KVC_OK) return 0;
+  DevInfo info;
+  if (check_device(&info) != KVC_OK) return 0;
+  const int splits = decode_splits(shape, policy, info.sms);
+  if (splits == 1) return 0;
+  const int G = shape->n_q_heads / shape->n_kv_heads;
+  const size_t slots = static_cast<size_t>(n_units(shape)) * splits * G;
+  const size_t ml = (slots * 2 * sizeof(float) + 255) / 256 * 256;
+  return ml + slots * shape->head_dim * sizeof(float);
+}
+
+kvc_status kvc_decode_attn(const kvc_shape* shape, const kvc_policy* policy, const void* q,
+                           const kvc_pools* pools, const int32_t* kept_count, float softmax_scale,
+                           void* out, void* workspace, size_t workspace_bytes, kvc_stream stream) {
+  SelectPlan sp;
+  kvc_status st = plan_select(shape, policy, &sp);
+  if (st != KVC_OK) return st;
+  if (!q || !pools || !kept_count || !out) return KVC_ERR_INVALID_ARG;
+  const int G = shape->n_q_heads / shape->n_kv_heads;
+  if (G > 8) return KVC_ERR_UNSUPPORTED;
+  if (!pools->k_bf16 || !pools->v_bf16) return KVC_ERR_INVALID_ARG;
+  if (sp.byte_mode && (!pools->k_i8 || !pools->v_i8 || !pools->k_i4 || !pools->v_i4 ||
+                       !pools->k_i8_scale || !pools->v_i8_scale || !pools->k_i4_scale ||
+                       !pools->v_i4_scale))
+    return KVC_ERR_INVALID_ARG;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  const int splits = decode_splits(shape, policy, info.sms);
+  const size_t need = kvc_decode_workspace_bytes(shape, policy);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+    return KVC_ERR_WORKSPACE;
+  if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / sqrtf(static_cast<float>(shape->head_dim));
+  DecodeArgs a = {};
+  a.U = static_cast<int32_t>(n_units(shape));
+  a.G = G;
+  a.d = shape->head_dim;
+  a.Hkv = shape->n_kv_heads;
+  a.L = shape->n_layers;
+  a.B = shape->batch;
+  a.capacity = policy->capacity;
+  a.quant_mode = policy->quant_mode;
+  a.splits = splits;
+  a.scale = softmax_scale;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.pools = *pools;
+  a.kept_count = kept_count;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  if (splits > 1) {
+    const size_t slots = static_cast<size_t>(a.U) * splits * G;
+    const size_t ml = (slots * 2 * sizeof(float) + 255) / 256 * 256;
+    a.ws_ml = static_cast<float*>(workspace);
+    a.ws_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ml);
+  }
+  a.pool_lo = sp.byte_mode ? KVC_POOL_INT4 : KVC_POOL_BF16;
+  a.pool_hi = KVC_N_POOLS;
+  if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,278 @@
+/*
+ * libkvc -- budgeted KV-cache compaction on one GB300 (sm_103a).
+ *
+ * One compaction pass over a KV cache, per unit u = (sequence b, layer l,
+ * KV head g), units ordered [B][L][H_kv]:
+ *
+ *   kvc_score                   window-attention mass of every cached token
+ *                               (+ bonus, optional page max)
+ *   kvc_select                  deterministic budgeted selection
+ *   kvc_compact_rerotate_quant  gather kept K/V rows, re-rotate kept keys to
+ *                               their new positions, quantise, store
+ *   kvc_decode_attn             one decode-attention step over the result
+ *
+ * Sources, cited by page title and section:
+ *   PASK     "Parser Transitions Already Reveal Structural Responsibility:
+ *             KV Persistence for Structured Generation" (arXiv 2608.28276)
+ *   PACE     "PACE: Keeping the Right Tokens in the KV Cache Is Not Enough
+ *             for Long-Horizon LLM Agents" (arXiv 2611.10240)
+ *   CommitKV "CommitKV: Lifecycle-Aware KV Cache Compression via Commit
+ *             Transitions for Multi-Turn Agents" (arXiv 2608.07855)
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is DEVICE memory of the current CUDA device, owned
+ *     by the caller.  The library keeps no pointer after a call returns and
+ *     allocates no device memory; scratch space is the caller's workspace,
+ *     sized by the matching *_workspace_bytes call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise.  Results are valid once the
+ *     caller synchronises the stream.
+ *   - Inputs are read-only (except `scores` under KVC_SCORE_ACCUMULATE).
+ *     Outputs must not alias inputs.
+ *   - Errors detectable from the arguments (null pointers, shapes, sizes,
+ *     alignment, capacity) are returned before anything is launched.
+ *     Conditions that depend on device data are written per unit to a
+ *     `unit_status` array (KVC_UNIT_*), never by trapping the GPU.
+ *   - Element layouts: bf16 = IEEE bfloat16 bits, fp16 = IEEE half bits,
+ *     row-major, innermost index last.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, passed as a plain pointer. */
+typedef void* kvc_stream;
+
+/* Host-side return codes. */
+typedef enum {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = 1,  /* a null pointer, a bad shape or size         */
+  KVC_ERR_UNSUPPORTED = 2,  /* a valid request this build does not handle */
+  KVC_ERR_WORKSPACE = 3,    /* workspace missing or too small             */
+  KVC_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed        */
+  KVC_ERR_NO_DEVICE = 5     /* no usable sm_103 device                    */
+} kvc_status;
+
+/* Per-unit device status, written to unit_status[u]. */
+enum {
+  KVC_UNIT_OK = 0,
+  KVC_UNIT_OVER_BUDGET = 1, /* forced rows alone exceed the token budget   */
+  KVC_UNIT_BAD_INDEX = 2,   /* a kept index or position outside its range */
+  KVC_UNIT_BAD_FLAGS = 3,   /* an item flagged both PROTECT and EXCLUDE    */
+  KVC_UNIT_TIMEOUT = 4      /* a bounded device wait gave up (no progress) */
+};
+
+/* Storage actions of the (tag, layer-group) table: PASK's {R, L, H} with L
+ * split into int4 and int8.  Pool index of a stored action = action - 1. */
+enum { KVC_ACT_RELEASE = 0, KVC_ACT_INT4 = 1, KVC_ACT_INT8 = 2, KVC_ACT_BF16 = 3 };
+enum { KVC_POOL_INT4 = 0, KVC_POOL_INT8 = 1, KVC_POOL_BF16 = 2, KVC_N_POOLS = 3 };
+
+/* Per-token (or per-page) flag bits. */
+enum { KVC_FLAG_PROTECT = 1, KVC_FLAG_EXCLUDE = 2 };
+
+/* Quantisation modes. */
+enum {
+  KVC_QUANT_G32_BF16 = 0,   /* groups of 32 elements, bf16 scale per group */
+  KVC_QUANT_ROW_FP16 = 1    /* one fp16 scale per row (PASK App. B.5)      */
+};
+
+/* kvc_score flags. */
+enum { KVC_SCORE_ACCUMULATE = 1 };
+
+typedef struct {
+  int32_t batch;       /* B                                        */
+  int32_t n_layers;    /* L                                        */
+  int32_t n_q_heads;   /* H_q, a multiple of H_kv                  */
+  int32_t n_kv_heads;  /* H_kv; G = H_q / H_kv query heads per KV head */
+  int32_t head_dim;    /* d: 64 or 128                             */
+  int64_t n_tokens;    /* T: cached rows per unit before compaction */
+} kvc_shape;
+
+/* ------------------------------------------------------------------------
+ * kvc_score -- observation-window attention mass (step a1/a2).
+ *
+ * PASK Eq. 1 (causal attention, softmax over K^T q / sqrt(d)); the window
+ * scorer (SnapKV, described in PASK App. C.3 and CommitKV Sec. 3.1): the
+ * last `window` queries of every query head score all cached keys, and the
+ * softmax weights are summed over the window rows and over the G query heads
+ * that share the KV head; PACE Sec. 3.1 adds an external bonus to the score.
+ * Query head h reads KV head h / G.  Window row w sits at cache index
+ * T - window + w and sees keys j <= T - window + w.
+ *
+ *   scores[u][j] = sum_{h in g} sum_w softmax_j(q_{h,w} . k_j * scale)
+ *                  + bonus[b][j] (+ scores[u][j] if KVC_SCORE_ACCUMULATE)
+ *   page_scores[u][p] = max_{j in page p} scores[u][j]      (page_size > 1)
+ *
+ * k_cache   bf16 [B][L][H_kv][T][d], keys rotated at their positions;
+ *           16-byte aligned.
+ * q_window  bf16 [B][L][H_q][window][d], rotated; 16-byte aligned.
+ * window    W >= 1, W <= T; W * G must be a multiple of 32 and <= 256.
+ * softmax_scale  <= 0 selects 1 / sqrt(d).
+ * bonus     optional fp32 [B][T] (NULL = 0).
+ * page_size 1 (no page scores) or 2, 4, 8, 16, 32 with T % page_size == 0.
+ * scores    fp32 [U][T] (read too under KVC_SCORE_ACCUMULATE).
+ * page_scores  fp32 [U][T / page_size]; required iff page_size > 1.
+ * unit_status  optional int32 [U]; KVC_UNIT_TIMEOUT if a device wait gave
+ *           up; untouched otherwise.
+ * workspace >= kvc_score_workspace_bytes(shape, window) bytes, 256-byte
+ *           aligned; its contents need not be initialised.
+ * ---------------------------------------------------------------------- */
+size_t kvc_score_workspace_bytes(const kvc_shape* shape, int32_t window);
+kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_window,
+                     int32_t window, float softmax_scale, const float* bonus,
+                     int32_t page_size, uint32_t flags, float* scores, float* page_scores,
+                     int32_t* unit_status, void* workspace, size_t workspace_bytes,
+                     kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Selection policy.  Exactly one of budget_tokens / budget_bytes is > 0.
+ *
+ * Token / page mode (budget_tokens > 0): per unit keep the forced items
+ * (n_sink first tokens, n_recent last tokens, PROTECT-flagged items) and
+ * fill the budget with the eligible items (not forced, not EXCLUDE-flagged)
+ * that rank first by (score descending, index ascending), after mapping
+ * -0 to +0 and NaN to -inf.  If the forced items alone exceed the budget
+ * the unit is KVC_UNIT_OVER_BUDGET and keeps nothing (CommitKV Eq. 4,
+ * |I| <= B; Eq. 13, protected pages are kept).  Page mode (page_size > 1)
+ * selects whole pages by page score: a page is forced if it holds a sink or
+ * recent token; budget_tokens must be a multiple of page_size.  All kept
+ * rows go to the bf16 pool.
+ *
+ * Byte mode (budget_bytes > 0): PASK's floor-constrained allocation
+ * (App. B.3-B.4, Sec. 3.5).  Each token's floor action is
+ * action_table[tags[b][t]][group(l)] with group(l) the layer group of
+ * PASK App. A.2 generalised to n_layer_groups groups,
+ * b_k = floor((k L + G - 1) / G).  Sink, recent and PROTECT tokens are
+ * bf16, EXCLUDE tokens are released.  Row cost (K+V bytes): bf16 4d;
+ * int8 2(d + s); int4 2(d/2 + s) with s = 2 d/32 (g32) or 2 (row mode).
+ * The remainder budget_bytes - sum(floor costs) is spent by promoting to
+ * bf16 the longest prefix of the (score desc, index asc) order of the
+ * remaining non-bf16 tokens whose summed upgrade costs fit; a negative
+ * remainder is written to floor_excess and nothing is promoted.
+ *
+ * renumber: 1 = kept rows get new positions 0..n_kept-1 in index order
+ *           (PACE Sec. 3.2 bounded positions), 0 = positions unchanged
+ *           (CommitKV Eq. 4).
+ * capacity: rows per pool per unit of the output arrays; must be >=
+ *           budget_tokens (token/page mode) or >= T (byte mode).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t budget_tokens;
+  int64_t budget_bytes;
+  int32_t n_sink;
+  int32_t n_recent;
+  int32_t page_size;       /* 1 = token mode                              */
+  int32_t renumber;
+  int32_t capacity;
+  int32_t quant_mode;      /* KVC_QUANT_*                                 */
+  int32_t n_tags;          /* byte mode: rows of action_table             */
+  int32_t n_layer_groups;  /* byte mode: columns of action_table          */
+  const uint8_t* flags;    /* optional uint8 [B][T] (token mode) or [B][T/P] (page mode) */
+  const uint8_t* tags;     /* byte mode: uint8 [B][T], each < n_tags      */
+  const uint8_t* action_table; /* byte mode: uint8 [n_tags][n_layer_groups] of KVC_ACT_* */
+} kvc_policy;
+
+/* ------------------------------------------------------------------------
+ * kvc_select -- masks and deterministic top-k / byte-budget selection
+ * (steps a3/a4).
+ *
+ * scores       fp32 [U][T] (token and byte mode) or [U][T/P] (page mode).
+ * kept_idx     int32 [KVC_N_POOLS][U][capacity]: kept token indices of each
+ *              pool, ascending; entries past kept_count are not written.
+ * kept_count   int32 [KVC_N_POOLS][U].
+ * unit_status  int32 [U], always written (KVC_UNIT_OK or an error code).
+ * floor_excess optional int64 [U] (byte mode; 0 otherwise).
+ * The workspace is unused today: pass NULL and 0.
+ * ---------------------------------------------------------------------- */
+size_t kvc_select_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy);
+kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const float* scores,
+                      int32_t* kept_idx, int32_t* kept_count, int32_t* unit_status,
+                      int64_t* floor_excess, void* workspace, size_t workspace_bytes,
+                      kvc_stream stream);
+
+/* Compacted pools.  A pool's pointers may be NULL when no call will store a
+ * row in it (token and page mode use only the bf16 pool). */
+typedef struct {
+  void* k_bf16;      /* bf16 [U][capacity][d]                                  */
+  void* v_bf16;
+  void* k_i8;        /* int8 codes [U][capacity][d]                            */
+  void* v_i8;
+  void* k_i8_scale;  /* g32: bf16 [U][capacity][d/32]; row mode: fp16 [U][capacity] */
+  void* v_i8_scale;
+  void* k_i4;        /* packed int4 [U][capacity][d/2]: element 2j in the low nibble */
+  void* v_i4;
+  void* k_i4_scale;  /* as k_i8_scale */
+  void* v_i4_scale;
+  int32_t* pos_out;      /* int32 [KVC_N_POOLS][U][capacity]: new position */
+  int32_t* orig_pos_out; /* optional, same layout: position before compaction */
+} kvc_pools;
+
+/* ------------------------------------------------------------------------
+ * kvc_compact_rerotate_quant -- gather, renumber, re-rotate, quantise,
+ * store (steps a5/a6).
+ *
+ * CommitKV Eq. 4: the kept index set is applied to K, V and positions.
+ * PACE Sec. 3.2: with renumber on, kept row i of the unit (all pools merged
+ * in index order) gets position p' = its rank; its key, stored rotated at
+ * p, is re-rotated by R_{p'-p} (Prop. 1), the cosine and sine of (p'-p)
+ * theta_i being formed from the caller's tables by the angle-difference
+ * identities and normalised to unit length.  Split-half rotary layout:
+ * element i pairs with i + d/2.  Fixed fp32 order, no fused multiply-add:
+ *   C = c'c + s's,  S = s'c - c's,  n = sqrt(C C + S S),  C /= n,  S /= n,
+ *   x' = x C - y S,  y' = y C + x S,  then round to bf16 (nearest even);
+ * p' == p copies the stored bits.  V rows are copied.
+ * PASK App. B.5: a quantised pool stores symmetric codes of the bf16 row:
+ * per group a = max|x|, scale = a / qmax rounded to the scale format
+ * (nearest even) and raised to its smallest positive value, code =
+ * round-half-even(x / scale) clipped to [-qmax, qmax], qmax 7 (int4) or 127
+ * (int8); an all-zero group stores zero codes and scale 1.
+ *
+ * pos_in       int32 [U][T] physical position of each cached row.
+ * kept_idx, kept_count  as written by kvc_select.
+ * rope_cos, rope_sin    fp32 [rope_max_pos][d/2]: cos / sin of p theta_i.
+ *              Every old and new position must be < rope_max_pos; a row
+ *              whose index or position is out of range is skipped and its
+ *              unit marked KVC_UNIT_BAD_INDEX.
+ * pools        output arrays (see kvc_pools).
+ * unit_status  optional int32 [U]; only errors are written.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_compact_rerotate_quant(const kvc_shape* shape, const kvc_policy* policy,
+                                      const void* k_cache, const void* v_cache,
+                                      const int32_t* pos_in, const int32_t* kept_idx,
+                                      const int32_t* kept_count, const float* rope_cos,
+                                      const float* rope_sin, int64_t rope_max_pos,
+                                      const kvc_pools* pools, int32_t* unit_status,
+                                      kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * kvc_decode_attn -- one decode-attention step over the compacted pools
+ * (step a7, the consumer check).
+ *
+ * PASK Eq. 1 over all kept rows of every pool of the unit, dequantised
+ * (x = code * scale); PASK App. B.5: fp32 scores, softmax statistics and
+ * accumulation, bf16 output; split partitions are merged by Eq. 15.
+ * q    bf16 [B][L][H_q][d], rotated at the decode position.
+ * out  bf16 [B][L][H_q][d]; a unit with no kept rows outputs zeros.
+ * softmax_scale <= 0 selects 1 / sqrt(d).
+ * workspace >= kvc_decode_workspace_bytes(shape, policy), 256-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t kvc_decode_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy);
+kvc_status kvc_decode_attn(const kvc_shape* shape, const kvc_policy* policy, const void* q,
+                           const kvc_pools* pools, const int32_t* kept_count,
+                           float softmax_scale, void* out, void* workspace,
+                           size_t workspace_bytes, kvc_stream stream);
+
+/* Static text for a status code. */
+const char* kvc_status_string(kvc_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

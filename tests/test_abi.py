@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every entry point of include/kvc.h.
+
+CPU only: no compute call is made; only host-side argument checks that
+return before touching a device are exercised.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvc.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    names = re.findall(r"\b(kvc_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from budgeted_kv_cache_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("kvc_score", "kvc_select", "kvc_compact_rerotate_quant", "kvc_decode_attn"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    f = lib.kvc_status_string
+    f.restype = ctypes.c_char_p
+    f.argtypes = [ctypes.c_int]
+    assert f(0) == b"ok"
+    assert f(1) == b"invalid argument"
+    assert f(3) == b"workspace missing or too small"
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    import budgeted_kv_cache_gb300 as kvc
+    kvc.library()
+    # null shape
+    assert lib.kvc_score(None, None, None, 0, ctypes.c_float(0), None, 1, 0, None, None, None,
+                         None, ctypes.c_size_t(0), None) == 1
+    bad = kvc.make_shape(1, 1, 4, 2, 96, 100)       # head_dim 96 is not supported
+    assert kvc.library().kvc_score(ctypes.byref(bad), None, None, 8, 0.0, None, 1, 0, None, None,
+                                   None, None, 0, None) == 2
+    shape = kvc.make_shape(1, 1, 4, 3, 64, 100)     # H_q not a multiple of H_kv
+    pol = kvc.Policy(budget_tokens=10, capacity=10).c()
+    assert kvc.library().kvc_select(ctypes.byref(shape), ctypes.byref(pol), None, None, None, None,
+                                    None, None, 0, None) == 1
+    shape = kvc.make_shape(1, 1, 4, 2, 64, 100)
+    both = kvc.Policy(budget_tokens=10, budget_bytes=100, capacity=100).c()   # two budgets
+    assert kvc.library().kvc_select(ctypes.byref(shape), ctypes.byref(both), None, None, None,
+                                    None, None, None, 0, None) == 1
+    small = kvc.Policy(budget_tokens=10, capacity=5).c()                       # capacity < budget
+    assert kvc.library().kvc_select(ctypes.byref(shape), ctypes.byref(small), None, None, None,
+                                    None, None, None, 0, None) == 1
+    page = kvc.Policy(budget_tokens=24, capacity=24, page_size=16).c()        # budget % P
+    assert kvc.library().kvc_select(ctypes.byref(shape), ctypes.byref(page), None, None, None,
+                                    None, None, None, 0, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import budgeted_kv_cache_gb300 as kvc
+    monkeypatch.setattr(kvc, "_LIB", None)
+    monkeypatch.setattr(kvc, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(kvc.KvcError):
+        kvc.library()

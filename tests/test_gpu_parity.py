@@ -1,0 +1,231 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU oracle.
+
+Each workload is run through kvc_score -> kvc_select ->
+kvc_compact_rerotate_quant -> kvc_decode_attn on the GPU and checked unit by
+unit against the oracle on the same seeded inputs:
+  * scores            within rel 1e-2 (+1e-6 absolute floor)
+  * selection         bit-exact when the oracle selects from the GPU's scores;
+                      with the oracle's own scores the kept sets may differ only
+                      at items within the score tolerance of the threshold
+  * pools             bit-exact (bf16 keys after re-rotation, values, int8/int4
+                      codes, scales, positions) for the same kept set
+  * decode output     max-abs 2e-2
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+import workloads as wl
+from helpers import (DECODE_ATOL, assert_pools_equal, assert_scores_close,
+                     assert_selection_consistent, bits, kept_lists, params_of, unit_inputs,
+                     unit_pools_from_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session")
+def kvc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from budgeted_kv_cache_gb300 import build
+    build.build()
+    import budgeted_kv_cache_gb300 as lib
+    lib.library()
+    return lib
+
+
+def run_pass(w, x):
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    p = pass_for_workload(w, inputs=x)
+    p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"], x["rope_sin"],
+          x.get("bonus"))
+    p.decode(x["q_decode"])
+    torch.cuda.synchronize()
+    return p
+
+
+def check_unit(w, x, p, u, e2e=True):
+    """All parity checks of one unit."""
+    ui = unit_inputs(w, x, u)
+    prm = params_of(w)
+    T, d = w.n_tokens, w.head_dim
+    scale = 1.0 / math.sqrt(d)
+    cos, sin = x["rope_cos"].cpu().numpy(), x["rope_sin"].cpu().numpy()
+    table = x["action_table"].cpu().numpy() if "action_table" in x else None
+
+    # scores
+    ref_scores = o.unit_scores(ui["k"], ui["q"], scale, ui["bonus"])
+    gpu_scores = p.scores[u].cpu().numpy()
+    assert_scores_close(gpu_scores, ref_scores)
+    gpu_pscores = None
+    if w.page_size > 1:
+        gpu_pscores = p.page_scores[u].cpu().numpy()
+        assert np.array_equal(gpu_pscores, o.page_max(gpu_scores, w.page_size)), "page max"
+
+    # selection from the GPU's own scores: bit-exact
+    act, excess, st = o.select_unit(gpu_scores, gpu_pscores, T, d, prm, ui["flags"], ui["tags"],
+                                    table, ui["group"])
+    assert int(p.unit_status[u]) == st
+    if w.byte_mode:
+        assert int(p.floor_excess[u]) == excess
+    gk = kept_lists(p, u)
+    for a in (o.ACT_INT4, o.ACT_INT8, o.ACT_BF16):
+        assert np.array_equal(gk[a], np.nonzero(act == a)[0]), f"unit {u} pool {a}"
+
+    # compaction of that kept set: bit-exact
+    ref_pools = o.compact_unit(ui["k"], ui["v"], ui["pos"], act, prm, cos, sin)
+    assert_pools_equal(unit_pools_from_gpu(p, u, w), ref_pools)
+    assert int(p.compact_status[u]) == 0
+
+    # decode step over the pools
+    ref_out = o.decode_unit(ui["qd"], ref_pools, scale, w.quant_mode)
+    gpu_out = p.out[u * w.group:(u + 1) * w.group].float().cpu().numpy()
+    assert np.max(np.abs(gpu_out - ref_out)) <= DECODE_ATOL
+
+    # end to end: the oracle's own scores and selection
+    if e2e and st == o.UNIT_OK and not w.byte_mode:
+        ref_src = ref_scores if w.page_size == 1 else o.page_max(ref_scores, w.page_size)
+        kept_ref, _ = o.select_tokens(ref_src, T, w.budget_tokens, w.n_sink, w.n_recent,
+                                      ui["flags"], w.page_size)
+        if w.page_size == 1:
+            forced, _, _ = o.item_masks(T, w.n_sink, w.n_recent, ui["flags"])
+            sel = np.setdiff1d(kept_ref, np.nonzero(forced)[0])
+            thr = float(np.min(ref_src[sel])) if sel.size else math.inf
+            assert_selection_consistent(ref_src, gk[o.ACT_BF16], kept_ref, thr)
+        else:
+            P = w.page_size
+            gp = np.unique(gk[o.ACT_BF16] // P)
+            rp = np.unique(kept_ref // P)
+            sp, rpg = o.sink_recent_pages(T, P, w.n_sink, w.n_recent)
+            forced, _, _ = o.item_masks(T // P, sp, rpg, ui["flags"])
+            sel = np.setdiff1d(rp, np.nonzero(forced)[0])
+            thr = float(np.min(ref_src[sel])) if sel.size else math.inf
+            assert_selection_consistent(ref_src, gp, rp, thr)
+
+
+# ------------------------------------------------------------------ small workloads
+
+def small_workloads():
+    c2 = wl.qwen3_8b_32k().replace(name="qwen_small", n_layers=1, n_kv_heads=2, n_q_heads=8,
+                                   n_tokens=5000, budget_tokens=512, decode_pos=512)
+    c3 = wl.pask_batch16().replace(name="pask_small", batch=2, n_layers=4, n_kv_heads=2,
+                                   n_q_heads=8, n_tokens=2000,
+                                   budget_bytes=(2000 * 512) // 3, decode_pos=2000)
+    c4 = wl.commitkv_pages_128k().replace(name="commitkv_small", n_layers=1, n_kv_heads=2,
+                                          n_q_heads=8, n_tokens=8192, budget_tokens=512,
+                                          protect_pages=4, retire_pages=50, decode_pos=8192)
+    c1 = wl.tiny()
+    c1r = wl.tiny().replace(name="tiny_ragged_d128", head_dim=128, n_tokens=1000, budget_tokens=200)
+    c3row = c3.replace(name="pask_small_rowfp16", quant_mode=wl.QUANT_ROW_FP16, head_dim=64,
+                       budget_bytes=(2000 * 256) // 3)
+    c2w32 = c2.replace(name="qwen_small_w32", window=32, n_tokens=3001, renumber=False,
+                       bonus_spans=0)
+    return [c1, c1r, c2, c2w32, c3, c3row, c4]
+
+
+@pytest.mark.parametrize("w", small_workloads(), ids=lambda w: w.name)
+def test_parity_small(kvc, w):
+    x = wl.make_inputs(w, device="cuda")
+    p = run_pass(w, x)
+    assert int(p.score_status.abs().sum()) == 0
+    for u in range(w.n_units):
+        check_unit(w, x, p, u)
+
+
+def test_score_accumulate(kvc):
+    w = wl.tiny().replace(n_tokens=700)
+    x = wl.make_inputs(w, device="cuda")
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    p = pass_for_workload(w, inputs=x)
+    bonus = torch.linspace(0, 1, w.n_tokens, device="cuda").view(1, -1).contiguous()
+    p.score(x["k_cache"], x["q_window"], bonus)
+    first = p.scores.clone()
+    p.score(x["k_cache"], x["q_window"], bonus, accumulate=True)
+    torch.cuda.synchronize()
+    for u in range(w.n_units):
+        ui = unit_inputs(w, x, u)
+        ref = o.unit_scores(ui["k"], ui["q"], 1 / 8, bonus[0].cpu().numpy(),
+                            first[u].cpu().numpy())
+        assert_scores_close(p.scores[u].cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_inactive_pass_is_bytewise_identity(kvc):
+    """Budget = T and no renumbering: the bf16 pool equals the input cache."""
+    w = wl.tiny().replace(n_tokens=640, budget_tokens=640, renumber=False)
+    x = wl.make_inputs(w, device="cuda")
+    p = run_pass(w, x)
+    assert torch.equal(p.kept_count[2], torch.full((w.n_units,), 640, dtype=torch.int32, device="cuda"))
+    assert torch.equal(p.pools.k_bf16.view(w.n_units, 640, -1), x["k_cache"].view(w.n_units, 640, -1))
+    assert torch.equal(p.pools.v_bf16.view(w.n_units, 640, -1), x["v_cache"].view(w.n_units, 640, -1))
+
+
+def test_over_budget_and_bad_flags(kvc):
+    w = wl.tiny().replace(n_tokens=512, budget_tokens=16, n_sink=10, n_recent=10)
+    x = wl.make_inputs(w, device="cuda")
+    p = run_pass(w, x)
+    assert torch.all(p.unit_status == o.UNIT_OVER_BUDGET)
+    assert int(p.kept_count.abs().sum()) == 0
+    w2 = wl.tiny().replace(n_tokens=512, budget_tokens=64)
+    x2 = wl.make_inputs(w2, device="cuda")
+    flags = torch.zeros(1, 512, dtype=torch.uint8, device="cuda")
+    flags[0, 100] = o.FLAG_PROTECT | o.FLAG_EXCLUDE
+    x2["flags"] = flags
+    p2 = run_pass(w2, x2)
+    assert torch.all(p2.unit_status == o.UNIT_BAD_FLAGS)
+
+
+def test_ties_and_special_scores_select_bit_exact(kvc):
+    """Selection alone on crafted scores: ties, -0, NaN, -inf, protect/exclude flags."""
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    rng = np.random.default_rng(5)
+    w = wl.tiny().replace(n_tokens=3000, budget_tokens=700, n_layers=3)
+    x = wl.make_inputs(w, device="cuda", with_tables=False)
+    vals = np.array([0.0, -0.0, 1.0, 0.5, np.nan, -np.inf, 2.0, 1e-30], np.float32)
+    scores = rng.choice(vals, size=(w.n_units, 3000)).astype(np.float32)
+    flags = rng.choice([0, 0, 0, 0, 1, 2], size=(1, 3000)).astype(np.uint8)
+    x["flags"] = torch.from_numpy(flags).cuda()
+    p = pass_for_workload(w, inputs=x)
+    p.select(scores=torch.from_numpy(scores).cuda())
+    torch.cuda.synchronize()
+    for u in range(w.n_units):
+        kept, st = o.select_tokens(scores[u], 3000, 700, w.n_sink, w.n_recent, flags[0])
+        assert int(p.unit_status[u]) == st
+        assert np.array_equal(kept_lists(p, u)[o.ACT_BF16], kept)
+
+
+def test_byte_mode_floor_excess(kvc):
+    """Floors above the byte budget: excess recorded, nothing promoted."""
+    w = wl.pask_batch16().replace(batch=1, n_layers=4, n_kv_heads=1, n_q_heads=4, n_tokens=1024,
+                                  budget_bytes=1024 * 512 // 10)
+    x = wl.make_inputs(w, device="cuda")
+    x["action_table"] = torch.full_like(x["action_table"], o.ACT_INT8)
+    p = run_pass(w, x)
+    for u in range(w.n_units):
+        check_unit(w, x, p, u, e2e=False)
+        assert int(p.floor_excess[u]) > 0
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _sample_units(w, n=3):
+    U = w.n_units
+    return sorted({0, U // 2, U - 1} if n >= 3 else {0, U - 1})
+
+
+@pytest.mark.parametrize("make", [wl.qwen3_8b_32k, wl.pask_batch16, wl.commitkv_pages_128k],
+                         ids=lambda f: f.__name__)
+def test_parity_full_size_sampled_units(kvc, make):
+    w = make()
+    x = wl.make_inputs(w, device="cuda")
+    p = run_pass(w, x)
+    assert int(p.score_status.abs().sum()) == 0
+    assert int(p.compact_status.abs().sum()) == 0
+    for u in _sample_units(w):
+        check_unit(w, x, p, u)
+    del p, x
+    torch.cuda.empty_cache()
