@@ -85,6 +85,8 @@ def unit_pools_from_gpu(pass_, u, w):
         pool.orig_pos = P.orig_pos_out[pi, u, :n].cpu().numpy()
         if a == o.ACT_BF16:
             pool.k, pool.v = bits(P.k_bf16[u, :n]), bits(P.v_bf16[u, :n])
+        elif n == 0:
+            pool.k = pool.v = None
         else:
             kc = P.k_i8 if a == o.ACT_INT8 else P.k_i4
             vc = P.v_i8 if a == o.ACT_INT8 else P.v_i4
