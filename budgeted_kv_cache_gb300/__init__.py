@@ -76,6 +76,7 @@ def _load():
             "kvc_compact_rerotate_quant": (ctypes.c_int, [SH, PO, P, P, P, P, P, P, P, I64, PL, P, P]),
             "kvc_decode_workspace_bytes": (SZ, [SH, PO]),
             "kvc_decode_attn": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P, SZ, P]),
+            "kvc_decode_attn_noalloc": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P]),
             "kvc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -236,3 +237,12 @@ def kvc_decode_attn(shape, policy: Policy, q, pools: Pools, kept_count, softmax_
     _check("kvc_decode_attn", _load().kvc_decode_attn(
         ctypes.byref(shape), ctypes.byref(cp), _p(q), ctypes.byref(cpools), _p(kept_count),
         float(softmax_scale), _p(out), _p(workspace), wb, _stream(stream)))
+
+
+def kvc_decode_attn_noalloc(shape, policy: Policy, q, pools: Pools, kept_count, softmax_scale,
+                            out, stream=None):
+    """kvc_decode_attn with the library's static scratch instead of a workspace."""
+    cp, cpools = policy.c(), pools.c()
+    _check("kvc_decode_attn_noalloc", _load().kvc_decode_attn_noalloc(
+        ctypes.byref(shape), ctypes.byref(cp), _p(q), ctypes.byref(cpools), _p(kept_count),
+        float(softmax_scale), _p(out), _stream(stream)))

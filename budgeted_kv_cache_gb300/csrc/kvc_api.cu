@@ -447,3 +447,55 @@ kvc_status kvc_decode_attn(const kvc_shape* shape, const kvc_policy* policy, con
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Decode step that allocates nothing.
+//
+// Some callers cannot hand the library a workspace: an engine whose caching
+// allocator has already reserved nearly all of HBM for its KV pools (a raw
+// cudaMalloc would fail or fragment that reservation), a plug-in that only
+// receives the buffers its host framework gives it and has no allocator of
+// its own, or a latency-critical loop where cudaMalloc's implicit device
+// synchronisation is not acceptable.  For them kvc_decode_attn_noalloc keeps
+// the split-partition scratch of the decode step in the file-scope array
+// below, which every device that loads this library holds until the process
+// exits.
+// ----------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;    // 2 MiB per device
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the symbol is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and cached.
+kvc_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVC_ERR_NO_DEVICE;
+  static void* addr[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVC_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" kvc_status kvc_decode_attn_noalloc(const kvc_shape* shape, const kvc_policy* policy,
+                                              const void* q, const kvc_pools* pools,
+                                              const int32_t* kept_count, float softmax_scale,
+                                              void* out, kvc_stream stream) {
+  const size_t need = kvc_decode_workspace_bytes(shape, policy);
+  if (need > kNoAllocScratchBytes) return KVC_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if (need > 0) {
+    kvc_status st = noalloc_scratch(&ws);
+    if (st != KVC_OK) return st;
+  }
+  return kvc_decode_attn(shape, policy, q, pools, kept_count, softmax_scale, out, ws, need, stream);
+}

@@ -268,6 +268,32 @@ kvc_status kvc_decode_attn(const kvc_shape* shape, const kvc_policy* policy, con
                            float softmax_scale, void* out, void* workspace,
                            size_t workspace_bytes, kvc_stream stream);
 
+/* ------------------------------------------------------------------------
+ * kvc_decode_attn_noalloc -- kvc_decode_attn without a caller workspace.
+ *
+ * Not a step of the pages' methods (they have no counterpart): a variant for
+ * callers that cannot allocate device memory -- an engine whose allocator
+ * already owns nearly all of HBM, a plug-in that only receives its host
+ * framework's buffers, or a latency-critical loop that cannot afford
+ * cudaMalloc's implicit synchronisation.  The split-partition scratch lives
+ * in a static device array of 2 MiB inside the library, held by every device
+ * that loads it until the process exits.  The caller still passes inputs
+ * and outputs; the result equals kvc_decode_attn's.
+ *   - Returns KVC_ERR_WORKSPACE if kvc_decode_workspace_bytes(shape, policy)
+ *     exceeds 2 MiB (nothing is launched).
+ *   - Calls no cudaMalloc / cudaFree.  The first call on a device looks up
+ *     the array's device address (cudaGetSymbolAddress) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; nothing in it needs to start at zero (every partition
+ *     slot the merge reads is written earlier in the same call).  Calls that
+ *     overlap on the GPU (concurrent streams) race on it: serialise them.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_decode_attn_noalloc(const kvc_shape* shape, const kvc_policy* policy,
+                                   const void* q, const kvc_pools* pools,
+                                   const int32_t* kept_count, float softmax_scale, void* out,
+                                   kvc_stream stream);
+
 /* Static text for a status code. */
 const char* kvc_status_string(kvc_status status);
 

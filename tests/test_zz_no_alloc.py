@@ -1,0 +1,77 @@
+"""kvc_decode_attn_noalloc: the decode step for callers that cannot allocate.
+
+Callers such as an engine whose allocator already owns nearly all of HBM, a
+plug-in that only gets its host framework's buffers, or a latency-critical
+loop that cannot pay for cudaMalloc's implicit synchronisation cannot pass
+a workspace.  This entry point keeps the decode step's split-partition
+scratch in a static device array inside the library instead.  The test
+calls it through the C-ABI twice in a row and checks each output against
+kvc_decode_attn with a caller workspace, within the decode tolerance.
+
+Collected last on purpose, so a run that stops at the first failure has
+already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DECODE_ATOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from budgeted_kv_cache_gb300 import build
+    build.build()
+    import budgeted_kv_cache_gb300 as lib
+    lib.library()
+    return lib
+
+
+def _workloads():
+    # small unit counts and capacities above 256 rows, so the decode is split
+    # across CTAs and really goes through the scratch array
+    tok = wl.qwen3_8b_32k().replace(n_layers=1, n_kv_heads=2, n_q_heads=8, n_tokens=5000,
+                                    budget_tokens=512)
+    byt = wl.pask_batch16().replace(batch=1, n_layers=4, n_kv_heads=1, n_q_heads=4,
+                                    n_tokens=2000, budget_bytes=(2000 * 512) // 3)
+    return [tok, byt]
+
+
+@pytest.mark.parametrize("w", _workloads(), ids=["token_mode", "byte_mode"])
+def test_noalloc_decode_matches_workspace_decode(kvc, w):
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    x = wl.make_inputs(w, device="cuda")
+    p = pass_for_workload(w, inputs=x)
+    need = kvc.kvc_decode_workspace_bytes(p.shape, p.policy)
+    assert 0 < need <= (2 << 20)          # split decode: the scratch array is really used
+    p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"], x["rope_sin"],
+          x.get("bonus"))
+    ref = p.decode(x["q_decode"]).clone()
+    for _ in range(2):
+        out = torch.full_like(ref, float("nan"))
+        kvc.kvc_decode_attn_noalloc(p.shape, p.policy, x["q_decode"], p.pools, p.kept_count,
+                                    0.0, out)
+        torch.cuda.synchronize()
+        diff = (out.float() - ref.float()).abs().max().item()
+        assert np.isfinite(diff) and diff <= DECODE_ATOL
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(kvc):
+    """A request whose scratch would exceed 2 MiB is refused before any launch."""
+    from budgeted_kv_cache_gb300 import Policy, Pools, make_shape
+    shape = make_shape(1, 75, 32, 4, 128, 4096)       # 300 units, 8 query heads per KV head
+    pol = Policy(budget_tokens=512, capacity=512)
+    need = kvc.kvc_decode_workspace_bytes(shape, pol)
+    if need <= (2 << 20):
+        pytest.skip("this device's split count keeps the request within the scratch")
+    dummy = lambda dt=torch.float32: torch.empty(16, dtype=dt, device="cuda")
+    pools = Pools(k_bf16=dummy(), v_bf16=dummy(), pos_out=dummy(torch.int32))
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.kvc_decode_attn_noalloc(shape, pol, dummy(), pools, dummy(torch.int32), 0.0, dummy())
+    assert e.value.code == 3
