@@ -369,10 +369,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="use only this many layers of the workload (small profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
     w = wl.ALL[args.workload]()
+    if args.layers > 0:
+        w = w.replace(n_layers=min(args.layers, w.n_layers),
+                      name=f"{w.name}_{min(args.layers, w.n_layers)}layers")
     if args.impl == "reference":
         run_reference(args, w, world, rank)
     else:

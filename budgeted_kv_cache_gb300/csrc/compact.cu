@@ -8,11 +8,12 @@
 // symmetric per-group scale (here bf16 scale per 32 elements, or the page's
 // fp16 scale per row).
 //
-// One row pair (a K row and its V row) per 2 * d/8 lanes: each lane moves 16
-// bytes (8 bf16) of one row with one 128-bit load, so a warp reads and
-// writes whole 256-byte rows at d = 128 (two row pairs per warp at d = 64).
+// One row per d/8 lanes: each lane moves 16 bytes (8 bf16) of one row with
+// one 128-bit load, so a warp reads and writes two whole 256-byte rows at
+// d = 128 (four at d = 64).  Key rows and value rows are handled by separate
+// warps, so the rotation work of a key warp is spread over all its lanes.
 // The split-half partner element (i <-> i + d/2) sits in lane ^ (d/16) and
-// comes over one shuffle.  All float operations use explicit round-to-
+// comes over one shuffle; the two partners split the cos/sin work.  All float operations use explicit round-to-
 // nearest intrinsics (no contraction into FMA), so the stored bits are a
 // fixed function of the inputs.
 #include "kvc_internal.cuh"
@@ -51,17 +52,17 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-__global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs a) {
   const int d = a.d;
-  const int lpr = d / 8;                        // lanes per K (or V) row
-  const int pairs_per_warp = 32 / (2 * lpr);
+  const int lpr = d / 8;                        // lanes per row (16 B = 8 bf16 per lane)
+  const int rows_per_warp = 32 / lpr;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane / (2 * lpr);
-  const int is_v = (lane / lpr) & 1;
+  const int sub = lane / lpr;
   const int hl = lane % lpr;
-  const int pool = a.pool_lo + blockIdx.z;
+  const int is_v = blockIdx.z & 1;              // K rows and V rows go to separate warps
+  const int pool = a.pool_lo + (blockIdx.z >> 1);
   const int u = blockIdx.y;
-  const int64_t i = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * pairs_per_warp + sub;
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * rows_per_warp + sub;
   const int U = a.U;
   const int cap = a.capacity;
   const int cnt = a.kept_count[pool * U + u];
@@ -75,10 +76,13 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     t = a.kept_idx[slot];
     if (t < 0 || t >= a.T) {
       valid = false;
-      if (hl == 0 && is_v == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
+      if (hl == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
     }
   }
-  if (valid) {
+  uint4 w = make_uint4(0, 0, 0, 0);
+  const __nv_bfloat16* src = is_v ? a.v : a.k;
+  if (valid) w = *reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(u) * a.T + t) * d + hl * 8);
+  if (valid && !is_v) {
     p = a.pos_in[static_cast<int64_t>(u) * a.T + t];
     p2 = p;
     if (a.renumber) {
@@ -96,57 +100,69 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     if (rotate && (p < 0 || p >= a.rope_max_pos || p2 < 0 || p2 >= a.rope_max_pos)) {
       valid = false;
       rotate = false;
-      if (hl == 0 && is_v == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
+      if (hl == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
     }
   }
 
-  const __nv_bfloat16* src = is_v ? a.v : a.k;
-  uint4 w = make_uint4(0, 0, 0, 0);
-  if (valid) w = *reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(u) * a.T + t) * d + hl * 8);
-
-  // partner half of the split-half pair lives in lane ^ (lpr / 2)
-  const int px = lpr / 2;
-  uint4 o;
-  o.x = __shfl_xor_sync(kFull, w.x, px);
-  o.y = __shfl_xor_sync(kFull, w.y, px);
-  o.z = __shfl_xor_sync(kFull, w.z, px);
-  o.w = __shfl_xor_sync(kFull, w.w, px);
-
   float x[8];
   unpack8(w, x);
-  if (valid && rotate && !is_v) {
+  // Re-rotation (key warps only; the branch is warp-uniform).  Lane hl holds
+  // elements 8 hl .. 8 hl + 7; its split-half partner is lane hl ^ (lpr / 2).
+  // The two lanes of a pair need the same 8 (C, S): each computes four of
+  // them and they swap the other four.
+  if (!is_v && __any_sync(kFull, rotate)) {
+    const int px = lpr / 2;
+    uint4 ow;
+    ow.x = __shfl_xor_sync(kFull, w.x, px);
+    ow.y = __shfl_xor_sync(kFull, w.y, px);
+    ow.z = __shfl_xor_sync(kFull, w.z, px);
+    ow.w = __shfl_xor_sync(kFull, w.w, px);
     float y[8];
-    unpack8(o, y);
-    const int j0 = (hl % px) * 8;                 // first pair index of this lane
-    const int half = d / 2;
-    const float* c0p = a.cos + static_cast<int64_t>(p) * half + j0;
-    const float* s0p = a.sin + static_cast<int64_t>(p) * half + j0;
-    const float* c1p = a.cos + static_cast<int64_t>(p2) * half + j0;
-    const float* s1p = a.sin + static_cast<int64_t>(p2) * half + j0;
-    float c0[8], s0[8], c1[8], s1[8];
-#pragma unroll
-    for (int k = 0; k < 8; k += 4) {
-      *reinterpret_cast<float4*>(c0 + k) = *reinterpret_cast<const float4*>(c0p + k);
-      *reinterpret_cast<float4*>(s0 + k) = *reinterpret_cast<const float4*>(s0p + k);
-      *reinterpret_cast<float4*>(c1 + k) = *reinterpret_cast<const float4*>(c1p + k);
-      *reinterpret_cast<float4*>(s1 + k) = *reinterpret_cast<const float4*>(s1p + k);
-    }
+    unpack8(ow, y);
     const bool first_half = hl < px;
+    const int j0 = (hl % px) * 8 + (first_half ? 0 : 4);   // the four pairs this lane forms
+    float C4[4] = {1.f, 1.f, 1.f, 1.f}, S4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (rotate) {
+      const int half = d / 2;
+      const float4 c0 = *reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p) * half + j0);
+      const float4 s0 = *reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p) * half + j0);
+      const float4 c1 = *reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p2) * half + j0);
+      const float4 s1 = *reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p2) * half + j0);
+      const float cc0[4] = {c0.x, c0.y, c0.z, c0.w}, ss0[4] = {s0.x, s0.y, s0.z, s0.w};
+      const float cc1[4] = {c1.x, c1.y, c1.z, c1.w}, ss1[4] = {s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float C = __fadd_rn(__fmul_rn(c1[k], c0[k]), __fmul_rn(s1[k], s0[k]));
-      float S = __fsub_rn(__fmul_rn(s1[k], c0[k]), __fmul_rn(c1[k], s0[k]));
-      const float nrm = __fsqrt_rn(__fadd_rn(__fmul_rn(C, C), __fmul_rn(S, S)));
-      C = __fdiv_rn(C, nrm);
-      S = __fdiv_rn(S, nrm);
-      // first half holds x (partner y); second half holds y (partner x)
-      x[k] = first_half ? __fsub_rn(__fmul_rn(x[k], C), __fmul_rn(y[k], S))
-                        : __fadd_rn(__fmul_rn(x[k], C), __fmul_rn(y[k], S));
+      for (int k = 0; k < 4; ++k) {
+        float C = __fadd_rn(__fmul_rn(cc1[k], cc0[k]), __fmul_rn(ss1[k], ss0[k]));
+        float S = __fsub_rn(__fmul_rn(ss1[k], cc0[k]), __fmul_rn(cc1[k], ss0[k]));
+        const float nrm = __fsqrt_rn(__fadd_rn(__fmul_rn(C, C), __fmul_rn(S, S)));
+        C4[k] = __fdiv_rn(C, nrm);
+        S4[k] = __fdiv_rn(S, nrm);
+      }
     }
-    // round to bf16: quantisation below starts from the stored bf16 row
+    float Cx[4], Sx[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = bf16_bits_to_float(float_to_bf16_bits(x[k]));
-    w = pack8_bf16(x);
+    for (int k = 0; k < 4; ++k) {
+      Cx[k] = __shfl_xor_sync(kFull, C4[k], px);
+      Sx[k] = __shfl_xor_sync(kFull, S4[k], px);
+    }
+    if (rotate) {
+      float C[8], S[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        C[k] = first_half ? C4[k] : Cx[k];
+        S[k] = first_half ? S4[k] : Sx[k];
+        C[k + 4] = first_half ? Cx[k] : C4[k];
+        S[k + 4] = first_half ? Sx[k] : S4[k];
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        // first half holds x (partner y); second half holds y (partner x)
+        const float r = first_half ? __fsub_rn(__fmul_rn(x[k], C[k]), __fmul_rn(y[k], S[k]))
+                                   : __fadd_rn(__fmul_rn(x[k], C[k]), __fmul_rn(y[k], S[k]));
+        x[k] = bf16_bits_to_float(float_to_bf16_bits(r));   // stored bf16 value
+      }
+      w = pack8_bf16(x);
+    }
   }
 
   const int64_t row = static_cast<int64_t>(u) * cap + i;
@@ -163,26 +179,26 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
     const int gl = row_mode ? lpr : 4;             // lanes per scale group
     for (int o2 = 1; o2 < gl; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o2));
-    float s = 1.f;
+    float sc = 1.f;
     uint16_t s_bits;
     if (!row_mode) {
       if (amax > 0.f) {
-        s = bf16_bits_to_float(float_to_bf16_bits(__fdiv_rn(amax, qmax)));
-        s = fmaxf(s, __uint_as_float(0x00010000u));          // 2^-133
+        sc = bf16_bits_to_float(float_to_bf16_bits(__fdiv_rn(amax, qmax)));
+        sc = fmaxf(sc, __uint_as_float(0x00010000u));          // 2^-133
       }
-      s_bits = float_to_bf16_bits(s);
+      s_bits = float_to_bf16_bits(sc);
     } else {
       if (amax > 0.f) {
-        s = __half2float(__float2half_rn(__fdiv_rn(amax, qmax)));
-        s = fminf(s, 65504.f);
-        s = fmaxf(s, 5.9604644775390625e-08f);               // 2^-24
+        sc = __half2float(__float2half_rn(__fdiv_rn(amax, qmax)));
+        sc = fminf(sc, 65504.f);
+        sc = fmaxf(sc, 5.9604644775390625e-08f);               // 2^-24
       }
-      s_bits = __half_as_ushort(__float2half_rn(s));
+      s_bits = __half_as_ushort(__float2half_rn(sc));
     }
     int qv[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      int q = amax > 0.f ? __float2int_rn(__fdiv_rn(x[k], s)) : 0;
+      int q = amax > 0.f ? __float2int_rn(__fdiv_rn(x[k], sc)) : 0;
       q = q > static_cast<int>(qmax) ? static_cast<int>(qmax) : q;
       q = q < -static_cast<int>(qmax) ? -static_cast<int>(qmax) : q;
       qv[k] = q;
@@ -221,11 +237,11 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
 }  // namespace
 
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
-  const int pairs_per_block = (kThreads / 32) * (32 / (2 * (a.d / 8)));
-  const int bx = (a.capacity + pairs_per_block - 1) / pairs_per_block;
+  const int rows_per_block = (kThreads / 32) * (32 / (a.d / 8));
+  const int bx = (a.capacity + rows_per_block - 1) / rows_per_block;
   const int n_pools = a.pool_hi - a.pool_lo;
   if (bx == 0 || n_pools <= 0) return cudaSuccess;
-  dim3 grid(bx, a.U, n_pools);
+  dim3 grid(bx, a.U, 2 * n_pools);            // z: (pool, K or V)
   compact_kernel<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }

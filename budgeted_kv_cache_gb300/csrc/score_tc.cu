@@ -23,8 +23,11 @@
 // Co-residency of all CTAs (needed by that wait) is guaranteed by launching
 // cooperatively; every wait is bounded in time.
 //
-// Warp roles (12 warps): 0 = TMA producer, 1 = MMA issuer, 2 = TMEM owner,
-// 3 = idle, 4..11 = epilogue (two warps per TMEM lane quarter).
+// Warp roles (18 warps): 0 = TMA producer, 1 = TMEM owner and MMA issuer,
+// 2..17 = epilogue, four warpgroups that each cover the four TMEM lane
+// quarters (warp w reads lanes 32 (w % 4) .. 32 (w % 4) + 31).  Warpgroups
+// 2b and 2b+1 share TMEM buffer b and split its columns, so every SM
+// sub-partition runs four epilogue warps.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -33,9 +36,9 @@ namespace kvc {
 
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kEpiWarp0 = 4;
-constexpr int kEpiThreads = 256;
+constexpr int kThreads = 576;
+constexpr int kEpiWarp0 = 2;
+constexpr int kEpiThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle-128 K chunk)
 
@@ -51,10 +54,10 @@ struct Smem {
   uint64_t* mmadone;
   uint32_t* tmem_slot;
   int* abort_flag;
-  float* lam;           // [256]
-  float* red;           // [128]
-  float* hm;            // [128]
-  float* hl;            // [128]
+  float* lam;           // [256] negated log-sum-exp of each window row
+  float* red;           // [2 buffers][2 parities][128] pass-2 partial sums
+  float* hm;            // [4 groups][256] pass-1 partial max
+  float* hl;            // [4 groups][256] pass-1 partial sum
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n_stages) {
@@ -73,8 +76,8 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.lam = reinterpret_cast<float*>(s.tmem_slot + 4);
   s.red = s.lam + 256;
-  s.hm = s.red + 128;
-  s.hl = s.hm + 128;
+  s.hm = s.red + 512;
+  s.hl = s.hm + 1024;
   return s;
 }
 
@@ -87,12 +90,86 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Online max / sum update of one window row with 32 more raw logits
+// (pass 1, log2 domain: y = z * cs).  Masked logits are -inf.
+__device__ __forceinline__ void row_update(const uint32_t (&r)[32], float cs, bool masked,
+                                           int64_t j0, int64_t last, float& m, float& l) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  if (masked) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (j0 + i > last) v[i] = -INFINITY;
+  }
+  float t[11];
+#pragma unroll
+  for (int k = 0; k < 10; ++k) t[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  t[10] = fmaxf(v[30], v[31]);
+  const float mx = fmaxf(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]),
+                               fmax3(t[6], t[7], t[8])),
+                         fmaxf(t[9], t[10]));
+  const float mc = mx * cs;
+  if (mc > m) {
+    l *= ex2_approx(m - mc);
+    m = mc;
+  }
+  if (m == -INFINITY) return;
+  const float nm = -m;
+  float sm[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sm[k] = ex2_approx(fmaf(v[k], cs, nm));
+#pragma unroll
+  for (int i = 8; i < 32; ++i) sm[i & 7] += ex2_approx(fmaf(v[i], cs, nm));
+  l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+}
+
+// Pass 2: add exp2(z * cs - lse_r) of 32 rows r to the token's mass (eight
+// running partial sums).  nlam holds -lse of those 32 rows.
+__device__ __forceinline__ void mass_accum(const uint32_t (&r)[32], const float* nlam, float cs,
+                                           float (&acc)[8]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 nl = *reinterpret_cast<const float4*>(nlam + i);
+    acc[(i >> 2) & 7] += ex2_approx(fmaf(__uint_as_float(r[i]), cs, nl.x));
+    acc[((i >> 2) + 1) & 7] += ex2_approx(fmaf(__uint_as_float(r[i + 1]), cs, nl.y));
+    acc[((i >> 2) + 2) & 7] += ex2_approx(fmaf(__uint_as_float(r[i + 2]), cs, nl.z));
+    acc[((i >> 2) + 3) & 7] += ex2_approx(fmaf(__uint_as_float(r[i + 3]), cs, nl.w));
+  }
+}
+
+// Same with the causal mask of the last tiles: row r0 + i sees token j iff
+// j <= Tq + (r0 + i) mod W.
+__device__ __forceinline__ void mass_accum_masked(const uint32_t (&r)[32], const float* nlam,
+                                                  float cs, int r0, int64_t j, int64_t Tq, int W,
+                                                  float (&acc)[8]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const bool vis = j <= Tq + ((r0 + i) % W);
+    acc[i & 7] += vis ? ex2_approx(fmaf(__uint_as_float(r[i]), cs, nlam[i])) : 0.f;
+  }
+}
+
+// Walk `nq` 32-column chunks of a TMEM tile, one load at a time: with four
+// epilogue warps per SM sub-partition the load latency of one warp is
+// covered by the arithmetic of the others.
+template <class ColF, class ProcF>
+__device__ __forceinline__ void tmem_chunks(uint32_t tbuf, int nq, ColF col, ProcF proc) {
+  for (int q = 0; q < nq; ++q) {
+    uint32_t A[32];
+    tmem_ld32_issue(tbuf + col(q), A);
+    tmem_ld_wait(A);
+    proc(A, q);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
              const ScoreArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned start, formed by pointer arithmetic on the shared array
+  // so that the compiler keeps every derived pointer in the shared space
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int n_kc = a.d / 64;
   const Smem s = carve(base, n_kc, a.q_rows, a.n_stages);
   const uint32_t q_chunk_bytes = static_cast<uint32_t>(a.q_rows) * 128u;
@@ -108,7 +185,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
-      mbar_init(smem_u32(&s.tempty[i]), kEpiThreads / 32);
+      mbar_init(smem_u32(&s.tempty[i]), 8);   // one arrival per warp of the two owning warpgroups
     }
     mbar_init(smem_u32(s.qfull), 1);
     mbar_init(smem_u32(s.qempty), 1);
@@ -127,7 +204,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_q);
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(s.tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -240,29 +317,40 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
-    // Every named barrier below is an OR-reduction of a failure flag, and no
-    // thread leaves the item loop between two of them, so a bounded wait
-    // that gives up in one warp ends all epilogue warps at the same barrier.
-    const int e = warp - kEpiWarp0;            // 0..7
+    // Warpgroup g (0..3) owns TMEM buffer tb = g % 2, i.e. every tile whose
+    // running index jt has jt % 2 == tb, and column half h = g / 2 of it:
+    // in pass 1 token columns [64 h, 64 h + 64) of each row block, in pass 2
+    // window rows [R/2 h, R/2 (h + 1)).  The two groups of a buffer meet at a
+    // per-tile pair barrier in pass 2 to add their halves of each token's sum.
+    // Every named barrier is an OR-reduction of a failure flag, and no thread
+    // leaves the item loop between two of them, so a bounded wait that gives
+    // up in one warp ends all epilogue warps at the same barrier.
+    const int e = warp - kEpiWarp0;            // 0..15
     const int qr = warp & 3;                   // TMEM lane quarter of this warp
-    const int hf = e >> 2;                     // which half of the columns
+    const int grp = e >> 2;                    // 0..3
+    const uint32_t tbo = static_cast<uint32_t>(grp & 1);   // TMEM buffer of this group
+    const int half = grp >> 1;
+    const int pair_bar = 2 + static_cast<int>(tbo);        // named barrier of the buffer's pair
     const int et = threadIdx.x - kEpiWarp0 * 32;
+    const int lrow = qr * 32 + lane;           // TMEM lane of this thread
     const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
+    const uint32_t tbuf = tmem_base + lane_addr + tbo * 256;
     const float cs = a.scale_log2;
     const int64_t T = a.T;
     const int64_t Tq = T - a.W;                // row w sees keys j <= Tq + w
     const int n_cc = a.R / 32;
     const int cc_split = (n_cc + 1) / 2;
-    const int cc_lo = hf ? cc_split : 0;
-    const int cc_hi = hf ? n_cc : cc_split;
-    // pass-1 geometry: which row this thread owns and which token columns
-    const int row = (n_rb == 2) ? hf * 128 + qr * 32 + lane : qr * 32 + lane;
-    const int tok_lo = (n_rb == 2) ? 0 : hf * 64;
-    const int ntok = (n_rb == 2) ? 128 : 64;
-    const int colbase = ((n_rb == 2) ? hf * 128 : 0) + tok_lo;
-    const bool row_valid = row < a.R;
-    const int64_t row_last = Tq + (row_valid ? row % a.W : 0);
-    const bool stats_owner = ((n_rb == 2) || hf == 0) && row_valid;
+    const int cc_lo = half ? cc_split : 0;
+    const int n_my_cc = half ? n_cc - cc_split : cc_split;
+    // pass-1 rows of this thread: lrow + 128 rb, rb < n_rb
+    bool rvalid[2];
+    int64_t rlast[2];
+#pragma unroll
+    for (int rb = 0; rb < 2; ++rb) {
+      const int r = lrow + 128 * rb;
+      rvalid[rb] = rb < n_rb && r < a.R;
+      rlast[rb] = Tq + (rvalid[rb] ? r % a.W : 0);
+    }
 
     uint32_t jt = 0;
     bool fail = false;
@@ -275,56 +363,50 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       cur_u = u;
 
       // ---------------- pass 1: per-row online max / sum (log2 domain)
-      float m = -INFINITY, l = 0.f;
+      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
       for (int t = 0; t < nt; ++t, ++jt) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
+        if (tb != tbo) continue;
         if (fail || !mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
           fail = true;
           continue;
         }
         tc_fence_after();
-        const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + tok_lo;
-        const bool all_visible = (j0 + ntok - 1) <= Tq;
-        for (int cc = 0; cc < ntok; cc += 32) {
-          float v[32];
-          tmem_ld32(tmem_base + lane_addr + tb * 256 + colbase + cc, v);
-          if (!all_visible) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (j0 + cc + i > row_last) v[i] = -INFINITY;
-          }
-          float mx = v[0];
-#pragma unroll
-          for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
-          const float mn = fmaxf(m, mx * cs);
-          if (mn == -INFINITY) continue;
-          float sum = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sum += ex2_approx(fmaf(v[i], cs, -mn));
-          l = l * ex2_approx(m - mn) + sum;
-          m = mn;
-        }
+        const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + 64 * half;
+        const bool masked = (j0 + 63) > Tq;
+        tmem_chunks(tbuf, 2 * n_rb,
+                    [half](int q) { return (q >> 1) * 128 + 64 * half + (q & 1) * 32; },
+                    [&](const uint32_t(&r)[32], int q) {
+                      const int64_t jc = j0 + (q & 1) * 32;
+                      if (q < 2) row_update(r, cs, masked, jc, rlast[0], m0, l0);
+                      else       row_update(r, cs, masked, jc, rlast[1], m1, l1);
+                    });
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
       }
-      if (n_rb == 1) {   // the two halves saw different token columns of the same row
-        if (hf == 1) {
-          s.hm[qr * 32 + lane] = m;
-          s.hl[qr * 32 + lane] = l;
-        }
-        fail = named_bar_or(1, kEpiThreads, fail);
-        if (hf == 0) {
-          const float m2 = s.hm[qr * 32 + lane], l2 = s.hl[qr * 32 + lane];
-          const float mn = fmaxf(m, m2);
+      // merge the four warpgroups' statistics of each row
+      s.hm[grp * 256 + lrow] = m0;
+      s.hl[grp * 256 + lrow] = l0;
+      s.hm[grp * 256 + 128 + lrow] = m1;
+      s.hl[grp * 256 + 128 + lrow] = l1;
+      fail = named_bar_or(1, kEpiThreads, fail);
+      if (grp == 0 && !fail) {
+#pragma unroll
+        for (int rb = 0; rb < 2; ++rb) {
+          float mn = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) mn = fmaxf(mn, s.hm[g * 256 + rb * 128 + lrow]);
+          float ls = 0.f;
           if (mn != -INFINITY) {
-            l = l * ex2_approx(m - mn) + l2 * ex2_approx(m2 - mn);
-            m = mn;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              ls += s.hl[g * 256 + rb * 128 + lrow] * ex2_approx(s.hm[g * 256 + rb * 128 + lrow] - mn);
           }
+          if (rvalid[rb])
+            a.stats[(static_cast<size_t>(u) * S + c) * a.R + lrow + 128 * rb] = make_float2(mn, ls);
         }
       }
-      if (!fail && stats_owner)
-        a.stats[(static_cast<size_t>(u) * S + c) * a.R + row] = make_float2(m, l);
       __threadfence();
       fail = named_bar_or(1, kEpiThreads, fail);
       if (fail) break;
@@ -353,64 +435,69 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       }
       fail = named_bar_or(1, kEpiThreads, timed_out);
       if (fail) break;
-      // log-sum-exp of every row over the whole unit
+      // log-sum-exp of every row over the whole unit (stored negated)
       for (int r = et; r < a.R; r += kEpiThreads) {
         float M = -INFINITY, Ls = 0.f;
-        for (int cc = 0; cc < S; ++cc) {
-          const float2 st = __ldcg(&a.stats[(static_cast<size_t>(u) * S + cc) * a.R + r]);
-          if (st.x == -INFINITY) continue;
-          if (st.x > M) {
-            Ls = Ls * ex2_approx(M - st.x) + st.y;
-            M = st.x;
-          } else {
-            Ls += st.y * ex2_approx(st.x - M);
+        const float2* st_row = a.stats + static_cast<size_t>(u) * S * a.R + r;
+        for (int c0 = 0; c0 < S; c0 += 8) {
+          float2 st[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            st[k] = (c0 + k < S) ? __ldcg(st_row + static_cast<size_t>(c0 + k) * a.R)
+                                 : make_float2(-INFINITY, 0.f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (st[k].x == -INFINITY) continue;
+            if (st[k].x > M) {
+              Ls = Ls * ex2_approx(M - st[k].x) + st[k].y;
+              M = st[k].x;
+            } else {
+              Ls += st[k].y * ex2_approx(st[k].x - M);
+            }
           }
         }
-        s.lam[r] = M + __log2f(Ls);
+        s.lam[r] = -(M + __log2f(Ls));
       }
       named_bar_sync(1, kEpiThreads);
 
       // ---------------- pass 2: per-token sum of exp2(z cs - lse) over rows
       for (int t = 0; t < nt; ++t, ++jt) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
+        if (tb != tbo) continue;
         const int64_t tile0 = static_cast<int64_t>(t0 + t) * kTileTokens;
-        const int64_t j = tile0 + qr * 32 + lane;
-        float acc = 0.f;
+        const int64_t j = tile0 + lrow;
+        const bool masked = (tile0 + kTileTokens - 1) > Tq;
+        float* dst = a.scores + static_cast<int64_t>(u) * T + j;
+        float extra = 0.f;
+        if (half == 0 && j < T) {     // global inputs, loaded before the TMEM work
+          if (a.bonus) extra += __ldg(a.bonus + static_cast<int64_t>(b) * T + j);
+          if (a.accumulate) extra += *dst;
+        }
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (!fail && mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
           tc_fence_after();
-          const bool all_visible = (tile0 + kTileTokens - 1) <= Tq;
-          for (int cc = cc_lo; cc < cc_hi; ++cc) {
-            float v[32];
-            tmem_ld32(tmem_base + lane_addr + tb * 256 + cc * 32, v);
-            if (all_visible) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc += ex2_approx(fmaf(v[i], cs, -s.lam[cc * 32 + i]));
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int r = cc * 32 + i;
-                const bool vis = j <= Tq + (r % a.W);
-                acc += vis ? ex2_approx(fmaf(v[i], cs, -s.lam[r])) : 0.f;
-              }
-            }
-          }
+          if (n_my_cc > 0)
+            tmem_chunks(tbuf, n_my_cc, [cc_lo](int q) { return (cc_lo + q) * 32; },
+                        [&](const uint32_t(&r)[32], int q) {
+                          const int cc = cc_lo + q;
+                          if (!masked) mass_accum(r, s.lam + cc * 32, cs, acc);
+                          else mass_accum_masked(r, s.lam + cc * 32, cs, cc * 32, j, Tq, a.W, acc);
+                        });
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
         } else {
           fail = true;
         }
-        if (hf == 1) s.red[qr * 32 + lane] = acc;
-        fail = named_bar_or(1, kEpiThreads, fail);
-        if (fail) break;
-        if (hf == 0) {
-          acc += s.red[qr * 32 + lane];
+        float part = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        float* red = s.red + (tbo * 2 + ((jt >> 1) & 1)) * 128;
+        if (half == 1) red[lrow] = part;
+        fail = named_bar_or(pair_bar, 256, fail);
+        if (fail) continue;      // the whole pair sees the same flag
+        if (half == 0) {
           float sc = -INFINITY;
           if (j < T) {
-            sc = acc;
-            if (a.bonus) sc += a.bonus[static_cast<int64_t>(b) * T + j];
-            float* dst = a.scores + static_cast<int64_t>(u) * T + j;
-            if (a.accumulate) sc += *dst;
+            sc = part + red[lrow] + extra;
             *dst = sc;
           }
           const int P = a.page_size;
@@ -421,8 +508,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
               a.page_scores[static_cast<int64_t>(u) * (T / P) + j / P] = pm;
           }
         }
-        named_bar_sync(1, kEpiThreads);
       }
+      // the next item's pass 1 rewrites hm / hl and lam only after this barrier
+      fail = named_bar_or(1, kEpiThreads, fail);
       if (fail) break;
     }
     if (fail && et == 0 && cur_u >= 0 && a.unit_status) a.unit_status[cur_u] = KVC_UNIT_TIMEOUT;
@@ -430,7 +518,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -445,7 +533,7 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages) {
   bytes += static_cast<size_t>(n_stages) * n_kc * kChunkBytes;
   bytes += (2 * n_stages + 8) * 8;                       // barriers
   bytes += 16;                                           // tmem slot, abort flag
-  bytes += (256 + 3 * 128) * 4;                          // lam, red, hm, hl
+  bytes += (256 + 512 + 2 * 1024) * 4;                  // lam, red, hm, hl
   return bytes;
 }
 

@@ -14,8 +14,9 @@
 // items still matching the key prefix and locate, with a block scan, the
 // bin where the running weight crosses the target.  Items above the final
 // key are taken; items equal to it are taken in index order while the
-// running weight still fits.  A last pass writes the kept indices in index
-// order with block-wide prefix sums, so every list comes out ascending.
+// running weight still fits.  A last phase writes the kept indices in index
+// order: each warp owns a contiguous range of items and the warps' offsets
+// come from two 32-entry scans, so every list comes out ascending.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -115,7 +116,7 @@ __device__ __forceinline__ uint32_t item_weight(const Ctx& c, const Item& it) {
   return c.a->byte_mode ? c.cost[KVC_ACT_BF16] - c.cost[it.base] : 1u;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectArgs a) {
   __shared__ uint32_t hist[2048];
   __shared__ unsigned long long wtot[32];
   __shared__ unsigned long long red[4];
@@ -283,44 +284,107 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a)
   }
 
   // ---------------- phase C: write the kept lists in index order
+  // Warp w owns the contiguous item range [w_lo, w_hi) and walks it 32 items
+  // at a time: (1) total tie weight per warp, scanned across warps; (2) the
+  // promotion decisions and per-pool counts, scanned across warps; (3) the
+  // same decisions again, writing each kept item at its final position.
+  __shared__ unsigned long long s_tie[32];
+  __shared__ uint32_t s_pool[KVC_N_POOLS][32];
+  const int warp = tid >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int64_t per_w = (c.n + 32 * 32 - 1) / (32 * 32) * 32;
+  const int64_t w_lo = min(c.n, static_cast<int64_t>(warp) * per_w);
+  const int64_t w_hi = min(c.n, w_lo + per_w);
   const unsigned long long tie_slack = a.byte_mode ? 0ull : 1ull;
-  unsigned long long tie_carry = 0;
-  uint32_t carry[KVC_N_POOLS] = {0, 0, 0};
   const int P = a.page_size;
-  for (int64_t c0 = 0; c0 < c.n; c0 += kThreads) {
-    const int64_t i = c0 + tid;
-    const bool valid = i < c.n;
+
+  auto tie_weight = [&](const Item& it) -> unsigned long long {
+    const bool cand = it.key != 0 && !sel_none;
+    return (cand && !sel_all && it.key == tau) ? item_weight(c, it) : 0ull;
+  };
+  auto decide = [&](const Item& it, unsigned long long tie_before, unsigned long long tw) -> uint32_t {
+    const bool cand = it.key != 0 && !sel_none;
+    const bool promoted =
+        cand && (sel_all || it.key > tau || (tw > 0 && tie_before + tw <= t + tie_slack));
+    return promoted ? KVC_ACT_BF16 : it.base;
+  };
+  auto load = [&](int64_t i) -> Item {
     Item it;
     it.key = 0;
     it.base = KVC_ACT_RELEASE;
-    if (valid) it = get(i, err);
-    const bool cand = it.key != 0 && !sel_none;
-    const bool is_tie = cand && !sel_all && it.key == tau;
-    const unsigned long long tw = is_tie ? item_weight(c, it) : 0ull;
-    unsigned long long tie_total;
-    const unsigned long long tie_before = tie_carry + block_excl_scan<unsigned long long>(tw, wtot, tie_total);
-    tie_carry += tie_total;
-    const bool promoted =
-        cand && (sel_all || it.key > tau || (is_tie && tie_before + tw <= t + tie_slack));
-    const uint32_t act = promoted ? KVC_ACT_BF16 : it.base;
-    unsigned long long bits = 0;
-    if (valid && act != KVC_ACT_RELEASE) bits = 1ull << (16 * (act - 1));
-    unsigned long long pool_total;
-    const unsigned long long before = block_excl_scan<unsigned long long>(bits, wtot, pool_total);
-    if (bits) {
-      const int pool = act - 1;
-      const uint32_t pos = carry[pool] + static_cast<uint32_t>((before >> (16 * pool)) & 0xffff);
-      int32_t* dst = a.kept_idx + (static_cast<int64_t>(pool) * a.U + c.u) * a.capacity;
-      if (P == 1) {
-        dst[pos] = static_cast<int32_t>(i);
-      } else {
-        for (int q = 0; q < P; ++q) dst[static_cast<int64_t>(pos) * P + q] = static_cast<int32_t>(i * P + q);
-      }
-    }
-    for (int pool = 0; pool < KVC_N_POOLS; ++pool)
-      carry[pool] += static_cast<uint32_t>((pool_total >> (16 * pool)) & 0xffff);
+    if (i < w_hi) it = get(i, err);
+    return it;
+  };
+
+  // (1) tie weight per warp
+  unsigned long long tie_tot = 0;
+  for (int64_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+    unsigned long long tw = tie_weight(load(i0 + lane));
+    for (int o = 16; o > 0; o >>= 1) tw += __shfl_xor_sync(kFull, tw, o);
+    tie_tot += tw;
   }
-  if (tid < KVC_N_POOLS) cnt[tid * a.U + c.u] = static_cast<int32_t>(carry[tid]) * P;
+  if (lane == 0) s_tie[warp] = tie_tot;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long v = s_tie[lane];
+    s_tie[lane] = warp_incl_scan(v, lane) - v;
+  }
+  __syncthreads();
+  // (2) decisions and pool counts per warp
+  uint32_t pc[KVC_N_POOLS] = {0, 0, 0};
+  unsigned long long tie_run = s_tie[warp];
+  for (int64_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+    const int64_t i = i0 + lane;
+    const Item it = load(i);
+    const unsigned long long tw = tie_weight(it);
+    const unsigned long long incl = warp_incl_scan(tw, lane);
+    const uint32_t act = (i < w_hi) ? decide(it, tie_run + incl - tw, tw) : KVC_ACT_RELEASE;
+    tie_run += __shfl_sync(kFull, incl, 31);
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) pc[q] += __popc(__ballot_sync(kFull, act == q + 1u));
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) s_pool[q][warp] = pc[q];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) {
+      const uint32_t v = s_pool[q][lane];
+      s_pool[q][lane] = warp_incl_scan(v, lane);        // inclusive: entry 31 is the total
+    }
+  }
+  __syncthreads();
+  // (3) write
+  uint32_t pos_run[KVC_N_POOLS];
+#pragma unroll
+  for (int q = 0; q < KVC_N_POOLS; ++q) pos_run[q] = warp ? s_pool[q][warp - 1] : 0u;
+  tie_run = s_tie[warp];
+  for (int64_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+    const int64_t i = i0 + lane;
+    const Item it = load(i);
+    const unsigned long long tw = tie_weight(it);
+    const unsigned long long incl = warp_incl_scan(tw, lane);
+    const uint32_t act = (i < w_hi) ? decide(it, tie_run + incl - tw, tw) : KVC_ACT_RELEASE;
+    tie_run += __shfl_sync(kFull, incl, 31);
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) {
+      const unsigned m = __ballot_sync(kFull, act == q + 1u);
+      if (act == q + 1u) {
+        const uint32_t pos = pos_run[q] + __popc(m & lt_mask);
+        int32_t* dst = a.kept_idx + (static_cast<int64_t>(q) * a.U + c.u) * a.capacity;
+        if (P == 1) {
+          dst[pos] = static_cast<int32_t>(i);
+        } else {
+          for (int k = 0; k < P; ++k)
+            dst[static_cast<int64_t>(pos) * P + k] = static_cast<int32_t>(i * P + k);
+        }
+      }
+      pos_run[q] += __popc(m);
+    }
+  }
+  if (tid < KVC_N_POOLS) cnt[tid * a.U + c.u] = static_cast<int32_t>(s_pool[tid][31]) * P;
   if (tid == 0) {
     a.unit_status[c.u] = KVC_UNIT_OK;
     if (a.floor_excess) a.floor_excess[c.u] = excess;
