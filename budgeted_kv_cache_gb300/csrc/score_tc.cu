@@ -25,9 +25,10 @@
 //
 // Warp roles (18 warps): 0 = TMA producer, 1 = TMEM owner and MMA issuer,
 // 2..17 = epilogue, four warpgroups that each cover the four TMEM lane
-// quarters (warp w reads lanes 32 (w % 4) .. 32 (w % 4) + 31).  Warpgroups
-// 2b and 2b+1 share TMEM buffer b and split its columns, so every SM
-// sub-partition runs four epilogue warps.
+// quarters (warp w reads lanes 32 (w % 4) .. 32 (w % 4) + 31).  All four
+// warpgroups work on every tile, each on a quarter of its columns, while the
+// MMA warp fills the other TMEM buffer; every SM sub-partition runs four
+// epilogue warps.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -55,7 +56,7 @@ struct Smem {
   uint32_t* tmem_slot;
   int* abort_flag;
   float* lam;           // [256] negated log-sum-exp of each window row
-  float* red;           // [2 buffers][2 parities][128] pass-2 partial sums
+  float* red;           // [2 parities][4 groups][128] pass-2 partial sums
   float* hm;            // [4 groups][256] pass-1 partial max
   float* hl;            // [4 groups][256] pass-1 partial sum
 };
@@ -76,7 +77,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.lam = reinterpret_cast<float*>(s.tmem_slot + 4);
   s.red = s.lam + 256;
-  s.hm = s.red + 512;
+  s.hm = s.red + 1024;
   s.hl = s.hm + 1024;
   return s;
 }
@@ -91,7 +92,8 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
 }
 
 // Online max / sum update of one window row with 32 more raw logits
-// (pass 1, log2 domain: y = z * cs).  Masked logits are -inf.
+// (pass 1, log2 domain: y = z * cs).  Masked logits are -inf.  Pairs of
+// logits go through packed two-lane fp32 multiply-add / add instructions.
 __device__ __forceinline__ void row_update(const uint32_t (&r)[32], float cs, bool masked,
                                            int64_t j0, int64_t last, float& m, float& l) {
   float v[32];
@@ -115,26 +117,37 @@ __device__ __forceinline__ void row_update(const uint32_t (&r)[32], float cs, bo
     m = mc;
   }
   if (m == -INFINITY) return;
-  const float nm = -m;
-  float sm[8];
+  const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-m, -m);
+  float2 s2[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) sm[k] = ex2_approx(fmaf(v[k], cs, nm));
+  for (int k = 0; k < 4; ++k) {
+    const float2 x = __ffma2_rn(make_float2(v[2 * k], v[2 * k + 1]), cs2, nm2);
+    s2[k] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+  }
 #pragma unroll
-  for (int i = 8; i < 32; ++i) sm[i & 7] += ex2_approx(fmaf(v[i], cs, nm));
-  l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+  for (int i = 8; i < 32; i += 2) {
+    const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), cs2, nm2);
+    s2[(i >> 1) & 3] = __fadd2_rn(s2[(i >> 1) & 3], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+  }
+  const float2 u2 = __fadd2_rn(__fadd2_rn(s2[0], s2[1]), __fadd2_rn(s2[2], s2[3]));
+  l += u2.x + u2.y;
 }
 
-// Pass 2: add exp2(z * cs - lse_r) of 32 rows r to the token's mass (eight
-// running partial sums).  nlam holds -lse of those 32 rows.
+// Pass 2: add exp2(z * cs - lse_r) of 32 rows r to the token's mass (four
+// packed pairs of running sums).  nlam holds -lse of those 32 rows.
 __device__ __forceinline__ void mass_accum(const uint32_t (&r)[32], const float* nlam, float cs,
-                                           float (&acc)[8]) {
+                                           float2 (&acc)[4]) {
+  const float2 cs2 = make_float2(cs, cs);
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
     const float4 nl = *reinterpret_cast<const float4*>(nlam + i);
-    acc[(i >> 2) & 7] += ex2_approx(fmaf(__uint_as_float(r[i]), cs, nl.x));
-    acc[((i >> 2) + 1) & 7] += ex2_approx(fmaf(__uint_as_float(r[i + 1]), cs, nl.y));
-    acc[((i >> 2) + 2) & 7] += ex2_approx(fmaf(__uint_as_float(r[i + 2]), cs, nl.z));
-    acc[((i >> 2) + 3) & 7] += ex2_approx(fmaf(__uint_as_float(r[i + 3]), cs, nl.w));
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), cs2,
+                                make_float2(nl.x, nl.y));
+    const float2 y = __ffma2_rn(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
+                                cs2, make_float2(nl.z, nl.w));
+    const int k = (i >> 2) & 1;
+    acc[2 * k] = __fadd2_rn(acc[2 * k], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+    acc[2 * k + 1] = __fadd2_rn(acc[2 * k + 1], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
   }
 }
 
@@ -142,11 +155,13 @@ __device__ __forceinline__ void mass_accum(const uint32_t (&r)[32], const float*
 // j <= Tq + (r0 + i) mod W.
 __device__ __forceinline__ void mass_accum_masked(const uint32_t (&r)[32], const float* nlam,
                                                   float cs, int r0, int64_t j, int64_t Tq, int W,
-                                                  float (&acc)[8]) {
+                                                  float2 (&acc)[4]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const bool vis = j <= Tq + ((r0 + i) % W);
-    acc[i & 7] += vis ? ex2_approx(fmaf(__uint_as_float(r[i]), cs, nlam[i])) : 0.f;
+  for (int i = 0; i < 32; i += 2) {
+    const bool v0 = j <= Tq + ((r0 + i) % W), v1 = j <= Tq + ((r0 + i + 1) % W);
+    const float e0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[i]), cs, nlam[i])) : 0.f;
+    const float e1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[i + 1]), cs, nlam[i + 1])) : 0.f;
+    acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], make_float2(e0, e1));
   }
 }
 
@@ -163,6 +178,7 @@ __device__ __forceinline__ void tmem_chunks(uint32_t tbuf, int nq, ColF col, Pro
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
              const ScoreArgs a) {
@@ -170,7 +186,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
   // 1024-byte aligned start, formed by pointer arithmetic on the shared array
   // so that the compiler keeps every derived pointer in the shared space
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int n_kc = a.d / 64;
+  constexpr int n_kc = D / 64;
   const Smem s = carve(base, n_kc, a.q_rows, a.n_stages);
   const uint32_t q_chunk_bytes = static_cast<uint32_t>(a.q_rows) * 128u;
   const uint32_t stage_bytes = static_cast<uint32_t>(n_kc) * kChunkBytes;
@@ -185,7 +201,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
-      mbar_init(smem_u32(&s.tempty[i]), 8);   // one arrival per warp of the two owning warpgroups
+      mbar_init(smem_u32(&s.tempty[i]), kEpiThreads / 32);   // one arrival per epilogue warp
     }
     mbar_init(smem_u32(s.qfull), 1);
     mbar_init(smem_u32(s.qempty), 1);
@@ -263,8 +279,15 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     if (lane == 0) {
       const uint32_t idesc1 = mma_idesc_bf16(128, 128);
       const uint32_t idesc2 = mma_idesc_bf16(128, a.R);
-      const uint32_t q_base = smem_u32(s.q);
-      const int ksteps = a.d / 16;
+      // Operand descriptors: one base descriptor per buffer, every k-step and
+      // stage reached by adding its byte offset / 16 to the start-address
+      // field (shared addresses stay below 2^18, so the field never carries).
+      // This keeps the issuing thread to a few instructions per MMA, which
+      // matters because it shares its sub-partition with busy epilogue warps.
+      constexpr int KS = D / 16;
+      const uint64_t qdesc0 = sw128_desc(smem_u32(s.q));
+      const uint64_t kdesc0 = sw128_desc(smem_u32(s.k));
+      const uint32_t qchunk16 = q_chunk_bytes >> 4;
       uint32_t jt = 0;
       int li = 0;
       for (int it = blockIdx.x; it < a.n_items; it += gridDim.x, ++li) {
@@ -286,21 +309,24 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
               break;
             }
             tc_fence_after();
-            const uint32_t k_base = smem_u32(s.k + st * stage_bytes);
+            const uint64_t kd = kdesc0 + ((st * stage_bytes) >> 4);
             const uint32_t d_tmem = tmem_base + tb * 256;
             if (pass == 0) {
-              for (int rb = 0; rb < n_rb; ++rb)
-                for (int ks = 0; ks < ksteps; ++ks) {
-                  const uint32_t kc = ks >> 2, kb = (ks & 3) * 32;
-                  const uint64_t ad = sw128_desc(q_base + kc * q_chunk_bytes + rb * kChunkBytes + kb);
-                  const uint64_t bd = sw128_desc(k_base + kc * kChunkBytes + kb);
+#pragma unroll
+              for (int rb = 0; rb < 2; ++rb) {
+                if (rb >= n_rb) break;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                  const uint64_t ad = qdesc0 + ((ks >> 2) * qchunk16 + rb * (kChunkBytes >> 4) + (ks & 3) * 2);
+                  const uint64_t bd = kd + ((ks >> 2) * (kChunkBytes >> 4) + (ks & 3) * 2);
                   tc_mma_bf16(d_tmem + rb * 128, ad, bd, idesc1, ks > 0);
                 }
+              }
             } else {
-              for (int ks = 0; ks < ksteps; ++ks) {
-                const uint32_t kc = ks >> 2, kb = (ks & 3) * 32;
-                const uint64_t ad = sw128_desc(k_base + kc * kChunkBytes + kb);
-                const uint64_t bd = sw128_desc(q_base + kc * q_chunk_bytes + kb);
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks) {
+                const uint64_t ad = kd + ((ks >> 2) * (kChunkBytes >> 4) + (ks & 3) * 2);
+                const uint64_t bd = qdesc0 + ((ks >> 2) * qchunk16 + (ks & 3) * 2);
                 tc_mma_bf16(d_tmem, ad, bd, idesc2, ks > 0);
               }
             }
@@ -317,31 +343,24 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
-    // Warpgroup g (0..3) owns TMEM buffer tb = g % 2, i.e. every tile whose
-    // running index jt has jt % 2 == tb, and column half h = g / 2 of it:
-    // in pass 1 token columns [64 h, 64 h + 64) of each row block, in pass 2
-    // window rows [R/2 h, R/2 (h + 1)).  The two groups of a buffer meet at a
-    // per-tile pair barrier in pass 2 to add their halves of each token's sum.
+    // All four warpgroups process every tile; warpgroup g takes token
+    // columns [32 g, 32 g + 32) of each row block in pass 1 and a quarter of
+    // the window rows in pass 2.  Tile jt lives in TMEM buffer jt % 2.
     // Every named barrier is an OR-reduction of a failure flag, and no thread
     // leaves the item loop between two of them, so a bounded wait that gives
     // up in one warp ends all epilogue warps at the same barrier.
     const int e = warp - kEpiWarp0;            // 0..15
     const int qr = warp & 3;                   // TMEM lane quarter of this warp
     const int grp = e >> 2;                    // 0..3
-    const uint32_t tbo = static_cast<uint32_t>(grp & 1);   // TMEM buffer of this group
-    const int half = grp >> 1;
-    const int pair_bar = 2 + static_cast<int>(tbo);        // named barrier of the buffer's pair
     const int et = threadIdx.x - kEpiWarp0 * 32;
     const int lrow = qr * 32 + lane;           // TMEM lane of this thread
     const uint32_t lane_addr = static_cast<uint32_t>(qr * 32) << 16;
-    const uint32_t tbuf = tmem_base + lane_addr + tbo * 256;
     const float cs = a.scale_log2;
     const int64_t T = a.T;
     const int64_t Tq = T - a.W;                // row w sees keys j <= Tq + w
     const int n_cc = a.R / 32;
-    const int cc_split = (n_cc + 1) / 2;
-    const int cc_lo = half ? cc_split : 0;
-    const int n_my_cc = half ? n_cc - cc_split : cc_split;
+    const int cc_lo = (n_cc * grp) / 4;
+    const int n_my_cc = (n_cc * (grp + 1)) / 4 - cc_lo;
     // pass-1 rows of this thread: lrow + 128 rb, rb < n_rb
     bool rvalid[2];
     int64_t rlast[2];
@@ -366,20 +385,18 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
       for (int t = 0; t < nt; ++t, ++jt) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
-        if (tb != tbo) continue;
         if (fail || !mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
           fail = true;
           continue;
         }
         tc_fence_after();
-        const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + 64 * half;
-        const bool masked = (j0 + 63) > Tq;
-        tmem_chunks(tbuf, 2 * n_rb,
-                    [half](int q) { return (q >> 1) * 128 + 64 * half + (q & 1) * 32; },
+        const uint32_t tbuf = tmem_base + lane_addr + tb * 256;
+        const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + 32 * grp;
+        const bool masked = (j0 + 31) > Tq;
+        tmem_chunks(tbuf, n_rb, [grp](int q) { return q * 128 + 32 * grp; },
                     [&](const uint32_t(&r)[32], int q) {
-                      const int64_t jc = j0 + (q & 1) * 32;
-                      if (q < 2) row_update(r, cs, masked, jc, rlast[0], m0, l0);
-                      else       row_update(r, cs, masked, jc, rlast[1], m1, l1);
+                      if (q == 0) row_update(r, cs, masked, j0, rlast[0], m0, l0);
+                      else        row_update(r, cs, masked, j0, rlast[1], m1, l1);
                     });
         tc_fence_before();
         __syncwarp();
@@ -463,19 +480,20 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       // ---------------- pass 2: per-token sum of exp2(z cs - lse) over rows
       for (int t = 0; t < nt; ++t, ++jt) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
-        if (tb != tbo) continue;
         const int64_t tile0 = static_cast<int64_t>(t0 + t) * kTileTokens;
         const int64_t j = tile0 + lrow;
         const bool masked = (tile0 + kTileTokens - 1) > Tq;
         float* dst = a.scores + static_cast<int64_t>(u) * T + j;
         float extra = 0.f;
-        if (half == 0 && j < T) {     // global inputs, loaded before the TMEM work
+        if (grp == 0 && j < T) {      // global inputs, loaded before the TMEM work
           if (a.bonus) extra += __ldg(a.bonus + static_cast<int64_t>(b) * T + j);
           if (a.accumulate) extra += *dst;
         }
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
         if (!fail && mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
           tc_fence_after();
+          const uint32_t tbuf = tmem_base + lane_addr + tb * 256;
           if (n_my_cc > 0)
             tmem_chunks(tbuf, n_my_cc, [cc_lo](int q) { return (cc_lo + q) * 32; },
                         [&](const uint32_t(&r)[32], int q) {
@@ -489,15 +507,15 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         } else {
           fail = true;
         }
-        float part = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-        float* red = s.red + (tbo * 2 + ((jt >> 1) & 1)) * 128;
-        if (half == 1) red[lrow] = part;
-        fail = named_bar_or(pair_bar, 256, fail);
-        if (fail) continue;      // the whole pair sees the same flag
-        if (half == 0) {
+        float* red = s.red + (jt & 1) * 512;      // consecutive tiles alternate slots
+        const float2 a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        red[grp * 128 + lrow] = a2.x + a2.y;
+        fail = named_bar_or(2, kEpiThreads, fail);
+        if (fail) continue;      // every epilogue thread sees the same flag
+        if (grp == 0) {
           float sc = -INFINITY;
           if (j < T) {
-            sc = part + red[lrow] + extra;
+            sc = ((red[lrow] + red[128 + lrow]) + (red[256 + lrow] + red[384 + lrow])) + extra;
             *dst = sc;
           }
           const int P = a.page_size;
@@ -533,13 +551,15 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages) {
   bytes += static_cast<size_t>(n_stages) * n_kc * kChunkBytes;
   bytes += (2 * n_stages + 8) * 8;                       // barriers
   bytes += 16;                                           // tmem slot, abort flag
-  bytes += (256 + 512 + 2 * 1024) * 4;                  // lam, red, hm, hl
+  bytes += (256 + 1024 + 2 * 1024) * 4;                 // lam, red, hm, hl
   return bytes;
 }
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q,
                          int grid, size_t smem_bytes, cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  void (*kern)(const CUtensorMap, const CUtensorMap, const ScoreArgs) =
+      a.d == 64 ? score_kernel<64> : score_kernel<128>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -552,7 +572,7 @@ cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CU
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_kernel, tmap_k, tmap_q, a);
+  return cudaLaunchKernelEx(&cfg, kern, tmap_k, tmap_q, a);
 }
 
 }  // namespace kvc
