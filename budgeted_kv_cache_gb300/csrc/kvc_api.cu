@@ -325,7 +325,7 @@ kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const fl
   a.unit_status = unit_status;
   a.floor_excess = floor_excess;
   const size_t cache_bytes = static_cast<size_t>(sp.n_items) * 5;
-  a.cache_items = cache_bytes <= 200 * 1024 ? 1 : 0;
+  a.cache_items = cache_bytes <= 190 * 1024 ? 1 : 0;   // + 34 KB static shared memory
   const size_t smem = a.cache_items ? (cache_bytes + 15) / 16 * 16 : 0;
   if (launch_select(a, static_cast<cudaStream_t>(stream), smem) != cudaSuccess) return KVC_ERR_CUDA;
   return KVC_OK;

@@ -9,10 +9,10 @@
 // order to bf16.
 //
 // Both are one weighted radix select on a 32-bit order key (1 per item in
-// token mode, the upgrade cost in byte mode): three digit passes (11, 11,
-// 10 bits) each build a warp-aggregated shared-memory histogram of the
-// items still matching the key prefix and locate, with a block scan, the
-// bin where the running weight crosses the target.  Items above the final
+// token mode, the upgrade cost in byte mode): four 8-bit digit passes each
+// build per-warp shared-memory histograms of the items still matching the
+// key prefix and locate, with a block scan, the bin where the running weight
+// crosses the target.  Items above the final
 // key are taken; items equal to it are taken in index order while the
 // running weight still fits.  A last phase writes the kept indices in index
 // order: each warp owns a contiguous range of items and the warps' offsets
@@ -117,10 +117,11 @@ __device__ __forceinline__ uint32_t item_weight(const Ctx& c, const Item& it) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectArgs a) {
-  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t hist_w[32 * 256];     // per-warp histograms
   __shared__ unsigned long long wtot[32];
   __shared__ unsigned long long red[4];
   __shared__ int s_bin;
+  __shared__ uint32_t s_kmin, s_kmax;
   __shared__ unsigned long long s_above;
   extern __shared__ uint8_t dsm[];
 
@@ -146,7 +147,6 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
 
   uint32_t* ckey = reinterpret_cast<uint32_t*>(dsm);
   uint8_t* cbase = dsm + 4 * (a.cache_items ? c.n : 0);
-  const int64_t n_pad = (c.n + kThreads - 1) / kThreads * kThreads;
 
   auto get = [&](int64_t i, int& err) -> Item {
     if (a.cache_items) {
@@ -159,37 +159,67 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   };
 
   // ---------------- phase A: classify, count, charge floors
+  // Four independent items per thread per iteration keep several loads in
+  // flight.  The smallest and largest candidate keys are kept too: the radix
+  // passes below start at the highest bit where they differ.
   if (tid < 4) red[tid] = 0;
+  if (tid == 0) {
+    s_kmin = 0xffffffffu;
+    s_kmax = 0u;
+  }
   __syncthreads();
   unsigned long long n_forced = 0, n_cand = 0, floor_bytes = 0;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
   int err = 0;
-  for (int64_t i = tid; i < c.n; i += kThreads) {
-    const Item it = eval_item(c, i, err);
-    if (a.cache_items) {
-      ckey[i] = it.key;
-      cbase[i] = it.base;
+  for (int64_t i0 = tid; i0 < c.n; i0 += 4 * kThreads) {
+    Item it[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + k * kThreads;
+      it[k].key = 0;
+      it[k].base = KVC_ACT_RELEASE;
+      if (i < c.n) it[k] = eval_item(c, i, err);
     }
-    n_forced += (!a.byte_mode && it.base == KVC_ACT_BF16);
-    n_cand += (it.key != 0);
-    floor_bytes += c.cost[it.base];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + k * kThreads;
+      if (i >= c.n) continue;
+      if (a.cache_items) {
+        ckey[i] = it[k].key;
+        cbase[i] = it[k].base;
+      }
+      n_forced += (!a.byte_mode && it[k].base == KVC_ACT_BF16);
+      n_cand += (it[k].key != 0);
+      floor_bytes += c.cost[it[k].base];
+      if (it[k].key != 0) {
+        kmin = min(kmin, it[k].key);
+        kmax = max(kmax, it[k].key);
+      }
+    }
   }
   for (int o = 16; o > 0; o >>= 1) {
     n_forced += __shfl_xor_sync(kFull, n_forced, o);
     n_cand += __shfl_xor_sync(kFull, n_cand, o);
     floor_bytes += __shfl_xor_sync(kFull, floor_bytes, o);
     err |= __shfl_xor_sync(kFull, err, o);
+    kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
   }
   if (lane == 0) {
     atomicAdd(&red[0], n_forced);
     atomicAdd(&red[1], n_cand);
     atomicAdd(&red[2], floor_bytes);
     atomicOr(reinterpret_cast<unsigned int*>(&red[3]), static_cast<unsigned int>(err));
+    atomicMin(&s_kmin, kmin);
+    atomicMax(&s_kmax, kmax);
   }
   __syncthreads();
   n_forced = red[0];
   n_cand = red[1];
   floor_bytes = red[2];
   err = static_cast<int>(red[3]);
+  kmin = s_kmin;
+  kmax = s_kmax;
 
   int32_t* cnt = a.kept_count;
   if (err) {
@@ -227,47 +257,44 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   }
 
   // ---------------- phase B: weighted radix select of the crossing key
+  // 8-bit digits, most significant first, over the bits where candidate
+  // keys can differ (those above the highest bit of kmin ^ kmax are common).
+  // Each warp builds a private 256-bin histogram of its own contiguous item
+  // range, the 32 histograms are summed, and a block scan over the bins
+  // (highest first) finds the bin where the running weight crosses t.
   uint32_t tau = 0;
-  if (!sel_none) {
-    uint32_t prefix = 0;
-    for (int p = 0; p < 3; ++p) {
-      const int shift = p == 0 ? 21 : (p == 1 ? 10 : 0);
-      const int bits = p == 2 ? 10 : 11;
-      const int nb = 1 << bits;
-      for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (int64_t i = tid; i < n_pad; i += kThreads) {
-        bool active = false;
-        uint32_t bin = 0, w = 0;
-        if (i < c.n) {
-          const Item it = get(i, err);
-          active = it.key != 0 && (p == 0 || (it.key >> (shift + bits)) == prefix);
-          bin = (it.key >> shift) & (nb - 1);
-          w = item_weight(c, it);
-        }
-        const unsigned act_mask = __ballot_sync(kFull, active);
-        if (active) {
-          const unsigned peers = __match_any_sync(act_mask, bin);
-          const uint32_t sum = a.byte_mode ? __reduce_add_sync(peers, w) : __popc(peers);
-          if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], sum);
-        }
+  if (!sel_none && n_cand > 0) {
+    const int warp = tid >> 5;
+    const int64_t per_w = (c.n + 32 * 32 - 1) / (32 * 32) * 32;
+    const int64_t w_lo = min(c.n, static_cast<int64_t>(warp) * per_w);
+    const int64_t w_hi = min(c.n, w_lo + per_w);
+    uint32_t* whist = hist_w + warp * 256;
+    const int top = (kmin == kmax) ? -1 : 31 - __clz(kmin ^ kmax);
+    uint64_t pfx = static_cast<uint64_t>(kmax) >> (top + 1);   // common high bits
+    for (int hi = top; hi >= 0; hi -= 8) {
+      const int shift = max(0, hi - 7);
+      const int width = hi - shift + 1;
+      const uint32_t nb = 1u << width;
+      for (int i = lane; i < 256; i += 32) whist[i] = 0;
+      __syncwarp();
+      for (int64_t i = w_lo + lane; i < w_hi; i += 32) {
+        const Item it = get(i, err);
+        if (it.key != 0 && (static_cast<uint64_t>(it.key) >> (hi + 1)) == pfx)
+          atomicAdd(&whist[(it.key >> shift) & (nb - 1)], item_weight(c, it));
       }
       if (tid == 0) s_bin = -1;
       __syncthreads();
-      // bins in descending order: thread tid owns bins nb-1-(tid*per+k)
-      const int per = nb / kThreads;
+      // thread b < nb sums bin nb - 1 - b over the warps (descending bin order)
       unsigned long long local = 0;
-      for (int k = 0; k < per; ++k) local += hist[nb - 1 - (tid * per + k)];
+      if (tid < static_cast<int>(nb)) {
+        const int bn = static_cast<int>(nb) - 1 - tid;
+        for (int w = 0; w < 32; ++w) local += hist_w[w * 256 + bn];
+      }
       unsigned long long total;
-      unsigned long long run = block_excl_scan<unsigned long long>(local, wtot, total);
-      for (int k = 0; k < per; ++k) {
-        const int bn = nb - 1 - (tid * per + k);
-        const unsigned long long h = hist[bn];
-        if (run <= t && t < run + h) {
-          s_bin = bn;
-          s_above = run;
-        }
-        run += h;
+      const unsigned long long run = block_excl_scan<unsigned long long>(local, wtot, total);
+      if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
+        s_bin = static_cast<int>(nb) - 1 - tid;
+        s_above = run;
       }
       __syncthreads();
       const int bn = s_bin;
@@ -278,16 +305,23 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
         break;
       }
       t -= above;
-      prefix = (prefix << bits) | static_cast<uint32_t>(bn);
+      pfx = (pfx << width) | static_cast<uint32_t>(bn);
     }
-    tau = prefix;
+    tau = static_cast<uint32_t>(pfx);
+    // (one distinct key: no pass runs, every candidate is a tie at tau)
+  } else if (!sel_none) {
+    sel_all = true;          // no candidates: nothing to promote
   }
 
   // ---------------- phase C: write the kept lists in index order
   // Warp w owns the contiguous item range [w_lo, w_hi) and walks it 32 items
-  // at a time: (1) total tie weight per warp, scanned across warps; (2) the
-  // promotion decisions and per-pool counts, scanned across warps; (3) the
-  // same decisions again, writing each kept item at its final position.
+  // at a time, twice.  Walk 1 counts, per pool, the items whose action does
+  // not depend on a tie, and the ties (items with key == tau) with their
+  // weight.  Ties are taken in index order while their running weight fits,
+  // so after a scan of the tie weights over the warps each warp knows how
+  // many of its ties are kept (a warp straddling the cut in byte mode counts
+  // its own).  A scan of the per-pool counts gives every warp its output
+  // offsets; walk 2 repeats the decisions and writes each kept item.
   __shared__ unsigned long long s_tie[32];
   __shared__ uint32_t s_pool[KVC_N_POOLS][32];
   const int warp = tid >> 5;
@@ -316,33 +350,77 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     return it;
   };
 
-  // (1) tie weight per warp
-  unsigned long long tie_tot = 0;
+  // walk 1
+  uint32_t pc[KVC_N_POOLS] = {0, 0, 0};       // tie-independent items per pool
+  uint32_t tb_pc[KVC_N_POOLS] = {0, 0, 0};    // ties per pool of their unpromoted action
+  uint32_t tie_n = 0;
+  unsigned long long tie_w = 0;
   for (int64_t i0 = w_lo; i0 < w_hi; i0 += 32) {
-    unsigned long long tw = tie_weight(load(i0 + lane));
-    for (int o = 16; o > 0; o >>= 1) tw += __shfl_xor_sync(kFull, tw, o);
-    tie_tot += tw;
+    const Item it = load(i0 + lane);
+    const unsigned long long tw = tie_weight(it);
+    const bool tie = tw != 0;
+    const uint32_t act = (i0 + lane < w_hi && !tie) ? decide(it, 0, 0) : KVC_ACT_RELEASE;
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) pc[q] += __popc(__ballot_sync(kFull, act == q + 1u));
+    const unsigned tm = __ballot_sync(kFull, tie);
+    if (tm) {
+      tie_n += __popc(tm);
+      unsigned long long ws = tw;
+      for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(kFull, ws, o);
+      tie_w += ws;
+#pragma unroll
+      for (int q = 0; q < KVC_N_POOLS; ++q) tb_pc[q] += __popc(__ballot_sync(kFull, tie && it.base == q + 1u));
+    }
   }
-  if (lane == 0) s_tie[warp] = tie_tot;
+  if (lane == 0) s_tie[warp] = a.byte_mode ? tie_w : tie_n;
   __syncthreads();
   if (warp == 0) {
     const unsigned long long v = s_tie[lane];
-    s_tie[lane] = warp_incl_scan(v, lane) - v;
+    s_tie[lane] = warp_incl_scan(v, lane) - v;     // exclusive offsets
   }
   __syncthreads();
-  // (2) decisions and pool counts per warp
-  uint32_t pc[KVC_N_POOLS] = {0, 0, 0};
-  unsigned long long tie_run = s_tie[warp];
-  for (int64_t i0 = w_lo; i0 < w_hi; i0 += 32) {
-    const int64_t i = i0 + lane;
-    const Item it = load(i);
-    const unsigned long long tw = tie_weight(it);
-    const unsigned long long incl = warp_incl_scan(tw, lane);
-    const uint32_t act = (i < w_hi) ? decide(it, tie_run + incl - tw, tw) : KVC_ACT_RELEASE;
-    tie_run += __shfl_sync(kFull, incl, 31);
-#pragma unroll
-    for (int q = 0; q < KVC_N_POOLS; ++q) pc[q] += __popc(__ballot_sync(kFull, act == q + 1u));
+  const unsigned long long tie_off = s_tie[warp];
+  // kept ties of this warp: a prefix of its ties in index order
+  const unsigned long long my_tie_total = a.byte_mode ? tie_w : tie_n;
+  bool partial = false;
+  uint32_t prom = 0;
+  if (tie_n > 0) {
+    if (tie_off + my_tie_total <= t + tie_slack) prom = tie_n;
+    else if (tie_off >= t + tie_slack) prom = 0;
+    else if (!a.byte_mode) prom = static_cast<uint32_t>(t + 1 - tie_off);
+    else partial = true;
   }
+  if (partial) {              // byte mode, the warp where the cut falls: count exactly
+    unsigned long long tie_run = tie_off;
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) tb_pc[q] = 0;
+    prom = 0;
+    for (int64_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+      const Item it = load(i0 + lane);
+      const unsigned long long tw = tie_weight(it);
+      if (!__any_sync(kFull, tw != 0)) continue;
+      const unsigned long long incl = warp_incl_scan(tw, lane);
+      const uint32_t act = decide(it, tie_run + incl - tw, tw);
+      tie_run += __shfl_sync(kFull, incl, 31);
+      prom += __popc(__ballot_sync(kFull, tw != 0 && act == KVC_ACT_BF16));
+#pragma unroll
+      for (int q = 0; q < KVC_N_POOLS; ++q)
+        tb_pc[q] += __popc(__ballot_sync(kFull, tw != 0 && act != KVC_ACT_BF16 && act == q + 1u));
+    }
+  } else if (prom == tie_n) {
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) tb_pc[q] = 0;
+  } else if (prom > 0) {       // count mode: ties are never stored unpromoted
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) tb_pc[q] = 0;
+  }
+  if (!a.byte_mode) {
+#pragma unroll
+    for (int q = 0; q < KVC_N_POOLS; ++q) tb_pc[q] = 0;   // unpromoted token-mode ties are released
+  }
+  pc[KVC_POOL_BF16] += prom;
+#pragma unroll
+  for (int q = 0; q < KVC_N_POOLS; ++q) pc[q] += tb_pc[q];
   if (lane == 0) {
 #pragma unroll
     for (int q = 0; q < KVC_N_POOLS; ++q) s_pool[q][warp] = pc[q];
@@ -356,17 +434,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
     }
   }
   __syncthreads();
-  // (3) write
+  // walk 2: write
   uint32_t pos_run[KVC_N_POOLS];
 #pragma unroll
   for (int q = 0; q < KVC_N_POOLS; ++q) pos_run[q] = warp ? s_pool[q][warp - 1] : 0u;
-  tie_run = s_tie[warp];
+  unsigned long long tie_run = tie_off;
   for (int64_t i0 = w_lo; i0 < w_hi; i0 += 32) {
     const int64_t i = i0 + lane;
     const Item it = load(i);
     const unsigned long long tw = tie_weight(it);
-    const unsigned long long incl = warp_incl_scan(tw, lane);
-    const uint32_t act = (i < w_hi) ? decide(it, tie_run + incl - tw, tw) : KVC_ACT_RELEASE;
+    unsigned long long incl = 0;
+    if (__any_sync(kFull, tw != 0)) incl = warp_incl_scan(a.byte_mode ? tw : (tw != 0 ? 1ull : 0ull), lane);
+    const unsigned long long tb_here = a.byte_mode ? tw : (tw != 0 ? 1ull : 0ull);
+    const uint32_t act = (i < w_hi) ? decide(it, tie_run + incl - tb_here, tb_here) : KVC_ACT_RELEASE;
     tie_run += __shfl_sync(kFull, incl, 31);
 #pragma unroll
     for (int q = 0; q < KVC_N_POOLS; ++q) {
