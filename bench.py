@@ -35,6 +35,14 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or TC util)"
+
+# DRAM bytes (read + write) of one score_kernel launch, per unit, from the ncu
+# capture summarised in profiles/score_kernel_qwen3_8b_T32768_4layers.md
+# (32 units: 274,451,968 B read + 6,573,568 B written).  Traffic grows with the
+# number of units (each unit's keys are read once), so a launch moves
+# bytes_per_unit x units.  Valid only for the kernel source with this SHA-1;
+# after any change the bench reports traffic as null until it is measured again.
+SCORE_TRAFFIC = {"sha1": "59d0d8ce04581035dae9728c00c590ff2bc5a6bd", "bytes_per_unit": (274451968 + 6573568) / 32}
 UNIT = "tokens/s (summed over layer x KV-head units)"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -59,6 +67,15 @@ def algorithmic_bytes(w, kept_per_unit: int) -> dict:
     if w.renumber:
         compact += min(w.max_pos, T) * d * 4            # cos + sin rows touched (fp32, d/2 each)
     return dict(score=score, select=select, compact=compact, total=score + select + compact)
+
+
+def score_traffic(n_units: int):
+    import hashlib
+    src = os.path.join(ROOT, "budgeted_kv_cache_gb300", "csrc", "score_tc.cu")
+    with open(src, "rb") as f:
+        if hashlib.sha1(f.read()).hexdigest() != SCORE_TRAFFIC["sha1"]:
+            return None
+    return SCORE_TRAFFIC["bytes_per_unit"] * n_units
 
 
 def algorithmic_flops(w) -> int:
@@ -345,7 +362,8 @@ def run_gpu(args, w, world, rank, local):
                    "parallelism": f"replicas x{world}",
                    "l2": "256 MiB buffer written between timed steps; K/V inputs (2.4 GB each) exceed L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "kernel": "score_kernel",
+                     "frac": achieved / hbm, "traffic": score_traffic(wr.n_units),
+                     "kernel": "score_kernel",
                      "peak_source": src,
                      "algorithmic_bytes_per_launch": ab["score"],
                      "tc_tflops_algorithmic": flops / (score_ms * 1e-3) / 1e12},
