@@ -57,8 +57,8 @@ struct Smem {
   int* abort_flag;
   float* lam;           // [256] negated log-sum-exp of each window row
   float* red;           // [2 parities][4 groups][128] pass-2 partial sums
-  float* hm;            // [4 groups][256] pass-1 partial max
-  float* hl;            // [4 groups][256] pass-1 partial sum
+  float* hm;            // [4 groups][128] pass-1 partial max (+ spare)
+  float* hl;            // [4 groups][128] pass-1 partial sum (+ spare)
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n_stages) {
@@ -91,27 +91,28 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Online max / sum update of one window row with 32 more raw logits
+// Online max / sum update of one window row with N more raw logits
 // (pass 1, log2 domain: y = z * cs).  Masked logits are -inf.  Pairs of
 // logits go through packed two-lane fp32 multiply-add / add instructions.
-__device__ __forceinline__ void row_update(const uint32_t (&r)[32], float cs, bool masked,
+template <int N>
+__device__ __forceinline__ void row_update(const uint32_t (&r)[N], float cs, bool masked,
                                            int64_t j0, int64_t last, float& m, float& l) {
-  float v[32];
+  float v[N];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
   if (masked) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < N; ++i)
       if (j0 + i > last) v[i] = -INFINITY;
   }
-  float t[11];
+  float mx[8];
 #pragma unroll
-  for (int k = 0; k < 10; ++k) t[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
-  t[10] = fmaxf(v[30], v[31]);
-  const float mx = fmaxf(fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]),
-                               fmax3(t[6], t[7], t[8])),
-                         fmaxf(t[9], t[10]));
-  const float mc = mx * cs;
+  for (int k = 0; k < 8; ++k) mx[k] = fmaxf(v[k], v[k + 8]);
+#pragma unroll
+  for (int i = 16; i < N; i += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], v[i + k], v[i + 8 + k]);
+  const float mc = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), mx[6]), mx[7]) * cs;
   if (mc > m) {
     l *= ex2_approx(m - mc);
     m = mc;
@@ -125,7 +126,7 @@ __device__ __forceinline__ void row_update(const uint32_t (&r)[32], float cs, bo
     s2[k] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
   }
 #pragma unroll
-  for (int i = 8; i < 32; i += 2) {
+  for (int i = 8; i < N; i += 2) {
     const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), cs2, nm2);
     s2[(i >> 1) & 3] = __fadd2_rn(s2[(i >> 1) & 3], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
   }
@@ -133,13 +134,14 @@ __device__ __forceinline__ void row_update(const uint32_t (&r)[32], float cs, bo
   l += u2.x + u2.y;
 }
 
-// Pass 2: add exp2(z * cs - lse_r) of 32 rows r to the token's mass (four
-// packed pairs of running sums).  nlam holds -lse of those 32 rows.
-__device__ __forceinline__ void mass_accum(const uint32_t (&r)[32], const float* nlam, float cs,
+// Pass 2: add exp2(z * cs - lse_r) of N rows r to the token's mass (four
+// packed pairs of running sums).  nlam holds -lse of those N rows.
+template <int N>
+__device__ __forceinline__ void mass_accum(const uint32_t (&r)[N], const float* nlam, float cs,
                                            float2 (&acc)[4]) {
   const float2 cs2 = make_float2(cs, cs);
 #pragma unroll
-  for (int i = 0; i < 32; i += 4) {
+  for (int i = 0; i < N; i += 4) {
     const float4 nl = *reinterpret_cast<const float4*>(nlam + i);
     const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), cs2,
                                 make_float2(nl.x, nl.y));
@@ -153,28 +155,16 @@ __device__ __forceinline__ void mass_accum(const uint32_t (&r)[32], const float*
 
 // Same with the causal mask of the last tiles: row r0 + i sees token j iff
 // j <= Tq + (r0 + i) mod W.
-__device__ __forceinline__ void mass_accum_masked(const uint32_t (&r)[32], const float* nlam,
+template <int N>
+__device__ __forceinline__ void mass_accum_masked(const uint32_t (&r)[N], const float* nlam,
                                                   float cs, int r0, int64_t j, int64_t Tq, int W,
                                                   float2 (&acc)[4]) {
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
+  for (int i = 0; i < N; i += 2) {
     const bool v0 = j <= Tq + ((r0 + i) % W), v1 = j <= Tq + ((r0 + i + 1) % W);
     const float e0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[i]), cs, nlam[i])) : 0.f;
     const float e1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[i + 1]), cs, nlam[i + 1])) : 0.f;
     acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], make_float2(e0, e1));
-  }
-}
-
-// Walk `nq` 32-column chunks of a TMEM tile, one load at a time: with four
-// epilogue warps per SM sub-partition the load latency of one warp is
-// covered by the arithmetic of the others.
-template <class ColF, class ProcF>
-__device__ __forceinline__ void tmem_chunks(uint32_t tbuf, int nq, ColF col, ProcF proc) {
-  for (int q = 0; q < nq; ++q) {
-    uint32_t A[32];
-    tmem_ld32_issue(tbuf + col(q), A);
-    tmem_ld_wait(A);
-    proc(A, q);
   }
 }
 
@@ -343,9 +333,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     }
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
-    // All four warpgroups process every tile; warpgroup g takes token
-    // columns [32 g, 32 g + 32) of each row block in pass 1 and a quarter of
-    // the window rows in pass 2.  Tile jt lives in TMEM buffer jt % 2.
+    // All four warpgroups process every tile, each on 64 adjacent TMEM
+    // columns read by one load: in pass 1 warpgroup g takes window-row block
+    // g / 2 and tokens [64 (g % 2), 64 (g % 2) + 64) of the tile; in pass 2
+    // window rows [64 g, 64 g + 64).  Tile jt lives in TMEM buffer jt % 2.
     // Every named barrier is an OR-reduction of a failure flag, and no thread
     // leaves the item loop between two of them, so a bounded wait that gives
     // up in one warp ends all epilogue warps at the same barrier.
@@ -358,18 +349,16 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     const float cs = a.scale_log2;
     const int64_t T = a.T;
     const int64_t Tq = T - a.W;                // row w sees keys j <= Tq + w
-    const int n_cc = a.R / 32;
-    const int cc_lo = (n_cc * grp) / 4;
-    const int n_my_cc = (n_cc * (grp + 1)) / 4 - cc_lo;
-    // pass-1 rows of this thread: lrow + 128 rb, rb < n_rb
-    bool rvalid[2];
-    int64_t rlast[2];
-#pragma unroll
-    for (int rb = 0; rb < 2; ++rb) {
-      const int r = lrow + 128 * rb;
-      rvalid[rb] = rb < n_rb && r < a.R;
-      rlast[rb] = Tq + (rvalid[rb] ? r % a.W : 0);
-    }
+    // pass 1: this thread's window row and token columns
+    const int rb = grp >> 1;
+    const int p1_row = lrow + 128 * rb;
+    const bool p1_active = rb < n_rb;          // warp-uniform
+    const bool p1_valid = p1_active && p1_row < a.R;
+    const int64_t p1_last = Tq + (p1_valid ? p1_row % a.W : 0);
+    const uint32_t p1_col = rb * 128 + (grp & 1) * 64;
+    // pass 2: this group's window rows
+    const int p2_r0 = 64 * grp;
+    const int p2_n = max(0, min(64, a.R - p2_r0));   // 64, 32 or 0 (R is a multiple of 32)
 
     uint32_t jt = 0;
     bool fail = false;
@@ -382,7 +371,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       cur_u = u;
 
       // ---------------- pass 1: per-row online max / sum (log2 domain)
-      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+      float m = -INFINITY, l = 0.f;
       for (int t = 0; t < nt; ++t, ++jt) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
         if (fail || !mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
@@ -390,39 +379,26 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
           continue;
         }
         tc_fence_after();
-        const uint32_t tbuf = tmem_base + lane_addr + tb * 256;
-        const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + 32 * grp;
-        const bool masked = (j0 + 31) > Tq;
-        tmem_chunks(tbuf, n_rb, [grp](int q) { return q * 128 + 32 * grp; },
-                    [&](const uint32_t(&r)[32], int q) {
-                      if (q == 0) row_update(r, cs, masked, j0, rlast[0], m0, l0);
-                      else        row_update(r, cs, masked, j0, rlast[1], m1, l1);
-                    });
+        if (p1_active) {
+          const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + (grp & 1) * 64;
+          uint32_t r[64];
+          tmem_ld64(tmem_base + lane_addr + tb * 256 + p1_col, r);
+          row_update<64>(r, cs, (j0 + 63) > Tq, j0, p1_last, m, l);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
       }
-      // merge the four warpgroups' statistics of each row
-      s.hm[grp * 256 + lrow] = m0;
-      s.hl[grp * 256 + lrow] = l0;
-      s.hm[grp * 256 + 128 + lrow] = m1;
-      s.hl[grp * 256 + 128 + lrow] = l1;
+      // merge the two warpgroups' statistics of each row
+      s.hm[grp * 128 + lrow] = m;
+      s.hl[grp * 128 + lrow] = l;
       fail = named_bar_or(1, kEpiThreads, fail);
-      if (grp == 0 && !fail) {
-#pragma unroll
-        for (int rb = 0; rb < 2; ++rb) {
-          float mn = -INFINITY;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) mn = fmaxf(mn, s.hm[g * 256 + rb * 128 + lrow]);
-          float ls = 0.f;
-          if (mn != -INFINITY) {
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-              ls += s.hl[g * 256 + rb * 128 + lrow] * ex2_approx(s.hm[g * 256 + rb * 128 + lrow] - mn);
-          }
-          if (rvalid[rb])
-            a.stats[(static_cast<size_t>(u) * S + c) * a.R + lrow + 128 * rb] = make_float2(mn, ls);
-        }
+      if ((grp & 1) == 0 && p1_valid && !fail) {
+        const float m2 = s.hm[(grp + 1) * 128 + lrow], l2 = s.hl[(grp + 1) * 128 + lrow];
+        const float mn = fmaxf(m, m2);
+        float ls = 0.f;
+        if (mn != -INFINITY) ls = l * ex2_approx(m - mn) + l2 * ex2_approx(m2 - mn);
+        a.stats[(static_cast<size_t>(u) * S + c) * a.R + p1_row] = make_float2(mn, ls);
       }
       __threadfence();
       fail = named_bar_or(1, kEpiThreads, fail);
@@ -478,29 +454,43 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       named_bar_sync(1, kEpiThreads);
 
       // ---------------- pass 2: per-token sum of exp2(z cs - lse) over rows
+      // The global inputs of a token (bonus, previous score) are loaded one
+      // tile ahead, so their latency never sits in front of a wait.
+      // Raw loads only: any arithmetic on a loaded value would stall here.
+      const bool ld_bonus = grp == 0 && a.bonus;
+      const bool ld_old = grp == 0 && a.accumulate;
+      auto tok_of = [&](int tt) { return static_cast<int64_t>(t0 + tt) * kTileTokens + lrow; };
+      float bon_next = 0.f, old_next = 0.f;
+      if (ld_bonus && tok_of(0) < T) bon_next = __ldg(a.bonus + static_cast<int64_t>(b) * T + tok_of(0));
+      if (ld_old && tok_of(0) < T) old_next = a.scores[static_cast<int64_t>(u) * T + tok_of(0)];
       for (int t = 0; t < nt; ++t, ++jt) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
         const int64_t tile0 = static_cast<int64_t>(t0 + t) * kTileTokens;
         const int64_t j = tile0 + lrow;
         const bool masked = (tile0 + kTileTokens - 1) > Tq;
         float* dst = a.scores + static_cast<int64_t>(u) * T + j;
-        float extra = 0.f;
-        if (grp == 0 && j < T) {      // global inputs, loaded before the TMEM work
-          if (a.bonus) extra += __ldg(a.bonus + static_cast<int64_t>(b) * T + j);
-          if (a.accumulate) extra += *dst;
+        const float bon = bon_next, old = old_next;
+        if (t + 1 < nt && tok_of(t + 1) < T) {
+          if (ld_bonus) bon_next = __ldg(a.bonus + static_cast<int64_t>(b) * T + tok_of(t + 1));
+          if (ld_old) old_next = a.scores[static_cast<int64_t>(u) * T + tok_of(t + 1)];
         }
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         if (!fail && mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
           tc_fence_after();
-          const uint32_t tbuf = tmem_base + lane_addr + tb * 256;
-          if (n_my_cc > 0)
-            tmem_chunks(tbuf, n_my_cc, [cc_lo](int q) { return (cc_lo + q) * 32; },
-                        [&](const uint32_t(&r)[32], int q) {
-                          const int cc = cc_lo + q;
-                          if (!masked) mass_accum(r, s.lam + cc * 32, cs, acc);
-                          else mass_accum_masked(r, s.lam + cc * 32, cs, cc * 32, j, Tq, a.W, acc);
-                        });
+          const uint32_t taddr = tmem_base + lane_addr + tb * 256 + p2_r0;
+          if (p2_n == 64) {
+            uint32_t r[64];
+            tmem_ld64(taddr, r);
+            if (!masked) mass_accum<64>(r, s.lam + p2_r0, cs, acc);
+            else mass_accum_masked<64>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
+          } else if (p2_n == 32) {
+            uint32_t r[32];
+            tmem_ld32_issue(taddr, r);
+            tmem_ld_wait(r);
+            if (!masked) mass_accum<32>(r, s.lam + p2_r0, cs, acc);
+            else mass_accum_masked<32>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
@@ -515,7 +505,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         if (grp == 0) {
           float sc = -INFINITY;
           if (j < T) {
-            sc = ((red[lrow] + red[128 + lrow]) + (red[256 + lrow] + red[384 + lrow])) + extra;
+            sc = ((red[lrow] + red[128 + lrow]) + (red[256 + lrow] + red[384 + lrow])) + (bon + old);
             *dst = sc;
           }
           const int P = a.page_size;
