@@ -42,6 +42,10 @@ constexpr int kEpiWarp0 = 2;
 constexpr int kEpiThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle-128 K chunk)
+// Sleep between failed barrier tests of the producer and MMA threads, so
+// their waits do not take issue slots from the epilogue warps.
+constexpr uint32_t kProducerSleepNs = 256;
+constexpr uint32_t kMmaSleepNs = 32;
 
 struct Smem {
   uint8_t* q;           // n_kc chunks of q_rows x 128 B
@@ -53,10 +57,11 @@ struct Smem {
   uint64_t* qfull;
   uint64_t* qempty;
   uint64_t* mmadone;
+  uint64_t* redfull;    // [4 slots][4 TMEM lane quarters]
   uint32_t* tmem_slot;
   int* abort_flag;
   float* lam;           // [256] negated log-sum-exp of each window row
-  float* red;           // [2 parities][4 groups][128] pass-2 partial sums
+  float* red;           // [4 slots][4 groups][128] pass-2 partial sums
   float* hm;            // [4 groups][128] pass-1 partial max (+ spare)
   float* hl;            // [4 groups][128] pass-1 partial sum (+ spare)
 };
@@ -73,11 +78,12 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n
   s.qfull = bars + 2 * n_stages + 4;
   s.qempty = bars + 2 * n_stages + 5;
   s.mmadone = bars + 2 * n_stages + 6;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * n_stages + 8);
+  s.redfull = bars + 2 * n_stages + 8;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * n_stages + 24);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.lam = reinterpret_cast<float*>(s.tmem_slot + 4);
   s.red = s.lam + 256;
-  s.hm = s.red + 1024;
+  s.hm = s.red + 2048;
   s.hl = s.hm + 1024;
   return s;
 }
@@ -196,6 +202,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     mbar_init(smem_u32(s.qfull), 1);
     mbar_init(smem_u32(s.qempty), 1);
     mbar_init(smem_u32(s.mmadone), 1);
+    for (int i = 0; i < 16; ++i) mbar_init(smem_u32(&s.redfull[i]), 96);   // 3 groups x 32 threads
     *s.abort_flag = 0;
     fence_barrier_init();
   }
@@ -234,7 +241,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         const int u = it / S, c = it % S;
         const int t0 = c * a.chunk_tiles;
         const int nt = min(a.chunk_tiles, a.n_tiles - t0);
-        if (li > 0 && !mbar_wait(smem_u32(s.qempty), (li - 1) & 1, abort_flag)) break;
+        if (li > 0 && !mbar_wait_backoff(smem_u32(s.qempty), (li - 1) & 1, abort_flag, kProducerSleepNs))
+          break;
         mbar_arrive_expect_tx(smem_u32(s.qfull), static_cast<uint32_t>(n_kc * a.R * 128));
         for (int kc = 0; kc < n_kc; ++kc)
           tma_load_3d(smem_u32(s.q + kc * q_chunk_bytes), &tmap_q, smem_u32(s.qfull), kc * 64, 0,
@@ -245,7 +253,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
           for (int t = 0; t < nt; ++t, ++jt) {
             const uint32_t st = jt % a.n_stages;
             const uint32_t ph = (jt / a.n_stages) & 1;
-            if (!mbar_wait(smem_u32(&s.empty[st]), ph ^ 1, abort_flag)) {
+            if (!mbar_wait_backoff(smem_u32(&s.empty[st]), ph ^ 1, abort_flag, kProducerSleepNs)) {
               ok = false;
               break;
             }
@@ -284,7 +292,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         const int c = it % S;
         const int t0 = c * a.chunk_tiles;
         const int nt = min(a.chunk_tiles, a.n_tiles - t0);
-        if (!mbar_wait(smem_u32(s.qfull), li & 1, abort_flag)) break;
+        if (!mbar_wait_backoff(smem_u32(s.qfull), li & 1, abort_flag, kMmaSleepNs)) break;
         tc_fence_after();
         bool ok = true;
         for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -293,8 +301,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             const uint32_t ph = (jt / a.n_stages) & 1;
             const uint32_t tb = jt & 1;
             const uint32_t tph = (jt >> 1) & 1;
-            if (!mbar_wait(smem_u32(&s.full[st]), ph, abort_flag) ||
-                !mbar_wait(smem_u32(&s.tempty[tb]), tph ^ 1, abort_flag)) {
+            if (!mbar_wait_backoff(smem_u32(&s.full[st]), ph, abort_flag, kMmaSleepNs) ||
+                !mbar_wait_backoff(smem_u32(&s.tempty[tb]), tph ^ 1, abort_flag, kMmaSleepNs)) {
               ok = false;
               break;
             }
@@ -360,7 +368,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     const int p2_r0 = 64 * grp;
     const int p2_n = max(0, min(64, a.R - p2_r0));   // 64, 32 or 0 (R is a multiple of 32)
 
-    uint32_t jt = 0;
+    uint32_t jt = 0;           // tile counter of both passes (TMEM buffer, phase)
+    uint32_t jt2 = 0;          // pass-2 tile counter (reduction slot, phase, finalizer)
     bool fail = false;
     int cur_u = -1;
     for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
@@ -379,15 +388,21 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
           continue;
         }
         tc_fence_after();
+        // The accumulator columns are copied to registers and the buffer is
+        // released at once, so the MMA of tile jt + 2 overlaps this math.
         if (p1_active) {
-          const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + (grp & 1) * 64;
           uint32_t r[64];
           tmem_ld64(tmem_base + lane_addr + tb * 256 + p1_col, r);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
+          const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + (grp & 1) * 64;
           row_update<64>(r, cs, (j0 + 63) > Tq, j0, p1_last, m, l);
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
       }
       // merge the two warpgroups' statistics of each row
       s.hm[grp * 128 + lrow] = m;
@@ -400,7 +415,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         if (mn != -INFINITY) ls = l * ex2_approx(m - mn) + l2 * ex2_approx(m2 - mn);
         a.stats[(static_cast<size_t>(u) * S + c) * a.R + p1_row] = make_float2(mn, ls);
       }
-      __threadfence();
+      // Publication: the barrier orders every thread's statistics before the
+      // one gpu-scope release (the counter increment) that makes them
+      // visible to the unit's other CTAs.
       fail = named_bar_or(1, kEpiThreads, fail);
       if (fail) break;
       bool timed_out = false;
@@ -428,16 +445,19 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       }
       fail = named_bar_or(1, kEpiThreads, timed_out);
       if (fail) break;
-      // log-sum-exp of every row over the whole unit (stored negated)
-      for (int r = et; r < a.R; r += kEpiThreads) {
+      // log-sum-exp of every row over the whole unit (stored negated): two
+      // adjacent threads per row merge the even and the odd chunks, eight
+      // loads in flight each, then combine their two partial results.
+      for (int q = et; q < 2 * a.R; q += kEpiThreads) {
+        const int r = q >> 1, h = q & 1;
         float M = -INFINITY, Ls = 0.f;
         const float2* st_row = a.stats + static_cast<size_t>(u) * S * a.R + r;
-        for (int c0 = 0; c0 < S; c0 += 8) {
+        for (int c0 = h; c0 < S; c0 += 16) {
           float2 st[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            st[k] = (c0 + k < S) ? __ldcg(st_row + static_cast<size_t>(c0 + k) * a.R)
-                                 : make_float2(-INFINITY, 0.f);
+            st[k] = (c0 + 2 * k < S) ? __ldcg(st_row + static_cast<size_t>(c0 + 2 * k) * a.R)
+                                     : make_float2(-INFINITY, 0.f);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             if (st[k].x == -INFINITY) continue;
@@ -449,74 +469,117 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             }
           }
         }
-        s.lam[r] = -(M + __log2f(Ls));
+        const float M2 = __shfl_xor_sync(0xffffffffu, M, 1);
+        const float L2 = __shfl_xor_sync(0xffffffffu, Ls, 1);
+        const float Mx = fmaxf(M, M2);
+        const float Lt = (M == -INFINITY ? 0.f : Ls * ex2_approx(M - Mx)) +
+                         (M2 == -INFINITY ? 0.f : L2 * ex2_approx(M2 - Mx));
+        if (h == 0) s.lam[r] = -(Mx + __log2f(Lt));
       }
       named_bar_sync(1, kEpiThreads);
 
       // ---------------- pass 2: per-token sum of exp2(z cs - lse) over rows
-      // The global inputs of a token (bonus, previous score) are loaded one
-      // tile ahead, so their latency never sits in front of a wait.
-      // Raw loads only: any arithmetic on a loaded value would stall here.
-      const bool ld_bonus = grp == 0 && a.bonus;
-      const bool ld_old = grp == 0 && a.accumulate;
-      auto tok_of = [&](int tt) { return static_cast<int64_t>(t0 + tt) * kTileTokens + lrow; };
-      float bon_next = 0.f, old_next = 0.f;
-      if (ld_bonus && tok_of(0) < T) bon_next = __ldg(a.bonus + static_cast<int64_t>(b) * T + tok_of(0));
-      if (ld_old && tok_of(0) < T) old_next = a.scores[static_cast<int64_t>(u) * T + tok_of(0)];
-      for (int t = 0; t < nt; ++t, ++jt) {
+      // The four groups' partial sums of pass-2 tile jt2 meet in slot jt2 % 4
+      // of `red`.  Group jt2 % 4 keeps its own partial in registers and, one
+      // tile later (so the others have long written theirs), waits for
+      // redfull[slot][quarter] and writes the token's score.  The finalizing
+      // role rotates, so no group carries more work than another and no
+      // CTA-wide barrier sits between tiles.  A slot is rewritten by pass-2
+      // tile jt2 + 4 only after its finalize: those writers waited for that
+      // tile's accumulator, whose MMA waited for every warp (the finalizer
+      // too, after its finalize) to release a tile two or more behind it.
+      // The finalizer loads the token's bonus and previous score when the
+      // tile starts; they are consumed a tile later.
+      auto finalize = [&](uint32_t jtf, float own, float bon, float old, int64_t jf) {
+        const int sl = jtf & 3;
+        if (fail || !mbar_wait(smem_u32(&s.redfull[sl * 4 + qr]), (jtf >> 2) & 1, abort_flag)) {
+          fail = true;
+          return;
+        }
+        const float* rs = s.red + sl * 512 + lrow;
+        const float p0 = grp == 0 ? own : rs[0];
+        const float p1 = grp == 1 ? own : rs[128];
+        const float p2 = grp == 2 ? own : rs[256];
+        const float p3 = grp == 3 ? own : rs[384];
+        float sc = -INFINITY;
+        if (jf < T) {
+          sc = ((p0 + p1) + (p2 + p3)) + (bon + old);
+          a.scores[static_cast<int64_t>(u) * T + jf] = sc;
+        }
+        const int P = a.page_size;
+        if (P > 1) {
+          float pm = sc;
+          for (int o = 1; o < P; o <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
+          if (jf < T && (lane & (P - 1)) == 0)
+            a.page_scores[static_cast<int64_t>(u) * (T / P) + jf / P] = pm;
+        }
+      };
+      bool pend = false;                 // this group finalizes pass-2 tile jt_p
+      uint32_t jt_p = 0;
+      float own_p = 0.f, bon_p = 0.f, old_p = 0.f;
+      int64_t j_p = 0;
+      for (int t = 0; t < nt; ++t, ++jt, ++jt2) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
+        const int fg = static_cast<int>(jt2 & 3);
         const int64_t tile0 = static_cast<int64_t>(t0 + t) * kTileTokens;
         const int64_t j = tile0 + lrow;
         const bool masked = (tile0 + kTileTokens - 1) > Tq;
-        float* dst = a.scores + static_cast<int64_t>(u) * T + j;
-        const float bon = bon_next, old = old_next;
-        if (t + 1 < nt && tok_of(t + 1) < T) {
-          if (ld_bonus) bon_next = __ldg(a.bonus + static_cast<int64_t>(b) * T + tok_of(t + 1));
-          if (ld_old) old_next = a.scores[static_cast<int64_t>(u) * T + tok_of(t + 1)];
+        float bon = 0.f, old = 0.f;
+        if (grp == fg && j < T) {
+          if (a.bonus) bon = __ldg(a.bonus + static_cast<int64_t>(b) * T + j);
+          if (a.accumulate) old = a.scores[static_cast<int64_t>(u) * T + j];
         }
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
         if (!fail && mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
           tc_fence_after();
           const uint32_t taddr = tmem_base + lane_addr + tb * 256 + p2_r0;
+          // copy to registers, release the buffer, then do the math
           if (p2_n == 64) {
             uint32_t r[64];
             tmem_ld64(taddr, r);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
             if (!masked) mass_accum<64>(r, s.lam + p2_r0, cs, acc);
             else mass_accum_masked<64>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
           } else if (p2_n == 32) {
             uint32_t r[32];
             tmem_ld32_issue(taddr, r);
             tmem_ld_wait(r);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
             if (!masked) mass_accum<32>(r, s.lam + p2_r0, cs, acc);
             else mass_accum_masked<32>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
         } else {
           fail = true;
         }
-        float* red = s.red + (jt & 1) * 512;      // consecutive tiles alternate slots
         const float2 a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        red[grp * 128 + lrow] = a2.x + a2.y;
-        fail = named_bar_or(2, kEpiThreads, fail);
-        if (fail) continue;      // every epilogue thread sees the same flag
-        if (grp == 0) {
-          float sc = -INFINITY;
-          if (j < T) {
-            sc = ((red[lrow] + red[128 + lrow]) + (red[256 + lrow] + red[384 + lrow])) + (bon + old);
-            *dst = sc;
-          }
-          const int P = a.page_size;
-          if (P > 1) {
-            float pm = sc;
-            for (int o = 1; o < P; o <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
-            if (j < T && (lane & (P - 1)) == 0)
-              a.page_scores[static_cast<int64_t>(u) * (T / P) + j / P] = pm;
-          }
+        const float part = a2.x + a2.y;
+        if (grp != fg) {
+          s.red[(fg * 4 + grp) * 128 + lrow] = part;
+          mbar_arrive(smem_u32(&s.redfull[fg * 4 + qr]));
+        }
+        if (pend) {
+          finalize(jt_p, own_p, bon_p, old_p, j_p);
+          pend = false;
+        }
+        if (grp == fg) {
+          pend = true;
+          jt_p = jt2;
+          own_p = part;
+          bon_p = bon;
+          old_p = old;
+          j_p = j;
         }
       }
+      if (pend) finalize(jt_p, own_p, bon_p, old_p, j_p);
       // the next item's pass 1 rewrites hm / hl and lam only after this barrier
       fail = named_bar_or(1, kEpiThreads, fail);
       if (fail) break;
@@ -539,9 +602,9 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages) {
   size_t bytes = 1024;                                   // alignment slack
   bytes += static_cast<size_t>(n_kc) * q_rows * 128;     // Q
   bytes += static_cast<size_t>(n_stages) * n_kc * kChunkBytes;
-  bytes += (2 * n_stages + 8) * 8;                       // barriers
+  bytes += (2 * n_stages + 24) * 8;                      // barriers
   bytes += 16;                                           // tmem slot, abort flag
-  bytes += (256 + 1024 + 2 * 1024) * 4;                 // lam, red, hm, hl
+  bytes += (256 + 2048 + 2 * 1024) * 4;                 // lam, red, hm, hl
   return bytes;
 }
 
