@@ -140,6 +140,31 @@ __device__ __forceinline__ void row_update(const uint32_t (&r)[N], float cs, boo
   l += u2.x + u2.y;
 }
 
+// Sum of exp2(y - m) over N raw logits y = z * cs of one row against a
+// fixed reference m (pass 1 after the row's first tile): the row's running
+// reference is not raised for every tile, which saves the 64-way maximum.
+// Terms may exceed 1; the caller redoes the tile with its exact maximum if
+// the sum leaves the range where fp32 keeps it safely (above 2^100).
+template <int N>
+__device__ __forceinline__ float exp_sum(const uint32_t (&r)[N], float cs, float m) {
+  const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-m, -m);
+  float2 s2[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])),
+                                cs2, nm2);
+    s2[k] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+  }
+#pragma unroll
+  for (int i = 8; i < N; i += 2) {
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), cs2,
+                                nm2);
+    s2[(i >> 1) & 3] = __fadd2_rn(s2[(i >> 1) & 3], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+  }
+  const float2 u2 = __fadd2_rn(__fadd2_rn(s2[0], s2[1]), __fadd2_rn(s2[2], s2[3]));
+  return u2.x + u2.y;
+}
+
 // Pass 2: add exp2(z * cs - lse_r) of N rows r to the token's mass (four
 // packed pairs of running sums).  nlam holds -lse of those N rows.
 template <int N>
@@ -397,7 +422,11 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
           const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + (grp & 1) * 64;
-          row_update<64>(r, cs, (j0 + 63) > Tq, j0, p1_last, m, l);
+          const bool masked = (j0 + 63) > Tq;
+          float sum = 0.f;
+          if (!masked && m != -INFINITY) sum = exp_sum<64>(r, cs, m);
+          if (!masked && m != -INFINITY && sum <= 0x1p100f) l += sum;
+          else row_update<64>(r, cs, masked, j0, p1_last, m, l);
         } else {
           tc_fence_before();
           __syncwarp();
