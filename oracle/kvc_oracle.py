@@ -126,6 +126,45 @@ def window_mass(k, q, scale: float, row_block: int = 8) -> np.ndarray:
     return mass
 
 
+def window_row_lse(k, q, scale: float) -> np.ndarray:
+    """Natural-log log-sum-exp of each window row's visible logits, fp64.
+
+    The softmax denominator of PASK Eq. 1 for the rows of window_mass, in
+    the same row order (head-major: row h * W + w), as an attention kernel
+    that ran the window would report it.
+    """
+    k = np.asarray(k, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    T = k.shape[0]
+    G, W, d = q.shape
+    rows = q.reshape(G * W, d)
+    out = np.empty(G * W, dtype=np.float64)
+    for r in range(G * W):
+        z = (k[: T - W + (r % W) + 1] @ rows[r]) * scale
+        m = z.max()
+        out[r] = m + np.log(np.exp(z - m).sum())
+    return out
+
+
+def window_mass_given_lse(k, q, scale: float, row_lse) -> np.ndarray:
+    """mass[j] = sum over visible rows of exp(q_hw . k_j * scale - row_lse[hw]), fp64.
+
+    With the rows' own log-sum-exp this is window_mass; with any other
+    per-row value it is what the scorer computes from a caller's statistics.
+    """
+    k = np.asarray(k, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    lse = np.asarray(row_lse, dtype=np.float64)
+    T = k.shape[0]
+    G, W, d = q.shape
+    rows = q.reshape(G * W, d)
+    mass = np.zeros(T, dtype=np.float64)
+    for r in range(G * W):
+        n = T - W + (r % W) + 1
+        mass[:n] += np.exp((k[:n] @ rows[r]) * scale - lse[r])
+    return mass
+
+
 def unit_scores(k_bits, q_bits, scale: float, bonus=None, acc=None) -> np.ndarray:
     """score_j = fp32(mass_j + bonus_j + acc_j) for one unit (bf16 inputs as bits)."""
     k = bf16_bits_to_f32(k_bits)

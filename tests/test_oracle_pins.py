@@ -160,6 +160,34 @@ def test_window_mass_conservation_and_dominant_key():
     assert mass[5] > W * G * (1 - 1e-9)
 
 
+def test_window_row_lse_brute_force():
+    """Row log-sum-exp against a pure-Python loop with math.fsum on a tiny case."""
+    T, W, G, d = 23, 5, 2, 4
+    rng = np.random.default_rng(7)
+    k = rng.standard_normal((T, d))
+    q = rng.standard_normal((G, W, d))
+    ours = o.window_row_lse(k, q, 0.5)
+    for h in range(G):
+        for w in range(W):
+            zs = [0.5 * sum(q[h, w, i] * k[j, i] for i in range(d)) for j in range(T - W + w + 1)]
+            assert abs(ours[h * W + w] - math.log(math.fsum(math.exp(z) for z in zs))) < 1e-12
+
+
+def test_mass_given_lse_reduces_to_window_mass_and_scales():
+    """With the rows' own statistics the mass is window_mass; shifting every
+    row's statistic by c multiplies the mass by exp(-c)."""
+    T, W, G, d = 150, 16, 4, 32
+    rng = np.random.default_rng(8)
+    k = rng.standard_normal((T, d))
+    q = rng.standard_normal((G, W, d)) * 1.5
+    scale = 1 / math.sqrt(d)
+    lse = o.window_row_lse(k, q, scale)
+    np.testing.assert_allclose(o.window_mass_given_lse(k, q, scale, lse), o.window_mass(k, q, scale),
+                               rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(o.window_mass_given_lse(k, q, scale, lse + 0.75),
+                               o.window_mass(k, q, scale) * math.exp(-0.75), rtol=1e-12, atol=1e-15)
+
+
 def test_scores_add_bonus_and_accumulator():
     w = wl.tiny().replace(n_tokens=200, window=16)
     x = wl.make_inputs(w, with_tables=False)
