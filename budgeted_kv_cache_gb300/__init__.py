@@ -70,7 +70,7 @@ def _load():
         SH, PO, PL = ctypes.POINTER(kvc_shape), ctypes.POINTER(kvc_policy), ctypes.POINTER(kvc_pools)
         sig = {
             "kvc_score_workspace_bytes": (SZ, [SH, I32]),
-            "kvc_score": (ctypes.c_int, [SH, P, P, I32, F32, P, I32, U32, P, P, P, P, SZ, P]),
+            "kvc_score": (ctypes.c_int, [SH, P, P, I32, F32, P, P, I32, U32, P, P, P, P, SZ, P]),
             "kvc_select_workspace_bytes": (SZ, [SH, PO]),
             "kvc_select": (ctypes.c_int, [SH, PO, P, P, P, P, P, P, SZ, P]),
             "kvc_compact_rerotate_quant": (ctypes.c_int, [SH, PO, P, P, P, P, P, P, P, I64, PL, P, P]),
@@ -193,12 +193,13 @@ def kvc_score_workspace_bytes(shape: kvc_shape, window: int) -> int:
 
 
 def kvc_score(shape, k_cache, q_window, window, softmax_scale, bonus, page_size, flags, scores,
-              page_scores, unit_status, workspace, workspace_bytes=None, stream=None):
+              page_scores, unit_status, workspace, workspace_bytes=None, stream=None, row_lse=None):
+    """row_lse: optional fp32 [B][L][H_q][window] natural-log row statistics (skips pass 1)."""
     wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     _check("kvc_score", _load().kvc_score(
-        ctypes.byref(shape), _p(k_cache), _p(q_window), window, float(softmax_scale), _p(bonus),
-        page_size, flags, _p(scores), _p(page_scores), _p(unit_status), _p(workspace), wb,
-        _stream(stream)))
+        ctypes.byref(shape), _p(k_cache), _p(q_window), window, float(softmax_scale), _p(row_lse),
+        _p(bonus), page_size, flags, _p(scores), _p(page_scores), _p(unit_status), _p(workspace),
+        wb, _stream(stream)))
 
 
 def kvc_select_workspace_bytes(shape: kvc_shape, policy: Policy) -> int:

@@ -230,7 +230,8 @@ size_t kvc_score_workspace_bytes(const kvc_shape* shape, int32_t window) {
 }
 
 kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_window,
-                     int32_t window, float softmax_scale, const float* bonus, int32_t page_size,
+                     int32_t window, float softmax_scale, const float* row_lse,
+                     const float* bonus, int32_t page_size,
                      uint32_t flags, float* scores, float* page_scores, int32_t* unit_status,
                      void* workspace, size_t workspace_bytes, kvc_stream stream) {
   ScorePlan p;
@@ -263,6 +264,7 @@ kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_
   a.n_stages = p.n_stages;
   a.q_rows = p.q_rows;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.row_lse = row_lse;
   a.bonus = bonus;
   a.scores = scores;
   a.page_scores = page_size > 1 ? page_scores : nullptr;

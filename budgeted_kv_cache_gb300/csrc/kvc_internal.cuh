@@ -33,6 +33,7 @@ struct ScoreArgs {
   int32_t n_stages;
   int32_t q_rows;              // Q rows held in shared memory (multiple of 128)
   float scale_log2;            // softmax_scale * log2(e)
+  const float* row_lse;        // optional [U][R] natural-log row statistics
   const float* bonus;
   float* scores;
   float* page_scores;

@@ -274,7 +274,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
                       u, keep);
         ++q_loads;
         bool ok = true;
-        for (int pass = 0; pass < 2 && ok; ++pass) {
+        for (int pass = a.row_lse ? 1 : 0; pass < 2 && ok; ++pass) {
           for (int t = 0; t < nt; ++t, ++jt) {
             const uint32_t st = jt % a.n_stages;
             const uint32_t ph = (jt / a.n_stages) & 1;
@@ -320,7 +320,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         if (!mbar_wait_backoff(smem_u32(s.qfull), li & 1, abort_flag, kMmaSleepNs)) break;
         tc_fence_after();
         bool ok = true;
-        for (int pass = 0; pass < 2 && ok; ++pass) {
+        for (int pass = a.row_lse ? 1 : 0; pass < 2 && ok; ++pass) {
           for (int t = 0; t < nt; ++t, ++jt) {
             const uint32_t st = jt % a.n_stages;
             const uint32_t ph = (jt / a.n_stages) & 1;
@@ -404,108 +404,115 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       const int b = u / (a.L * a.Hkv);
       cur_u = u;
 
-      // ---------------- pass 1: per-row online max / sum (log2 domain)
-      float m = -INFINITY, l = 0.f;
-      for (int t = 0; t < nt; ++t, ++jt) {
-        const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
-        if (fail || !mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
-          fail = true;
-          continue;
-        }
-        tc_fence_after();
-        // The accumulator columns are copied to registers and the buffer is
-        // released at once, so the MMA of tile jt + 2 overlaps this math.
-        if (p1_active) {
-          uint32_t r[64];
-          tmem_ld64(tmem_base + lane_addr + tb * 256 + p1_col, r);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
-          const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + (grp & 1) * 64;
-          const bool masked = (j0 + 63) > Tq;
-          float sum = 0.f;
-          if (!masked && m != -INFINITY) sum = exp_sum<64>(r, cs, m);
-          if (!masked && m != -INFINITY && sum <= 0x1p100f) l += sum;
-          else row_update<64>(r, cs, masked, j0, p1_last, m, l);
-        } else {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
-        }
-      }
-      // merge the two warpgroups' statistics of each row
-      s.hm[grp * 128 + lrow] = m;
-      s.hl[grp * 128 + lrow] = l;
-      fail = named_bar_or(1, kEpiThreads, fail);
-      if ((grp & 1) == 0 && p1_valid && !fail) {
-        const float m2 = s.hm[(grp + 1) * 128 + lrow], l2 = s.hl[(grp + 1) * 128 + lrow];
-        const float mn = fmaxf(m, m2);
-        float ls = 0.f;
-        if (mn != -INFINITY) ls = l * ex2_approx(m - mn) + l2 * ex2_approx(m2 - mn);
-        a.stats[(static_cast<size_t>(u) * S + c) * a.R + p1_row] = make_float2(mn, ls);
-      }
-      // Publication: the barrier orders every thread's statistics before the
-      // one gpu-scope release (the counter increment) that makes them
-      // visible to the unit's other CTAs.
-      fail = named_bar_or(1, kEpiThreads, fail);
-      if (fail) break;
-      bool timed_out = false;
-      if (et == 0) {
-        atom_add_release_gpu(&a.counters[u], 1u);
-        uint64_t t_start = 0;
-        for (uint32_t n = 0;; ++n) {
-          if (ld_acquire_gpu(&a.counters[u]) >= static_cast<uint32_t>(S)) break;
-          if (*abort_flag) {
-            timed_out = true;
-            break;
+      if (a.row_lse == nullptr) {
+        // ---------------- pass 1: per-row online max / sum (log2 domain)
+        float m = -INFINITY, l = 0.f;
+        for (int t = 0; t < nt; ++t, ++jt) {
+          const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
+          if (fail || !mbar_wait(smem_u32(&s.tfull[tb]), tph, abort_flag)) {
+            fail = true;
+            continue;
           }
-          if ((n & 63) == 0) {
-            const uint64_t now = globaltimer_ns();
-            if (t_start == 0) {
-              t_start = now;
-            } else if (now - t_start > kWaitLimitNs) {
-              *abort_flag = 1;
+          tc_fence_after();
+          // The accumulator columns are copied to registers and the buffer is
+          // released at once, so the MMA of tile jt + 2 overlaps this math.
+          if (p1_active) {
+            uint32_t r[64];
+            tmem_ld64(tmem_base + lane_addr + tb * 256 + p1_col, r);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
+            const int64_t j0 = static_cast<int64_t>(t0 + t) * kTileTokens + (grp & 1) * 64;
+            const bool masked = (j0 + 63) > Tq;
+            float sum = 0.f;
+            if (!masked && m != -INFINITY) sum = exp_sum<64>(r, cs, m);
+            if (!masked && m != -INFINITY && sum <= 0x1p100f) l += sum;
+            else row_update<64>(r, cs, masked, j0, p1_last, m, l);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
+          }
+        }
+        // merge the two warpgroups' statistics of each row
+        s.hm[grp * 128 + lrow] = m;
+        s.hl[grp * 128 + lrow] = l;
+        fail = named_bar_or(1, kEpiThreads, fail);
+        if ((grp & 1) == 0 && p1_valid && !fail) {
+          const float m2 = s.hm[(grp + 1) * 128 + lrow], l2 = s.hl[(grp + 1) * 128 + lrow];
+          const float mn = fmaxf(m, m2);
+          float ls = 0.f;
+          if (mn != -INFINITY) ls = l * ex2_approx(m - mn) + l2 * ex2_approx(m2 - mn);
+          a.stats[(static_cast<size_t>(u) * S + c) * a.R + p1_row] = make_float2(mn, ls);
+        }
+        // Publication: the barrier orders every thread's statistics before the
+        // one gpu-scope release (the counter increment) that makes them
+        // visible to the unit's other CTAs.
+        fail = named_bar_or(1, kEpiThreads, fail);
+        if (fail) break;
+        bool timed_out = false;
+        if (et == 0) {
+          atom_add_release_gpu(&a.counters[u], 1u);
+          uint64_t t_start = 0;
+          for (uint32_t n = 0;; ++n) {
+            if (ld_acquire_gpu(&a.counters[u]) >= static_cast<uint32_t>(S)) break;
+            if (*abort_flag) {
               timed_out = true;
               break;
             }
+            if ((n & 63) == 0) {
+              const uint64_t now = globaltimer_ns();
+              if (t_start == 0) {
+                t_start = now;
+              } else if (now - t_start > kWaitLimitNs) {
+                *abort_flag = 1;
+                timed_out = true;
+                break;
+              }
+            }
+            __nanosleep(32);
           }
-          __nanosleep(32);
         }
-      }
-      fail = named_bar_or(1, kEpiThreads, timed_out);
-      if (fail) break;
-      // log-sum-exp of every row over the whole unit (stored negated): two
-      // adjacent threads per row merge the even and the odd chunks, eight
-      // loads in flight each, then combine their two partial results.
-      for (int q = et; q < 2 * a.R; q += kEpiThreads) {
-        const int r = q >> 1, h = q & 1;
-        float M = -INFINITY, Ls = 0.f;
-        const float2* st_row = a.stats + static_cast<size_t>(u) * S * a.R + r;
-        for (int c0 = h; c0 < S; c0 += 16) {
-          float2 st[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            st[k] = (c0 + 2 * k < S) ? __ldcg(st_row + static_cast<size_t>(c0 + 2 * k) * a.R)
-                                     : make_float2(-INFINITY, 0.f);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (st[k].x == -INFINITY) continue;
-            if (st[k].x > M) {
-              Ls = Ls * ex2_approx(M - st[k].x) + st[k].y;
-              M = st[k].x;
-            } else {
-              Ls += st[k].y * ex2_approx(st[k].x - M);
+        fail = named_bar_or(1, kEpiThreads, timed_out);
+        if (fail) break;
+        // log-sum-exp of every row over the whole unit (stored negated): two
+        // adjacent threads per row merge the even and the odd chunks, eight
+        // loads in flight each, then combine their two partial results.
+        for (int q = et; q < 2 * a.R; q += kEpiThreads) {
+          const int r = q >> 1, h = q & 1;
+          float M = -INFINITY, Ls = 0.f;
+          const float2* st_row = a.stats + static_cast<size_t>(u) * S * a.R + r;
+          for (int c0 = h; c0 < S; c0 += 16) {
+            float2 st[8];
+  #pragma unroll
+            for (int k = 0; k < 8; ++k)
+              st[k] = (c0 + 2 * k < S) ? __ldcg(st_row + static_cast<size_t>(c0 + 2 * k) * a.R)
+                                       : make_float2(-INFINITY, 0.f);
+  #pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (st[k].x == -INFINITY) continue;
+              if (st[k].x > M) {
+                Ls = Ls * ex2_approx(M - st[k].x) + st[k].y;
+                M = st[k].x;
+              } else {
+                Ls += st[k].y * ex2_approx(st[k].x - M);
+              }
             }
           }
+          const float M2 = __shfl_xor_sync(0xffffffffu, M, 1);
+          const float L2 = __shfl_xor_sync(0xffffffffu, Ls, 1);
+          const float Mx = fmaxf(M, M2);
+          const float Lt = (M == -INFINITY ? 0.f : Ls * ex2_approx(M - Mx)) +
+                           (M2 == -INFINITY ? 0.f : L2 * ex2_approx(M2 - Mx));
+          if (h == 0) s.lam[r] = -(Mx + __log2f(Lt));
         }
-        const float M2 = __shfl_xor_sync(0xffffffffu, M, 1);
-        const float L2 = __shfl_xor_sync(0xffffffffu, Ls, 1);
-        const float Mx = fmaxf(M, M2);
-        const float Lt = (M == -INFINITY ? 0.f : Ls * ex2_approx(M - Mx)) +
-                         (M2 == -INFINITY ? 0.f : L2 * ex2_approx(M2 - Mx));
-        if (h == 0) s.lam[r] = -(Mx + __log2f(Lt));
+        named_bar_sync(1, kEpiThreads);
+      } else {
+        // the caller's natural-log row statistics, in the log2 domain
+        const float* rl = a.row_lse + static_cast<size_t>(u) * a.R;
+        for (int r = et; r < a.R; r += kEpiThreads) s.lam[r] = -(__ldg(rl + r) * 1.44269504088896340736f);
+        named_bar_sync(1, kEpiThreads);
       }
-      named_bar_sync(1, kEpiThreads);
 
       // ---------------- pass 2: per-token sum of exp2(z cs - lse) over rows
       // The four groups' partial sums of pass-2 tile jt2 meet in slot jt2 % 4

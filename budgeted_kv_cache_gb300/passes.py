@@ -43,10 +43,12 @@ class CompactionPass:
         self.decode_ws = e(db, dt=torch.uint8) if db > 0 else None
         self.out = e(U * self.G, head_dim, dt=torch.bfloat16)
 
-    def score(self, k_cache, q_window, bonus=None, accumulate: bool = False, stream=None):
+    def score(self, k_cache, q_window, bonus=None, accumulate: bool = False, stream=None,
+              row_lse=None):
         kvc_score(self.shape, k_cache, q_window, self.window, self.scale, bonus,
                   self.policy.page_size, SCORE_ACCUMULATE if accumulate else 0, self.scores,
-                  self.page_scores, self.score_status, self.score_ws, stream=stream)
+                  self.page_scores, self.score_status, self.score_ws, stream=stream,
+                  row_lse=row_lse)
 
     def select(self, scores: Optional[torch.Tensor] = None, stream=None):
         src = scores if scores is not None else (

@@ -114,6 +114,13 @@ typedef struct {
  * q_window  bf16 [B][L][H_q][window][d], rotated; 16-byte aligned.
  * window    W >= 1, W <= T; W * G must be a multiple of 32 and <= 256.
  * softmax_scale  <= 0 selects 1 / sqrt(d).
+ * row_lse   optional fp32 [B][L][H_q][window]: the natural-log log-sum-exp
+ *           of each window row's logits q_{h,w} . k_j * scale over the keys
+ *           it sees, when the caller already has it (an attention kernel
+ *           that produced the window's outputs returns it).  The row
+ *           statistics pass is then skipped and softmax_j is formed as
+ *           exp(q_{h,w} . k_j * scale - row_lse[h][w]).  NULL = computed
+ *           here (two passes over the keys).
  * bonus     optional fp32 [B][T] (NULL = 0).
  * page_size 1 (no page scores) or 2, 4, 8, 16, 32 with T % page_size == 0.
  * scores    fp32 [U][T] (read too under KVC_SCORE_ACCUMULATE).
@@ -125,7 +132,7 @@ typedef struct {
  * ---------------------------------------------------------------------- */
 size_t kvc_score_workspace_bytes(const kvc_shape* shape, int32_t window);
 kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_window,
-                     int32_t window, float softmax_scale, const float* bonus,
+                     int32_t window, float softmax_scale, const float* row_lse, const float* bonus,
                      int32_t page_size, uint32_t flags, float* scores, float* page_scores,
                      int32_t* unit_status, void* workspace, size_t workspace_bytes,
                      kvc_stream stream);

@@ -51,11 +51,11 @@ def test_argument_errors_return_before_any_launch(lib):
     import budgeted_kv_cache_gb300 as kvc
     kvc.library()
     # null shape
-    assert lib.kvc_score(None, None, None, 0, ctypes.c_float(0), None, 1, 0, None, None, None,
-                         None, ctypes.c_size_t(0), None) == 1
+    assert lib.kvc_score(None, None, None, 0, ctypes.c_float(0), None, None, 1, 0, None, None,
+                         None, None, ctypes.c_size_t(0), None) == 1
     bad = kvc.make_shape(1, 1, 4, 2, 96, 100)       # head_dim 96 is not supported
-    assert kvc.library().kvc_score(ctypes.byref(bad), None, None, 8, 0.0, None, 1, 0, None, None,
-                                   None, None, 0, None) == 2
+    assert kvc.library().kvc_score(ctypes.byref(bad), None, None, 8, 0.0, None, None, 1, 0, None,
+                                   None, None, None, 0, None) == 2
     shape = kvc.make_shape(1, 1, 4, 3, 64, 100)     # H_q not a multiple of H_kv
     pol = kvc.Policy(budget_tokens=10, capacity=10).c()
     assert kvc.library().kvc_select(ctypes.byref(shape), ctypes.byref(pol), None, None, None, None,

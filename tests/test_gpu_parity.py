@@ -152,6 +152,33 @@ def test_score_accumulate(kvc):
         assert_scores_close(p.scores[u].cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("shift", [0.0, 0.5])
+def test_score_with_caller_row_lse(kvc, shift):
+    """Row statistics supplied by the caller (pass 1 skipped): the oracle's
+    mass given those statistics, with the true statistics (shift 0) and with
+    every row's statistic raised by `shift` (the mass scales by exp(-shift))."""
+    w = wl.tiny().replace(n_tokens=1100)
+    x = wl.make_inputs(w, device="cuda")
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    p = pass_for_workload(w, inputs=x)
+    G, W = w.group, w.window
+    scale = 1.0 / math.sqrt(w.head_dim)
+    lse = np.zeros((w.n_units, G * W), np.float32)
+    for u in range(w.n_units):
+        ui = unit_inputs(w, x, u)
+        lse[u] = o.window_row_lse(o.bf16_bits_to_f32(ui["k"]), o.bf16_bits_to_f32(ui["q"]),
+                                  scale) + shift
+    row_lse = torch.from_numpy(lse).cuda()
+    p.score(x["k_cache"], x["q_window"], x.get("bonus"), row_lse=row_lse)
+    torch.cuda.synchronize()
+    for u in range(w.n_units):
+        ui = unit_inputs(w, x, u)
+        mass = o.window_mass_given_lse(o.bf16_bits_to_f32(ui["k"]), o.bf16_bits_to_f32(ui["q"]),
+                                       scale, lse[u].astype(np.float64))
+        ref = mass + (ui["bonus"].astype(np.float64) if ui["bonus"] is not None else 0.0)
+        assert_scores_close(p.scores[u].cpu().numpy(), ref.astype(np.float32))
+
+
 # ------------------------------------------------------------------ edge cases
 
 def test_inactive_pass_is_bytewise_identity(kvc):
