@@ -3,10 +3,20 @@
 // PASK Eq. 1 over every kept row of the unit, dequantised inside the kernel
 // (x = code * scale); PASK App. B.5: fp32 scores, softmax statistics and
 // accumulation, bf16 output.  The kept rows of a unit (int4, int8 and bf16
-// pools, concatenated) are split across `splits` CTAs; each CTA streams its
-// rows in chunks of 128 once for all G query heads of the KV head and keeps
-// an online (max, sum, unnormalised value sum) per head.  Partitions are
-// merged with PASK Eq. 15; empty partitions contribute nothing.
+// pools, concatenated in that order) are split across `splits` CTAs and the
+// partitions merged with PASK Eq. 15; empty partitions contribute nothing.
+//
+// Layout of the work (HBM-bound: every kept row is read once for all G
+// query heads of its KV head):
+//   * a warp takes 32 consecutive rows per step; for the scores each lane
+//     owns one key row and reads it with 16-byte loads (the query heads sit
+//     in shared memory and are read as broadcasts);
+//   * for P V each lane owns d / 32 adjacent columns, so every value row is
+//     one coalesced warp load, and the 32 probabilities reach the lanes by
+//     shuffles;
+//   * each warp keeps its own online (max, sum, unnormalised value sum) per
+//     head; the CTA's four warps, then the CTAs of a unit, are merged with
+//     Eq. 15.
 #include <math.h>
 
 #include "kvc_internal.cuh"
@@ -16,181 +26,314 @@ namespace kvc {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
 constexpr int kMaxG = 8;
+constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct RowRef {
+struct PoolPtrs {
   const void* k;
   const void* v;
   const void* ks;
   const void* vs;
 };
 
-__device__ __forceinline__ float scale_at(const void* sp, int64_t row, int col, int d, bool row_mode) {
+__device__ __forceinline__ PoolPtrs pool_ptrs(const kvc_pools& p, int pool) {
+  if (pool == KVC_POOL_BF16) return {p.k_bf16, p.v_bf16, nullptr, nullptr};
+  if (pool == KVC_POOL_INT8) return {p.k_i8, p.v_i8, p.k_i8_scale, p.v_i8_scale};
+  return {p.k_i4, p.v_i4, p.k_i4_scale, p.v_i4_scale};
+}
+
+__device__ __forceinline__ float load_scale(const void* sp, int64_t row, int group, int d,
+                                            bool row_mode) {
   const uint16_t* s = static_cast<const uint16_t*>(sp);
-  if (row_mode) return __half2float(__ushort_as_half(s[row]));
-  return bf16_bits_to_float(s[row * (d / 32) + col / 32]);
+  if (row_mode) return __half2float(__ushort_as_half(__ldg(s + row)));
+  return bf16_bits_to_float(__ldg(s + row * (d / 32) + group));
 }
 
-// Element `col` of row `row` of a pool, dequantised.
-__device__ __forceinline__ float load_elem(int pool, const void* base, const void* sp, int64_t row,
-                                           int col, int d, bool row_mode) {
-  if (pool == KVC_POOL_BF16)
-    return bf16_bits_to_float(static_cast<const uint16_t*>(base)[row * d + col]);
-  if (pool == KVC_POOL_INT8) {
-    const int8_t c = static_cast<const int8_t*>(base)[row * d + col];
-    return static_cast<float>(c) * scale_at(sp, row, col, d, row_mode);
+// FMAs of 8 consecutive key elements (starting at element e0) with every
+// query head; the query rows in shared memory are pre-scaled to log2 units.
+template <int D>
+__device__ __forceinline__ void dot8(const float (&x)[8], const float (*qs)[D], int e0, int G,
+                                     float (&s)[kMaxG]) {
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
+    if (h < G) {
+      const float4 q0 = *reinterpret_cast<const float4*>(&qs[h][e0]);
+      const float4 q1 = *reinterpret_cast<const float4*>(&qs[h][e0 + 4]);
+      float t = s[h];
+      t = fmaf(x[0], q0.x, t);
+      t = fmaf(x[1], q0.y, t);
+      t = fmaf(x[2], q0.z, t);
+      t = fmaf(x[3], q0.w, t);
+      t = fmaf(x[4], q1.x, t);
+      t = fmaf(x[5], q1.y, t);
+      t = fmaf(x[6], q1.z, t);
+      t = fmaf(x[7], q1.w, t);
+      s[h] = t;
+    }
   }
-  const uint8_t byte = static_cast<const uint8_t*>(base)[row * (d / 2) + col / 2];
-  int c = (col & 1) ? (byte >> 4) : (byte & 0xf);
-  c = c > 7 ? c - 16 : c;
-  return static_cast<float>(c) * scale_at(sp, row, col, d, row_mode);
 }
 
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
-  __shared__ float qs[kMaxG][128];
-  __shared__ float sc[kThreads][kMaxG + 1];
-  __shared__ float cmax[kMaxG], csum[kMaxG];
-  __shared__ int rpool[kThreads];
-  __shared__ int64_t rrow[kThreads];
-  __shared__ float accs[kThreads][kMaxG];
+// Scores of key row `row` of `pool` against every query head.  All loads
+// of a batch (half a bf16 row, or a whole int8 / int4 row and its scales)
+// are issued before any is used.
+template <int D>
+__device__ __forceinline__ void key_dot(int pool, const PoolPtrs& pp, int64_t row, bool row_mode,
+                                        const float (*qs)[D], int G, float (&s)[kMaxG]) {
+  if (pool == KVC_POOL_BF16) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pp.k) + row * D);
+#pragma unroll
+    for (int half = 0; half < D / 64; ++half) {
+      uint4 w[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) w[v] = __ldg(src + half * 8 + v);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint32_t r[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          x[2 * k] = __uint_as_float(r[k] << 16);
+          x[2 * k + 1] = __uint_as_float(r[k] & 0xffff0000u);
+        }
+        dot8<D>(x, qs, half * 64 + v * 8, G, s);
+      }
+    }
+  } else {
+    constexpr int NG = D / 32;                   // scale groups per row
+    float sc[NG];
+    if (row_mode) {
+      const float r = load_scale(pp.ks, row, 0, D, true);
+#pragma unroll
+      for (int g = 0; g < NG; ++g) sc[g] = r;
+    } else {
+#pragma unroll
+      for (int g = 0; g < NG; ++g) sc[g] = load_scale(pp.ks, row, g, D, false);
+    }
+    if (pool == KVC_POOL_INT8) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(pp.k) + row * D);
+      uint4 w[D / 16];
+#pragma unroll
+      for (int v = 0; v < D / 16; ++v) w[v] = __ldg(src + v);
+#pragma unroll
+      for (int v = 0; v < D / 16; ++v) {
+        const uint32_t r[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          float x[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            x[k] = static_cast<float>(static_cast<int8_t>(r[2 * hlf + (k >> 2)] >> (8 * (k & 3)))) *
+                   sc[(v * 16) / 32];
+          dot8<D>(x, qs, v * 16 + hlf * 8, G, s);
+        }
+      }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(pp.k) + row * (D / 2));
+      uint4 w[D / 32];
+#pragma unroll
+      for (int v = 0; v < D / 32; ++v) w[v] = __ldg(src + v);
+#pragma unroll
+      for (int v = 0; v < D / 32; ++v) {
+        const uint32_t r[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          float x[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)      // low nibble = even element; sign-extended
+            x[k] = static_cast<float>(static_cast<int32_t>(r[k4] << (28 - 4 * k)) >> 28) * sc[v];
+          dot8<D>(x, qs, v * 32 + k4 * 8, G, s);
+        }
+      }
+    }
+  }
+}
+
+// This lane's d / 32 columns of value row `row` of `pool`, dequantised.
+template <int D>
+__device__ __forceinline__ void load_value_cols(int pool, const PoolPtrs& pp, int64_t row, int lane,
+                                                bool row_mode, float (&v)[D / 32]) {
+  constexpr int NC = D / 32;
+  const int c0 = lane * NC;
+  if (pool == KVC_POOL_BF16) {
+    const uint16_t* src = static_cast<const uint16_t*>(pp.v) + row * D + c0;
+    if (NC == 4) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+      v[0] = __uint_as_float(w.x << 16);
+      v[1] = __uint_as_float(w.x & 0xffff0000u);
+      v[2] = __uint_as_float(w.y << 16);
+      v[3] = __uint_as_float(w.y & 0xffff0000u);
+    } else {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src));
+      v[0] = __uint_as_float(w << 16);
+      v[1 % NC] = __uint_as_float(w & 0xffff0000u);
+    }
+  } else if (pool == KVC_POOL_INT8) {
+    const float sc = load_scale(pp.vs, row, c0 / 32, D, row_mode);
+    const int8_t* src = static_cast<const int8_t*>(pp.v) + row * D + c0;
+    if (NC == 4) {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src));
+#pragma unroll
+      for (int k = 0; k < NC; ++k) v[k] = static_cast<float>(static_cast<int8_t>(w >> (8 * k))) * sc;
+    } else {
+      const uint16_t w = __ldg(reinterpret_cast<const uint16_t*>(src));
+#pragma unroll
+      for (int k = 0; k < NC; ++k) v[k] = static_cast<float>(static_cast<int8_t>(w >> (8 * k))) * sc;
+    }
+  } else {
+    const float sc = load_scale(pp.vs, row, c0 / 32, D, row_mode);
+    const uint8_t* src = static_cast<const uint8_t*>(pp.v) + row * (D / 2) + c0 / 2;
+    uint32_t w;
+    if (NC == 4) w = __ldg(reinterpret_cast<const uint16_t*>(src));
+    else w = __ldg(src);
+#pragma unroll
+    for (int k = 0; k < NC; ++k)
+      v[k] = static_cast<float>(static_cast<int32_t>(w << (28 - 4 * k)) >> 28) * sc;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeArgs a) {
+  constexpr int NC = D / 32;
+  __shared__ __align__(16) float qs[kMaxG][D];
+  __shared__ float wm[kWarps][kMaxG], wl[kWarps][kMaxG];
+  __shared__ float wacc[kWarps][kMaxG][D];
 
   const int u = blockIdx.x, split = blockIdx.y;
-  const int G = a.G, d = a.d, tid = threadIdx.x;
+  const int G = a.G, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool row_mode = a.quant_mode == KVC_QUANT_ROW_FP16;
-  const __nv_bfloat16* q = a.q + static_cast<int64_t>(u) * G * d;
-  for (int idx = tid; idx < G * d; idx += kThreads)
-    qs[idx / d][idx % d] = __bfloat162float(q[idx]);
-
+  const float cs = a.scale * kLog2e;
+  {
+    const __nv_bfloat16* q = a.q + static_cast<int64_t>(u) * G * D;
+    for (int idx = tid; idx < G * D; idx += kThreads) qs[idx / D][idx % D] = __bfloat162float(q[idx]) * cs;
+  }
   int cnt[KVC_N_POOLS];
   int n = 0;
+#pragma unroll
   for (int p = 0; p < KVC_N_POOLS; ++p) {
     cnt[p] = (p >= a.pool_lo && p < a.pool_hi) ? a.kept_count[p * a.U + u] : 0;
     n += cnt[p];
   }
   const int per = (n + a.splits - 1) / a.splits;
   const int lo = min(n, split * per), hi = min(n, lo + per);
+  __syncthreads();
 
-  // PV layout: thread = (row group rg, column c); 128 / d row groups.
-  const int rgs = kThreads / d;
-  const int rg = tid / d, col = tid % d;
-  float m[kMaxG], l[kMaxG], acc[kMaxG];
+  float m[kMaxG], l[kMaxG], acc[kMaxG][NC];
 #pragma unroll
   for (int h = 0; h < kMaxG; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
-    acc[h] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[h][c] = 0.f;
   }
-  const float cs = a.scale * kLog2e;
-  __syncthreads();
 
-  for (int base = lo; base < hi; base += kThreads) {
-    const int r = base + tid;
-    int pool = -1;
-    int64_t row = 0;
+  for (int base = lo + warp * 32; base < hi; base += kThreads) {
+    // ---- scores: lane = row
+    const int r = base + lane;
+    int pool = -1, rr = r;
     if (r < hi) {
-      int rr = r;
+#pragma unroll
       for (int p = 0; p < KVC_N_POOLS; ++p) {
-        if (rr < cnt[p]) {
-          pool = p;
-          break;
+        if (pool < 0) {
+          if (rr < cnt[p]) pool = p;
+          else rr -= cnt[p];
         }
-        rr -= cnt[p];
       }
-      row = static_cast<int64_t>(u) * a.capacity + rr;
     }
-    rpool[tid] = pool;
-    rrow[tid] = row;
-    // scores of this thread's row for every head
+    const int64_t row = static_cast<int64_t>(u) * a.capacity + rr;
     float s[kMaxG];
 #pragma unroll
     for (int h = 0; h < kMaxG; ++h) s[h] = 0.f;
-    if (pool >= 0) {
-      const void* kb = pool == KVC_POOL_BF16 ? a.pools.k_bf16
-                       : pool == KVC_POOL_INT8 ? a.pools.k_i8 : a.pools.k_i4;
-      const void* ksp = pool == KVC_POOL_INT8 ? a.pools.k_i8_scale : a.pools.k_i4_scale;
-      for (int e = 0; e < d; ++e) {
-        const float kv = load_elem(pool, kb, ksp, row, e, d, row_mode);
+    if (pool >= 0) key_dot<D>(pool, pool_ptrs(a.pools, pool), row, row_mode, qs, G, s);
+    // ---- online softmax per head over this step's 32 rows (log2 domain)
+    float pr[kMaxG];
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h)
-          if (h < G) s[h] = fmaf(kv, qs[h][e], s[h]);
+    for (int h = 0; h < kMaxG; ++h) {
+      if (h < G) {
+        const float sv = pool >= 0 ? s[h] : -INFINITY;
+        float mx = sv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        const float mn = fmaxf(m[h], mx);          // finite: the step has a row
+        const float corr = m[h] == -INFINITY ? 0.f : exp2f(m[h] - mn);
+        pr[h] = pool >= 0 ? exp2f(sv - mn) : 0.f;
+        float sm = pr[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kFull, sm, o);
+        l[h] = l[h] * corr + sm;
+        m[h] = mn;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[h][c] *= corr;
       }
     }
+    // ---- P V: lane = columns; the step's rows eight at a time, their loads
+    // issued together; row j's pool and place come from lane j
+#pragma unroll 1
+    for (int j0 = 0; j0 < 32; j0 += 8) {
+      if (base + j0 >= hi) break;                 // uniform across the warp
+      float v[8][NC];
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) sc[tid][h] = pool >= 0 ? s[h] * cs : -INFINITY;
-    __syncthreads();
-    // chunk max per head (warp w handles heads w, w+4)
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int h = warp; h < G; h += kThreads / 32) {
-      float mx = -INFINITY;
-      for (int k = lane; k < kThreads; k += 32) mx = fmaxf(mx, sc[k][h]);
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      if (lane == 0) cmax[h] = mx;
-    }
-    __syncthreads();
-    // probabilities relative to the new running max
+      for (int k = 0; k < 8; ++k) {
+        const int pk = __shfl_sync(kFull, pool, j0 + k);
+        const int rk = __shfl_sync(kFull, rr, j0 + k);
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) {
-      if (h >= G) break;
-      const float mn = fmaxf(m[h], cmax[h]);
-      sc[tid][h] = (sc[tid][h] == -INFINITY) ? 0.f : exp2f(sc[tid][h] - mn);
-    }
-    __syncthreads();
-    for (int h = warp; h < G; h += kThreads / 32) {
-      float sm = 0.f;
-      for (int k = lane; k < kThreads; k += 32) sm += sc[k][h];
-      for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-      if (lane == 0) csum[h] = sm;
-    }
-    __syncthreads();
+        for (int c = 0; c < NC; ++c) v[k][c] = 0.f;
+        if (pk >= 0)
+          load_value_cols<D>(pk, pool_ptrs(a.pools, pk), static_cast<int64_t>(u) * a.capacity + rk,
+                             lane, row_mode, v[k]);
+      }
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) {
-      if (h >= G) break;
-      const float mn = fmaxf(m[h], cmax[h]);
-      const float corr = (m[h] == -INFINITY) ? 0.f : exp2f(m[h] - mn);
-      l[h] = l[h] * corr + csum[h];
-      acc[h] *= corr;
-      m[h] = mn;
-    }
-    // P V for this thread's column over its row group
-    for (int k = rg; k < kThreads; k += rgs) {
-      const int pool_k = rpool[k];
-      if (pool_k < 0) continue;
-      const void* vb = pool_k == KVC_POOL_BF16 ? a.pools.v_bf16
-                       : pool_k == KVC_POOL_INT8 ? a.pools.v_i8 : a.pools.v_i4;
-      const void* vsp = pool_k == KVC_POOL_INT8 ? a.pools.v_i8_scale : a.pools.v_i4_scale;
-      const float vv = load_elem(pool_k, vb, vsp, rrow[k], col, d, row_mode);
+      for (int k = 0; k < 8; ++k) {
 #pragma unroll
-      for (int h = 0; h < kMaxG; ++h)
-        if (h < G) acc[h] = fmaf(sc[k][h], vv, acc[h]);
+        for (int h = 0; h < kMaxG; ++h) {
+          if (h < G) {
+            const float pj = __shfl_sync(kFull, pr[h], j0 + k);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[h][c] = fmaf(pj, v[k][c], acc[h][c]);
+          }
+        }
+      }
     }
-    __syncthreads();
   }
 
-  // combine the row groups of each column
-  if (rgs > 1) {
-    for (int g = 1; g < rgs; ++g) {
-      if (rg == g)
-        for (int h = 0; h < G; ++h) accs[col][h] = acc[h];
-      __syncthreads();
-      if (rg == 0)
-        for (int h = 0; h < G; ++h) acc[h] += accs[col][h];
-      __syncthreads();
+  // ---- merge the warps of the CTA (Eq. 15), then write out or publish
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
+    if (h < G) {
+      if (lane == 0) {
+        wm[warp][h] = m[h];
+        wl[warp][h] = l[h];
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c) wacc[warp][h][lane * NC + c] = acc[h][c];
     }
   }
-  if (rg != 0) return;
-  if (a.splits == 1) {
-    for (int h = 0; h < G; ++h) {
-      const float o = l[h] > 0.f ? acc[h] / l[h] : 0.f;
-      a.out[(static_cast<int64_t>(u) * G + h) * d + col] = __float2bfloat16_rn(o);
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int h = idx / D, col = idx % D;
+    float v = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) v = fmaxf(v, wm[w][h]);
+    float num = 0.f, den = 0.f;
+    if (v != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        if (wm[w][h] == -INFINITY) continue;       // a warp that saw no row
+        const float f = exp2f(wm[w][h] - v);
+        num += f * wacc[w][h][col];
+        den += f * wl[w][h];
+      }
     }
-  } else {
-    for (int h = 0; h < G; ++h) {
+    if (a.splits == 1) {
+      const float o = den > 0.f ? num / den : 0.f;
+      a.out[(static_cast<int64_t>(u) * G + h) * D + col] = __float2bfloat16_rn(o);
+    } else {
       const int64_t slot = (static_cast<int64_t>(u) * a.splits + split) * G + h;
-      a.ws_acc[slot * d + col] = acc[h];
+      a.ws_acc[slot * D + col] = num;
       if (col == 0) {
-        a.ws_ml[slot * 2] = m[h];
-        a.ws_ml[slot * 2 + 1] = l[h];
+        a.ws_ml[slot * 2] = v;
+        a.ws_ml[slot * 2 + 1] = den;
       }
     }
   }
@@ -223,7 +366,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  decode_kernel<<<dim3(a.U, a.splits), kThreads, 0, stream>>>(a);
+  if (a.d == 64) decode_kernel<64><<<dim3(a.U, a.splits), kThreads, 0, stream>>>(a);
+  else decode_kernel<128><<<dim3(a.U, a.splits), kThreads, 0, stream>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || a.splits == 1) return err;
   merge_kernel<<<dim3(a.U, a.G), 128, 0, stream>>>(a);

@@ -201,8 +201,10 @@ kvc_status plan_select(const kvc_shape* s, const kvc_policy* pol, SelectPlan* sp
 int decode_splits(const kvc_shape* s, const kvc_policy* pol, int sms) {
   const int64_t U = n_units(s);
   const int64_t rows = static_cast<int64_t>(pol->capacity) * (pol->budget_bytes > 0 ? 3 : 1);
-  int64_t want = (2LL * sms + U - 1) / U;
-  const int64_t most = std::max<int64_t>(1, (rows + 255) / 256);
+  // about eight CTAs (32 warps) per SM to keep enough row loads in flight,
+  // but no split shorter than 128 rows
+  int64_t want = (8LL * sms + U - 1) / U;
+  const int64_t most = std::max<int64_t>(1, (rows + 127) / 128);
   want = std::min<int64_t>(std::min<int64_t>(want, most), 32);
   return static_cast<int>(std::max<int64_t>(want, 1));
 }
