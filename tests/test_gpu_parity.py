@@ -256,3 +256,19 @@ def test_parity_full_size_sampled_units(kvc, make):
         check_unit(w, x, p, u)
     del p, x
     torch.cuda.empty_cache()
+
+
+def test_parity_million_token_stage_a_sampled_units(kvc):
+    """The 1,048,576-row session (8 layers, 64 units, 34 GB of K/V): one
+    compaction to 2,048 renumbered rows, two units checked end to end."""
+    w = wl.million_token_8l()
+    x = wl.make_inputs(w, device="cuda")
+    p = run_pass(w, x)
+    assert int(p.score_status.abs().sum()) == 0
+    assert int(p.compact_status.abs().sum()) == 0
+    assert torch.equal(p.kept_count[2], torch.full((w.n_units,), w.budget_tokens, dtype=torch.int32,
+                                                  device="cuda"))
+    for u in _sample_units(w, n=2):
+        check_unit(w, x, p, u)
+    del p, x
+    torch.cuda.empty_cache()
