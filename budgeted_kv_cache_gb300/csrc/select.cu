@@ -471,6 +471,211 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   }
 }
 
+// ----------------------------------------------------------------------------
+// Token / page mode with at most 32,768 items per unit.  Item q * 1024 + t
+// (q < 32) belongs to thread t, so every load is coalesced, all 32 of a
+// thread's scores and flags are requested before any is used, and the keys
+// stay in registers through the radix passes.  In index order the items of
+// slab q come thread by thread, so the write-out needs one ballot per slab
+// and one block scan over the 1,024 (slab, warp) counts.  Same rule and
+// same results as select_kernel (forced items, then the top k candidates by
+// (score descending, index ascending)).
+constexpr int kFastSlabs = 32;
+constexpr int kFastMaxItems = kThreads * kFastSlabs;
+
+__global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_constant__ SelectArgs a) {
+  __shared__ uint32_t hist_w[32 * 256];     // per-warp histograms
+  __shared__ unsigned long long wtot[32];
+  __shared__ uint32_t scan_w[32];
+  __shared__ uint32_t s_cnt[kFastSlabs * 32];
+  __shared__ uint32_t s_red[4];
+  __shared__ uint32_t s_kmin, s_kmax;
+  __shared__ int s_bin;
+  __shared__ unsigned long long s_above;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int u = blockIdx.x;
+  const int b = u / (a.L * a.Hkv);
+  const int n = static_cast<int>(a.n_items);
+  const float* sc = a.scores + static_cast<int64_t>(u) * n;
+  const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * n : nullptr;
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  // ---------------- classify
+  float v[kFastSlabs];
+  uint8_t f[kFastSlabs];
+#pragma unroll
+  for (int q = 0; q < kFastSlabs; ++q) {
+    const int i = q * kThreads + tid;
+    v[q] = i < n ? __ldg(sc + i) : 0.f;
+    f[q] = (fl != nullptr && i < n) ? __ldg(fl + i) : 0;
+  }
+  uint32_t key[kFastSlabs];
+  uint32_t forced_bits = 0;
+  uint32_t n_forced = 0, n_cand = 0, kmin = 0xffffffffu, kmax = 0u;
+  int err = 0;
+#pragma unroll
+  for (int q = 0; q < kFastSlabs; ++q) {
+    const int i = q * kThreads + tid;
+    key[q] = 0;
+    if (i < n) {
+      const bool window = i < a.sink_items || i >= n - a.recent_items;
+      const bool protect = f[q] & KVC_FLAG_PROTECT;
+      const bool exclude = f[q] & KVC_FLAG_EXCLUDE;
+      if (protect && exclude) err = 1;
+      const bool forced = window || protect;
+      const bool excluded = exclude && !window;
+      if (forced) {
+        forced_bits |= 1u << q;
+        ++n_forced;
+      } else if (!excluded) {
+        key[q] = order_key(v[q]);
+        ++n_cand;
+        kmin = min(kmin, key[q]);
+        kmax = max(kmax, key[q]);
+      }
+    }
+  }
+  if (tid == 0) {
+    s_red[0] = s_red[1] = s_red[2] = 0;
+    s_kmin = 0xffffffffu;
+    s_kmax = 0u;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    n_forced += __shfl_xor_sync(kFull, n_forced, o);
+    n_cand += __shfl_xor_sync(kFull, n_cand, o);
+    err |= __shfl_xor_sync(kFull, err, o);
+    kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+  }
+  if (lane == 0) {
+    atomicAdd(&s_red[0], n_forced);
+    atomicAdd(&s_red[1], n_cand);
+    atomicOr(&s_red[2], static_cast<uint32_t>(err));
+    atomicMin(&s_kmin, kmin);
+    atomicMax(&s_kmax, kmax);
+  }
+  __syncthreads();
+  n_forced = s_red[0];
+  n_cand = s_red[1];
+  err = static_cast<int>(s_red[2]);
+  kmin = s_kmin;
+  kmax = s_kmax;
+
+  int32_t* cnt = a.kept_count;
+  if (err || n_forced > static_cast<uint32_t>(a.budget_items)) {
+    if (tid < KVC_N_POOLS) cnt[tid * a.U + u] = 0;
+    if (tid == 0) {
+      a.unit_status[u] = err ? KVC_UNIT_BAD_FLAGS : KVC_UNIT_OVER_BUDGET;
+      if (a.floor_excess) a.floor_excess[u] = 0;
+    }
+    return;
+  }
+  const uint32_t k = min(static_cast<uint32_t>(a.budget_items) - n_forced, n_cand);
+
+  // ---------------- radix select of the k-th largest candidate key
+  // (8-bit digits over the bits where candidate keys differ; t counts the
+  // candidates still to place below the prefix)
+  uint32_t tau = 0xffffffffu, take_ties = 0;
+  if (k > 0) {
+    uint32_t t = k - 1;
+    uint32_t* whist = hist_w + warp * 256;
+    const int top = (kmin == kmax) ? -1 : 31 - __clz(kmin ^ kmax);
+    uint64_t pfx = static_cast<uint64_t>(kmax) >> (top + 1);
+    for (int hi = top; hi >= 0; hi -= 8) {
+      const int shift = max(0, hi - 7);
+      const int width = hi - shift + 1;
+      const uint32_t nb = 1u << width;
+      for (int i = lane; i < 256; i += 32) whist[i] = 0;
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < kFastSlabs; ++q)
+        if (key[q] != 0 && (static_cast<uint64_t>(key[q]) >> (hi + 1)) == pfx)
+          atomicAdd(&whist[(key[q] >> shift) & (nb - 1)], 1u);
+      if (tid == 0) s_bin = -1;
+      __syncthreads();
+      unsigned long long local = 0;
+      if (tid < static_cast<int>(nb)) {
+        const int bn = static_cast<int>(nb) - 1 - tid;
+        for (int w = 0; w < 32; ++w) local += hist_w[w * 256 + bn];
+      }
+      unsigned long long total;
+      const unsigned long long run = block_excl_scan<unsigned long long>(local, wtot, total);
+      if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
+        s_bin = static_cast<int>(nb) - 1 - tid;
+        s_above = run;
+      }
+      __syncthreads();
+      const int bn = s_bin;                      // always found: t < candidates under pfx
+      t -= static_cast<uint32_t>(s_above);
+      pfx = (pfx << width) | static_cast<uint32_t>(bn);
+      __syncthreads();
+    }
+    tau = static_cast<uint32_t>(pfx);
+    take_ties = t + 1;
+  }
+
+  // ---------------- ranks of the ties (key == tau) in index order
+  uint32_t tie_bits = 0;
+#pragma unroll
+  for (int q = 0; q < kFastSlabs; ++q) {
+    const bool tie = k > 0 && key[q] != 0 && key[q] == tau;
+    const unsigned m = __ballot_sync(kFull, tie);
+    if (tie) tie_bits |= 1u << q;
+    if (lane == 0) s_cnt[q * 32 + warp] = __popc(m);
+  }
+  __syncthreads();
+  uint32_t tot;
+  const uint32_t tie_off = block_excl_scan<uint32_t>(s_cnt[tid], scan_w, tot);
+  __syncthreads();
+  s_cnt[tid] = tie_off;                           // exclusive offset of (slab, warp) = tid
+  __syncthreads();
+  uint32_t keep_bits = forced_bits;
+#pragma unroll
+  for (int q = 0; q < kFastSlabs; ++q) {
+    const unsigned m = __ballot_sync(kFull, (tie_bits >> q) & 1u);
+    const uint32_t rank = s_cnt[q * 32 + warp] + __popc(m & lt_mask);
+    const bool keep = (k > 0 && key[q] != 0 && key[q] > tau) || (((tie_bits >> q) & 1u) && rank < take_ties);
+    if (keep) keep_bits |= 1u << q;
+  }
+  __syncthreads();
+  // ---------------- output positions in index order, then the write
+#pragma unroll
+  for (int q = 0; q < kFastSlabs; ++q) {
+    const unsigned m = __ballot_sync(kFull, (keep_bits >> q) & 1u);
+    if (lane == 0) s_cnt[q * 32 + warp] = __popc(m);
+  }
+  __syncthreads();
+  uint32_t kept_total;
+  const uint32_t pos_off = block_excl_scan<uint32_t>(s_cnt[tid], scan_w, kept_total);
+  __syncthreads();
+  s_cnt[tid] = pos_off;
+  __syncthreads();
+  const int P = a.page_size;
+  int32_t* dst = a.kept_idx + (static_cast<int64_t>(KVC_POOL_BF16) * a.U + u) * a.capacity;
+#pragma unroll
+  for (int q = 0; q < kFastSlabs; ++q) {
+    const bool keep = (keep_bits >> q) & 1u;
+    const unsigned m = __ballot_sync(kFull, keep);
+    if (keep) {
+      const uint32_t pos = s_cnt[q * 32 + warp] + __popc(m & lt_mask);
+      const int i = q * kThreads + tid;
+      if (P == 1) {
+        dst[pos] = i;
+      } else {
+        for (int j = 0; j < P; ++j) dst[static_cast<int64_t>(pos) * P + j] = i * P + j;
+      }
+    }
+  }
+  if (tid < KVC_N_POOLS) cnt[tid * a.U + u] = tid == KVC_POOL_BF16 ? static_cast<int32_t>(kept_total) * P : 0;
+  if (tid == 0) {
+    a.unit_status[u] = KVC_UNIT_OK;
+    if (a.floor_excess) a.floor_excess[u] = 0;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes) {
@@ -478,6 +683,10 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_
     cudaError_t err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem_bytes));
     if (err != cudaSuccess) return err;
+  }
+  if (!a.byte_mode && a.n_items <= kFastMaxItems) {
+    select_fast_kernel<<<a.U, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
   }
   select_kernel<<<a.U, kThreads, smem_bytes, stream>>>(a);
   return cudaGetLastError();
