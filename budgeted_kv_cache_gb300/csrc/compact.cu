@@ -43,16 +43,127 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
   }
 }
 
-__device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8]) {
-  uint32_t r[4];
+// Re-rotation of one key row's 8 elements held by this lane (see the file
+// comment): x holds them, w their packed bf16 bits; on return both hold the
+// rotated row.  Called by whole warps (the shuffles need every lane).
+__device__ __forceinline__ void rerotate_lane(int lpr, int hl, bool rotate, const float4 (&tab)[4],
+                                              float (&x)[8], uint4& w) {
+  const int px = lpr / 2;
+  uint4 ow;
+  ow.x = __shfl_xor_sync(kFull, w.x, px);
+  ow.y = __shfl_xor_sync(kFull, w.y, px);
+  ow.z = __shfl_xor_sync(kFull, w.z, px);
+  ow.w = __shfl_xor_sync(kFull, w.w, px);
+  float y[8];
+  unpack8(ow, y);
+  const bool first_half = hl < px;
+  float C4[4] = {1.f, 1.f, 1.f, 1.f}, S4[4] = {0.f, 0.f, 0.f, 0.f};
+  if (rotate) {
+    const float cc0[4] = {tab[0].x, tab[0].y, tab[0].z, tab[0].w};
+    const float ss0[4] = {tab[1].x, tab[1].y, tab[1].z, tab[1].w};
+    const float cc1[4] = {tab[2].x, tab[2].y, tab[2].z, tab[2].w};
+    const float ss1[4] = {tab[3].x, tab[3].y, tab[3].z, tab[3].w};
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    r[k] = static_cast<uint32_t>(float_to_bf16_bits(x[2 * k])) |
-           (static_cast<uint32_t>(float_to_bf16_bits(x[2 * k + 1])) << 16);
-  return make_uint4(r[0], r[1], r[2], r[3]);
+    for (int k = 0; k < 4; ++k) {
+      float C = __fadd_rn(__fmul_rn(cc1[k], cc0[k]), __fmul_rn(ss1[k], ss0[k]));
+      float S = __fsub_rn(__fmul_rn(ss1[k], cc0[k]), __fmul_rn(cc1[k], ss0[k]));
+      const float nrm = __fsqrt_rn(__fadd_rn(__fmul_rn(C, C), __fmul_rn(S, S)));
+      C4[k] = __fdiv_rn(C, nrm);
+      S4[k] = __fdiv_rn(S, nrm);
+    }
+  }
+  float Cx[4], Sx[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    Cx[k] = __shfl_xor_sync(kFull, C4[k], px);
+    Sx[k] = __shfl_xor_sync(kFull, S4[k], px);
+  }
+  if (rotate) {
+    uint32_t rb[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float Ck = k < 4 ? (first_half ? C4[k] : Cx[k]) : (first_half ? Cx[k - 4] : C4[k - 4]);
+      const float Sk = k < 4 ? (first_half ? S4[k] : Sx[k]) : (first_half ? Sx[k - 4] : S4[k - 4]);
+      // first half holds x (partner y); second half holds y (partner x)
+      const float r = first_half ? __fsub_rn(__fmul_rn(x[k], Ck), __fmul_rn(y[k], Sk))
+                                 : __fadd_rn(__fmul_rn(x[k], Ck), __fmul_rn(y[k], Sk));
+      rb[k] = float_to_bf16_bits(r);              // stored bf16 value
+      x[k] = bf16_bits_to_float(static_cast<uint16_t>(rb[k]));
+    }
+    w = make_uint4(rb[0] | (rb[1] << 16), rb[2] | (rb[3] << 16), rb[4] | (rb[5] << 16),
+                   rb[6] | (rb[7] << 16));
+  }
 }
 
-__global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs a) {
+// Quantise this lane's 8 elements of one row and store codes and scales.
+__device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, int is_v, int lpr,
+                                                int hl, bool valid, int64_t row,
+                                                const float (&x)[8]) {
+  const int d = a.d;
+  const bool row_mode = a.quant_mode == KVC_QUANT_ROW_FP16;
+  const float qmax = pool == KVC_POOL_INT4 ? 7.f : 127.f;
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+  const int gl = row_mode ? lpr : 4;             // lanes per scale group
+  for (int o2 = 1; o2 < gl; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o2));
+  float sc = 1.f;
+  uint16_t s_bits;
+  if (!row_mode) {
+    if (amax > 0.f) {
+      sc = bf16_bits_to_float(float_to_bf16_bits(__fdiv_rn(amax, qmax)));
+      sc = fmaxf(sc, __uint_as_float(0x00010000u));          // 2^-133
+    }
+    s_bits = float_to_bf16_bits(sc);
+  } else {
+    if (amax > 0.f) {
+      sc = __half2float(__float2half_rn(__fdiv_rn(amax, qmax)));
+      sc = fminf(sc, 65504.f);
+      sc = fmaxf(sc, 5.9604644775390625e-08f);               // 2^-24
+    }
+    s_bits = __half_as_ushort(__float2half_rn(sc));
+  }
+  int qv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    int q = amax > 0.f ? __float2int_rn(__fdiv_rn(x[k], sc)) : 0;
+    q = q > static_cast<int>(qmax) ? static_cast<int>(qmax) : q;
+    q = q < -static_cast<int>(qmax) ? -static_cast<int>(qmax) : q;
+    qv[k] = q;
+  }
+  if (!valid) return;
+  if (pool == KVC_POOL_INT8) {
+    uint8_t* dst = static_cast<uint8_t*>(is_v ? a.pools.v_i8 : a.pools.k_i8);
+    uint2 pk;
+    pk.x = (qv[0] & 0xff) | ((qv[1] & 0xff) << 8) | ((qv[2] & 0xff) << 16) | ((qv[3] & 0xff) << 24);
+    pk.y = (qv[4] & 0xff) | ((qv[5] & 0xff) << 8) | ((qv[6] & 0xff) << 16) | ((qv[7] & 0xff) << 24);
+    *reinterpret_cast<uint2*>(dst + row * d + hl * 8) = pk;
+  } else {
+    uint8_t* dst = static_cast<uint8_t*>(is_v ? a.pools.v_i4 : a.pools.k_i4);
+    uint32_t pk = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      pk |= static_cast<uint32_t>((qv[2 * k] & 0xf) | ((qv[2 * k + 1] & 0xf) << 4)) << (8 * k);
+    *reinterpret_cast<uint32_t*>(dst + row * (d / 2) + hl * 4) = pk;
+  }
+  void* sp = pool == KVC_POOL_INT8 ? (is_v ? a.pools.v_i8_scale : a.pools.k_i8_scale)
+                                   : (is_v ? a.pools.v_i4_scale : a.pools.k_i4_scale);
+  uint16_t* sdst = static_cast<uint16_t*>(sp);
+  if (!row_mode) {
+    if ((hl & 3) == 0) sdst[row * (d / 32) + hl / 4] = s_bits;
+  } else {
+    if (hl == 0) sdst[row] = s_bits;
+  }
+}
+
+// Each lane group moves kRows rows.  The loads of every stage (kept index;
+// row and position; rotation tables) are issued for all of them through
+// the read-only path before any is consumed, and the one status word a bad
+// index sets is written after the last load, so the loads of the rows are
+// not ordered behind a store.
+constexpr int kRows = 2;
+
+__global__ void __launch_bounds__(kThreads, 3) compact_kernel(const CompactArgs a) {
   const int d = a.d;
   const int lpr = d / 8;                        // lanes per row (16 B = 8 bf16 per lane)
   const int rows_per_warp = 32 / lpr;
@@ -62,182 +173,108 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   const int is_v = blockIdx.z & 1;              // K rows and V rows go to separate warps
   const int pool = a.pool_lo + (blockIdx.z >> 1);
   const int u = blockIdx.y;
-  const int64_t i = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * rows_per_warp + sub;
   const int U = a.U;
   const int cap = a.capacity;
-  const int cnt = a.kept_count[pool * U + u];
-  bool valid = i < cnt;
-  if (__all_sync(kFull, !valid)) return;
+  const int cnt = __ldg(a.kept_count + pool * U + u);
+  const int64_t i_base =
+      (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kRows * rows_per_warp + sub;
+  if (__all_sync(kFull, i_base >= cnt)) return;
 
-  const int64_t slot = (static_cast<int64_t>(pool) * U + u) * cap + i;
-  int32_t t = 0, p = 0, p2 = 0;
-  bool rotate = false;
-  if (valid) {
-    t = a.kept_idx[slot];
-    if (t < 0 || t >= a.T) {
-      valid = false;
-      if (hl == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
-    }
+  const int64_t slot0 = (static_cast<int64_t>(pool) * U + u) * cap;
+  bool valid[kRows];
+  int32_t t[kRows];
+#pragma unroll
+  for (int n = 0; n < kRows; ++n) {
+    const int64_t i = i_base + n * rows_per_warp;
+    valid[n] = i < cnt;
+    t[n] = valid[n] ? __ldg(a.kept_idx + slot0 + i) : 0;
   }
-  uint4 w = make_uint4(0, 0, 0, 0);
+  bool bad = false;
+  uint4 w[kRows];
+  int32_t p[kRows];
   const __nv_bfloat16* src = is_v ? a.v : a.k;
-  if (valid) w = *reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(u) * a.T + t) * d + hl * 8);
-  if (valid && !is_v) {
-    p = a.pos_in[static_cast<int64_t>(u) * a.T + t];
-    p2 = p;
-    if (a.renumber) {
-      // rank among the kept rows of every pool (pools are disjoint, ascending)
-      int rank = static_cast<int>(i);
-      for (int q = 0; q < KVC_N_POOLS; ++q) {
-        if (q == pool) continue;
-        const int cq = a.kept_count[q * U + u];
-        if (cq > 0)
-          rank += lower_bound_i32(a.kept_idx + (static_cast<int64_t>(q) * U + u) * cap, cq, t);
-      }
-      p2 = rank;
+#pragma unroll
+  for (int n = 0; n < kRows; ++n) {
+    if (valid[n] && (t[n] < 0 || t[n] >= a.T)) {
+      valid[n] = false;
+      bad = true;
     }
-    rotate = p2 != p;
-    if (rotate && (p < 0 || p >= a.rope_max_pos || p2 < 0 || p2 >= a.rope_max_pos)) {
-      valid = false;
-      rotate = false;
-      if (hl == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
+    w[n] = valid[n] ? __ldg(reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(u) * a.T + t[n]) * d) + hl)
+                    : make_uint4(0, 0, 0, 0);
+    p[n] = (valid[n] && !is_v) ? __ldg(a.pos_in + static_cast<int64_t>(u) * a.T + t[n]) : 0;
+  }
+  int32_t p2[kRows];
+  bool rotate[kRows];
+#pragma unroll
+  for (int n = 0; n < kRows; ++n) {
+    p2[n] = p[n];
+    rotate[n] = false;
+    if (valid[n] && !is_v) {
+      if (a.renumber) {
+        // rank among the kept rows of every pool (pools are disjoint, ascending)
+        int rank = static_cast<int>(i_base + n * rows_per_warp);
+        for (int q = 0; q < KVC_N_POOLS; ++q) {
+          if (q == pool) continue;
+          const int cq = __ldg(a.kept_count + q * U + u);
+          if (cq > 0)
+            rank += lower_bound_i32(a.kept_idx + (static_cast<int64_t>(q) * U + u) * cap, cq, t[n]);
+        }
+        p2[n] = rank;
+      }
+      rotate[n] = p2[n] != p[n];
+      if (rotate[n] && (p[n] < 0 || p[n] >= a.rope_max_pos || p2[n] < 0 || p2[n] >= a.rope_max_pos)) {
+        valid[n] = false;
+        rotate[n] = false;
+        bad = true;
+      }
     }
   }
-
-  float x[8];
-  unpack8(w, x);
-  // Re-rotation (key warps only; the branch is warp-uniform).  Lane hl holds
-  // elements 8 hl .. 8 hl + 7; its split-half partner is lane hl ^ (lpr / 2).
-  // The two lanes of a pair need the same 8 (C, S): each computes four of
-  // them and they swap the other four.
-  if (!is_v && __any_sync(kFull, rotate)) {
-    const int px = lpr / 2;
-    uint4 ow;
-    ow.x = __shfl_xor_sync(kFull, w.x, px);
-    ow.y = __shfl_xor_sync(kFull, w.y, px);
-    ow.z = __shfl_xor_sync(kFull, w.z, px);
-    ow.w = __shfl_xor_sync(kFull, w.w, px);
-    float y[8];
-    unpack8(ow, y);
-    const bool first_half = hl < px;
-    const int j0 = (hl % px) * 8 + (first_half ? 0 : 4);   // the four pairs this lane forms
-    float C4[4] = {1.f, 1.f, 1.f, 1.f}, S4[4] = {0.f, 0.f, 0.f, 0.f};
-    if (rotate) {
-      const int half = d / 2;
-      const float4 c0 = *reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p) * half + j0);
-      const float4 s0 = *reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p) * half + j0);
-      const float4 c1 = *reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p2) * half + j0);
-      const float4 s1 = *reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p2) * half + j0);
-      const float cc0[4] = {c0.x, c0.y, c0.z, c0.w}, ss0[4] = {s0.x, s0.y, s0.z, s0.w};
-      const float cc1[4] = {c1.x, c1.y, c1.z, c1.w}, ss1[4] = {s1.x, s1.y, s1.z, s1.w};
+  // rotation tables: cos / sin of the old and new position for the four
+  // (C, S) pairs this lane forms
+  const int px = lpr / 2;
+  const int j0 = (hl % px) * 8 + (hl < px ? 0 : 4);
+  const int half = d / 2;
+  float4 tab[kRows][4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float C = __fadd_rn(__fmul_rn(cc1[k], cc0[k]), __fmul_rn(ss1[k], ss0[k]));
-        float S = __fsub_rn(__fmul_rn(ss1[k], cc0[k]), __fmul_rn(cc1[k], ss0[k]));
-        const float nrm = __fsqrt_rn(__fadd_rn(__fmul_rn(C, C), __fmul_rn(S, S)));
-        C4[k] = __fdiv_rn(C, nrm);
-        S4[k] = __fdiv_rn(S, nrm);
-      }
-    }
-    float Cx[4], Sx[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      Cx[k] = __shfl_xor_sync(kFull, C4[k], px);
-      Sx[k] = __shfl_xor_sync(kFull, S4[k], px);
-    }
-    if (rotate) {
-      float C[8], S[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        C[k] = first_half ? C4[k] : Cx[k];
-        S[k] = first_half ? S4[k] : Sx[k];
-        C[k + 4] = first_half ? Cx[k] : C4[k];
-        S[k + 4] = first_half ? Sx[k] : S4[k];
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        // first half holds x (partner y); second half holds y (partner x)
-        const float r = first_half ? __fsub_rn(__fmul_rn(x[k], C[k]), __fmul_rn(y[k], S[k]))
-                                   : __fadd_rn(__fmul_rn(x[k], C[k]), __fmul_rn(y[k], S[k]));
-        x[k] = bf16_bits_to_float(float_to_bf16_bits(r));   // stored bf16 value
-      }
-      w = pack8_bf16(x);
-    }
-  }
-
-  const int64_t row = static_cast<int64_t>(u) * cap + i;
-  if (pool == KVC_POOL_BF16) {
-    if (valid) {
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.pools.v_bf16 : a.pools.k_bf16);
-      *reinterpret_cast<uint4*>(dst + row * d + hl * 8) = w;
-    }
-  } else {
-    const bool row_mode = a.quant_mode == KVC_QUANT_ROW_FP16;
-    const float qmax = pool == KVC_POOL_INT4 ? 7.f : 127.f;
-    float amax = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
-    const int gl = row_mode ? lpr : 4;             // lanes per scale group
-    for (int o2 = 1; o2 < gl; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o2));
-    float sc = 1.f;
-    uint16_t s_bits;
-    if (!row_mode) {
-      if (amax > 0.f) {
-        sc = bf16_bits_to_float(float_to_bf16_bits(__fdiv_rn(amax, qmax)));
-        sc = fmaxf(sc, __uint_as_float(0x00010000u));          // 2^-133
-      }
-      s_bits = float_to_bf16_bits(sc);
+  for (int n = 0; n < kRows; ++n) {
+    if (rotate[n]) {
+      tab[n][0] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p[n]) * half + j0));
+      tab[n][1] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p[n]) * half + j0));
+      tab[n][2] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p2[n]) * half + j0));
+      tab[n][3] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p2[n]) * half + j0));
     } else {
-      if (amax > 0.f) {
-        sc = __half2float(__float2half_rn(__fdiv_rn(amax, qmax)));
-        sc = fminf(sc, 65504.f);
-        sc = fmaxf(sc, 5.9604644775390625e-08f);               // 2^-24
-      }
-      s_bits = __half_as_ushort(__float2half_rn(sc));
-    }
-    int qv[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      int q = amax > 0.f ? __float2int_rn(__fdiv_rn(x[k], sc)) : 0;
-      q = q > static_cast<int>(qmax) ? static_cast<int>(qmax) : q;
-      q = q < -static_cast<int>(qmax) ? -static_cast<int>(qmax) : q;
-      qv[k] = q;
-    }
-    if (valid) {
-      if (pool == KVC_POOL_INT8) {
-        uint8_t* dst = static_cast<uint8_t*>(is_v ? a.pools.v_i8 : a.pools.k_i8);
-        uint2 pk;
-        pk.x = (qv[0] & 0xff) | ((qv[1] & 0xff) << 8) | ((qv[2] & 0xff) << 16) | ((qv[3] & 0xff) << 24);
-        pk.y = (qv[4] & 0xff) | ((qv[5] & 0xff) << 8) | ((qv[6] & 0xff) << 16) | ((qv[7] & 0xff) << 24);
-        *reinterpret_cast<uint2*>(dst + row * d + hl * 8) = pk;
-      } else {
-        uint8_t* dst = static_cast<uint8_t*>(is_v ? a.pools.v_i4 : a.pools.k_i4);
-        uint32_t pk = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          pk |= static_cast<uint32_t>((qv[2 * k] & 0xf) | ((qv[2 * k + 1] & 0xf) << 4)) << (8 * k);
-        *reinterpret_cast<uint32_t*>(dst + row * (d / 2) + hl * 4) = pk;
-      }
-      void* sp = pool == KVC_POOL_INT8 ? (is_v ? a.pools.v_i8_scale : a.pools.k_i8_scale)
-                                       : (is_v ? a.pools.v_i4_scale : a.pools.k_i4_scale);
-      uint16_t* sdst = static_cast<uint16_t*>(sp);
-      if (!row_mode) {
-        if ((hl & 3) == 0) sdst[row * (d / 32) + hl / 4] = s_bits;
-      } else {
-        if (hl == 0) sdst[row] = s_bits;
-      }
+      for (int k = 0; k < 4; ++k) tab[n][k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  if (valid && hl == 0 && !is_v) {
-    a.pools.pos_out[slot] = p2;
-    if (a.pools.orig_pos_out) a.pools.orig_pos_out[slot] = p;
+#pragma unroll
+  for (int n = 0; n < kRows; ++n) {
+    float x[8];
+    unpack8(w[n], x);
+    // the branch is warp-uniform: key warps only, and only if a row rotates
+    if (!is_v && __any_sync(kFull, rotate[n])) rerotate_lane(lpr, hl, rotate[n], tab[n], x, w[n]);
+    const int64_t i = i_base + n * rows_per_warp;
+    const int64_t row = static_cast<int64_t>(u) * cap + i;
+    if (pool == KVC_POOL_BF16) {
+      if (valid[n]) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.pools.v_bf16 : a.pools.k_bf16);
+        *reinterpret_cast<uint4*>(dst + row * d + hl * 8) = w[n];
+      }
+    } else {
+      store_quantised(a, pool, is_v, lpr, hl, valid[n], row, x);
+    }
+    if (valid[n] && hl == 0 && !is_v) {
+      a.pools.pos_out[slot0 + i] = p2[n];
+      if (a.pools.orig_pos_out) a.pools.orig_pos_out[slot0 + i] = p[n];
+    }
   }
+  if (bad && hl == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
 }
 
 }  // namespace
 
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
-  const int rows_per_block = (kThreads / 32) * (32 / (a.d / 8));
+  const int rows_per_block = (kThreads / 32) * (32 / (a.d / 8)) * kRows;
   const int bx = (a.capacity + rows_per_block - 1) / rows_per_block;
   const int n_pools = a.pool_hi - a.pool_lo;
   if (bx == 0 || n_pools <= 0) return cudaSuccess;
