@@ -163,7 +163,7 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
 // not ordered behind a store.
 constexpr int kRows = 2;
 
-__global__ void __launch_bounds__(kThreads, 3) compact_kernel(const CompactArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs a) {
   const int d = a.d;
   const int lpr = d / 8;                        // lanes per row (16 B = 8 bf16 per lane)
   const int rows_per_warp = 32 / lpr;
