@@ -372,6 +372,64 @@ def rerotate_bits(k_bits, p: int, p_new: int, cos_tab, sin_tab) -> np.ndarray:
     return f32_to_bf16_bits(np.concatenate([xr, yr], axis=-1))
 
 
+def reference_rerotate(k_bits, p: int, p_new: int, ref_bits, p_ref: int, cos_tab, sin_tab):
+    """Non-compounding re-rotation of one kept key through a reference store.
+
+    PACE Sec. 3.2 / App. D: at a key's first position-changing renumber a
+    copy of the stored key is kept together with the position p_ref it is
+    valid at, and every later position is derived from that copy (in fp32,
+    by rerotate_bits), so the key carries about two roundings however many
+    renumbers it survives.  Before use the copy is checked against the
+    stored key: rotated from p_ref to the key's current position p it must
+    reproduce the stored bits exactly; if it does not, the stored key is
+    used and becomes the new reference.
+
+    Returns (new key bits, reference bits, p_ref, check_failed); p_ref < 0
+    means "no reference" (the key has not been renumbered yet).
+    """
+    k_bits = np.asarray(k_bits, dtype=np.uint16)
+    if p_new == p:                                   # no renumber: carry as is
+        ref = None if p_ref < 0 else np.asarray(ref_bits, dtype=np.uint16).copy()
+        return k_bits.copy(), ref, p_ref, False
+    if p_ref >= 0:
+        ref = np.asarray(ref_bits, dtype=np.uint16)
+        if np.array_equal(rerotate_bits(ref, p_ref, p, cos_tab, sin_tab), k_bits):
+            return rerotate_bits(ref, p_ref, p_new, cos_tab, sin_tab), ref.copy(), p_ref, False
+        failed = True
+    else:
+        failed = False
+    return rerotate_bits(k_bits, p, p_new, cos_tab, sin_tab), k_bits.copy(), p, failed
+
+
+def renumber_drift(x, positions, cos_tab, sin_tab, use_store: bool) -> float:
+    """Relative error of a key renumbered along `positions` (PACE App. D).
+
+    x: exact pre-rotation key [d] (fp64).  The stored key starts as the bf16
+    rounding of x rotated (in fp64) to positions[0]; every later entry is a
+    renumber, done by re-rotating the stored key (use_store False) or through
+    the reference store.  Returns ||stored - exact|| / ||exact|| at the last
+    position, the exact key being x rotated in fp64 to it.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.size
+    h = d // 2
+
+    def exact(pos):
+        c = np.asarray(cos_tab[pos], np.float64)
+        s_ = np.asarray(sin_tab[pos], np.float64)
+        return np.concatenate([x[:h] * c - x[h:] * s_, x[h:] * c + x[:h] * s_])
+
+    k = f32_to_bf16_bits(exact(positions[0]).astype(np.float32))
+    ref, p_ref = None, -1
+    for p, p_new in zip(positions[:-1], positions[1:]):
+        if use_store:
+            k, ref, p_ref, _ = reference_rerotate(k, int(p), int(p_new), ref, p_ref, cos_tab, sin_tab)
+        else:
+            k = rerotate_bits(k, int(p), int(p_new), cos_tab, sin_tab)
+    e = exact(positions[-1])
+    return float(np.linalg.norm(bf16_bits_to_f32(k).astype(np.float64) - e) / np.linalg.norm(e))
+
+
 def new_positions(kept_sorted, pos_in, renumber: bool) -> np.ndarray:
     """p' = rank among the kept rows in logical order if renumbering, else p."""
     kept_sorted = np.asarray(kept_sorted)
@@ -522,6 +580,9 @@ class Pool:
     v: np.ndarray = None
     k_scale: np.ndarray = None      # fp32 [n][groups]
     v_scale: np.ndarray = None
+    k_ref: np.ndarray = None        # reference store: bf16 bits [n][d] (zeros: none)
+    p_ref: np.ndarray = None        # reference position [n] (-1: none)
+    ref_failures: int = 0           # kept keys whose reference failed its check
 
 
 @dataclass
@@ -564,8 +625,15 @@ def select_unit(scores, page_scores, n_tokens, head_dim, params: PassParams,
     return act, 0, st
 
 
-def compact_unit(k_bits, v_bits, pos_in, actions, params: PassParams, cos_tab, sin_tab):
-    """Gather, re-rotate and quantise the kept rows of one unit into pools."""
+def compact_unit(k_bits, v_bits, pos_in, actions, params: PassParams, cos_tab, sin_tab,
+                 ref_bits=None, ref_pos=None):
+    """Gather, re-rotate and quantise the kept rows of one unit into pools.
+
+    With a reference store (ref_bits [T][d] bf16 bits, ref_pos [T], -1 = no
+    reference) kept keys are re-rotated by reference_rerotate and each pool
+    carries its rows' references forward (PACE Sec. 3.2: moved with the slot
+    when rows are compacted).
+    """
     actions = np.asarray(actions)
     kept_all = np.nonzero(actions != ACT_RELEASE)[0]
     p_new_all = new_positions(kept_all, pos_in, params.renumber)
@@ -578,8 +646,18 @@ def compact_unit(k_bits, v_bits, pos_in, actions, params: PassParams, cos_tab, s
         pool.pos = np.array([new_of[int(i)] for i in idx], dtype=np.int64)
         d = k_bits.shape[-1]
         kr = np.zeros((idx.size, d), dtype=np.uint16)
-        for n, (i, p, p2) in enumerate(zip(idx, pool.orig_pos, pool.pos)):
-            kr[n] = rerotate_bits(k_bits[i], int(p), int(p2), cos_tab, sin_tab)
+        if ref_pos is None:
+            for n, (i, p, p2) in enumerate(zip(idx, pool.orig_pos, pool.pos)):
+                kr[n] = rerotate_bits(k_bits[i], int(p), int(p2), cos_tab, sin_tab)
+        else:
+            pool.k_ref = np.zeros((idx.size, d), dtype=np.uint16)
+            pool.p_ref = np.full(idx.size, -1, dtype=np.int64)
+            for n, (i, p, p2) in enumerate(zip(idx, pool.orig_pos, pool.pos)):
+                kr[n], ref, pr, bad = reference_rerotate(k_bits[i], int(p), int(p2), ref_bits[i],
+                                                         int(ref_pos[i]), cos_tab, sin_tab)
+                if pr >= 0:
+                    pool.k_ref[n], pool.p_ref[n] = ref, pr
+                pool.ref_failures += int(bad)
         vr = np.asarray(v_bits)[idx]
         if a == ACT_BF16:
             pool.k, pool.v = kr, vr
