@@ -59,6 +59,11 @@ class kvc_pools(ctypes.Structure):
 _LIB = None
 
 
+class kvc_ref_store(ctypes.Structure):
+    """Reference store of kvc_compact_rerotate_quant_ref (device pointers)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("ref_k", "ref_pos", "ref_k_out", "ref_pos_out", "failures")]
+
+
 def _load():
     global _LIB
     if _LIB is None:
@@ -68,12 +73,15 @@ def _load():
         P, I32, I64, U32, F32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                      ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t)
         SH, PO, PL = ctypes.POINTER(kvc_shape), ctypes.POINTER(kvc_policy), ctypes.POINTER(kvc_pools)
+        RS = ctypes.POINTER(kvc_ref_store)
         sig = {
             "kvc_score_workspace_bytes": (SZ, [SH, I32]),
             "kvc_score": (ctypes.c_int, [SH, P, P, I32, F32, P, P, I32, U32, P, P, P, P, SZ, P]),
             "kvc_select_workspace_bytes": (SZ, [SH, PO]),
             "kvc_select": (ctypes.c_int, [SH, PO, P, P, P, P, P, P, SZ, P]),
             "kvc_compact_rerotate_quant": (ctypes.c_int, [SH, PO, P, P, P, P, P, P, P, I64, PL, P, P]),
+            "kvc_compact_rerotate_quant_ref": (ctypes.c_int,
+                                               [SH, PO, P, P, P, P, P, P, P, I64, RS, PL, P, P]),
             "kvc_decode_workspace_bytes": (SZ, [SH, PO]),
             "kvc_decode_attn": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P, SZ, P]),
             "kvc_decode_attn_noalloc": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P]),
@@ -223,6 +231,19 @@ def kvc_compact_rerotate_quant(shape, policy: Policy, k_cache, v_cache, pos_in, 
         ctypes.byref(shape), ctypes.byref(cp), _p(k_cache), _p(v_cache), _p(pos_in),
         _p(kept_idx), _p(kept_count), _p(rope_cos), _p(rope_sin), int(rope_max_pos),
         ctypes.byref(cpools), _p(unit_status), _stream(stream)))
+
+
+def kvc_compact_rerotate_quant_ref(shape, policy: Policy, k_cache, v_cache, pos_in, kept_idx,
+                                   kept_count, rope_cos, rope_sin, rope_max_pos, ref_k, ref_pos,
+                                   ref_k_out, ref_pos_out, pools: Pools, failures=None,
+                                   unit_status=None, stream=None):
+    """kvc_compact_rerotate_quant through a key reference store (see include/kvc.h)."""
+    cp, cpools = policy.c(), pools.c()
+    rs = kvc_ref_store(_p(ref_k), _p(ref_pos), _p(ref_k_out), _p(ref_pos_out), _p(failures))
+    _check("kvc_compact_rerotate_quant_ref", _load().kvc_compact_rerotate_quant_ref(
+        ctypes.byref(shape), ctypes.byref(cp), _p(k_cache), _p(v_cache), _p(pos_in),
+        _p(kept_idx), _p(kept_count), _p(rope_cos), _p(rope_sin), int(rope_max_pos),
+        ctypes.byref(rs), ctypes.byref(cpools), _p(unit_status), _stream(stream)))
 
 
 def kvc_decode_workspace_bytes(shape, policy: Policy) -> int:

@@ -95,6 +95,27 @@ __device__ __forceinline__ void rerotate_lane(int lpr, int hl, bool rotate, cons
   }
 }
 
+// Re-rotation of this lane's part of one key row from position `from` to
+// `to` (rows whose `rot` is false are left as they are); whole warps call it.
+__device__ __forceinline__ void rotate_row(const CompactArgs& a, int lpr, int hl, bool rot,
+                                           int32_t from, int32_t to, uint4& w, float (&x)[8]) {
+  if (!__any_sync(kFull, rot)) return;
+  const int px = lpr / 2;
+  const int j0 = (hl % px) * 8 + (hl < px ? 0 : 4);
+  const int half = a.d / 2;
+  float4 tab[4];
+  if (rot) {
+    tab[0] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(from) * half + j0));
+    tab[1] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(from) * half + j0));
+    tab[2] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(to) * half + j0));
+    tab[3] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(to) * half + j0));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tab[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  rerotate_lane(lpr, hl, rot, tab, x, w);
+}
+
 // Quantise this lane's 8 elements of one row and store codes and scales.
 __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, int is_v, int lpr,
                                                 int hl, bool valid, int64_t row,
@@ -163,6 +184,7 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
 // not ordered behind a store.
 constexpr int kRows = 2;
 
+template <bool kStore>
 __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs a) {
   const int d = a.d;
   const int lpr = d / 8;                        // lanes per row (16 B = 8 bf16 per lane)
@@ -203,6 +225,25 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
                     : make_uint4(0, 0, 0, 0);
     p[n] = (valid[n] && !is_v) ? __ldg(a.pos_in + static_cast<int64_t>(u) * a.T + t[n]) : 0;
   }
+  // reference store (keys only): p_ref and the reference bits of each row
+  const bool use_store = kStore && !is_v;                       // block-uniform
+  int32_t pr[kRows];
+  uint4 wr[kRows];
+#pragma unroll
+  for (int n = 0; n < kRows; ++n) {
+    pr[n] = -1;
+    wr[n] = make_uint4(0, 0, 0, 0);
+    if (use_store && valid[n]) {
+      pr[n] = __ldg(a.ref.ref_pos + static_cast<int64_t>(u) * a.T + t[n]);
+      if (pr[n] >= a.rope_max_pos) {
+        valid[n] = false;
+        bad = true;
+      } else if (pr[n] >= 0) {
+        wr[n] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.ref.ref_k) +
+                                                     (static_cast<int64_t>(u) * a.T + t[n]) * d) + hl);
+      }
+    }
+  }
   int32_t p2[kRows];
   bool rotate[kRows];
 #pragma unroll
@@ -228,6 +269,13 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
         bad = true;
       }
     }
+  }
+  // with the store, rows rotate in their own branch below (no hoisted tables)
+  bool chg[kRows];
+#pragma unroll
+  for (int n = 0; n < kRows; ++n) {
+    chg[n] = use_store && rotate[n];
+    if (use_store) rotate[n] = false;
   }
   // rotation tables: cos / sin of the old and new position for the four
   // (C, S) pairs this lane forms
@@ -255,6 +303,42 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
     if (!is_v && __any_sync(kFull, rotate[n])) rerotate_lane(lpr, hl, rotate[n], tab[n], x, w[n]);
     const int64_t i = i_base + n * rows_per_warp;
     const int64_t row = static_cast<int64_t>(u) * cap + i;
+    if (use_store) {
+      // PACE reference store: check the copy (re-rotated p_ref -> p, it must
+      // reproduce the stored key in every lane of the row), then derive the
+      // new key from it, or from the stored key if there is no valid copy
+      const bool has_ref = valid[n] && pr[n] >= 0;
+      uint4 chk = wr[n];
+      float xc[8];
+      unpack8(chk, xc);
+      rotate_row(a, lpr, hl, chg[n] && has_ref && pr[n] != p[n], pr[n], p[n], chk, xc);
+      const bool lane_ok = chk.x == w[n].x && chk.y == w[n].y && chk.z == w[n].z && chk.w == w[n].w;
+      const unsigned gmask = (lpr == 32 ? kFull : ((1u << lpr) - 1u)) << (sub * lpr);
+      const bool ok = (__ballot_sync(kFull, lane_ok) & gmask) == gmask;
+      const bool use_ref = chg[n] && has_ref && ok;
+      const bool failed = chg[n] && has_ref && !ok;
+      uint4 nw = use_ref ? wr[n] : w[n];
+      const int32_t from = use_ref ? pr[n] : p[n];
+      float xs[8];
+      unpack8(nw, xs);
+      rotate_row(a, lpr, hl, chg[n] && from != p2[n], from, p2[n], nw, xs);
+      uint4 rw = has_ref ? wr[n] : make_uint4(0, 0, 0, 0);
+      int32_t rp = has_ref ? pr[n] : -1;
+      if (chg[n] && !use_ref) {            // first renumber, or a failed copy: the stored key
+        rw = w[n];
+        rp = p[n];
+      }
+      if (chg[n]) {
+        w[n] = nw;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = xs[k];
+      }
+      if (valid[n]) {
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ref.ref_k_out) + (slot0 + i) * d + hl * 8) = rw;
+        if (hl == 0) a.ref.ref_pos_out[slot0 + i] = rp;
+      }
+      if (failed && hl == 0 && a.ref.failures) atomicAdd(a.ref.failures + u, 1);
+    }
     if (pool == KVC_POOL_BF16) {
       if (valid[n]) {
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.pools.v_bf16 : a.pools.k_bf16);
@@ -279,7 +363,8 @@ cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
   const int n_pools = a.pool_hi - a.pool_lo;
   if (bx == 0 || n_pools <= 0) return cudaSuccess;
   dim3 grid(bx, a.U, 2 * n_pools);            // z: (pool, K or V)
-  compact_kernel<<<grid, kThreads, 0, stream>>>(a);
+  if (a.ref.ref_pos != nullptr) compact_kernel<true><<<grid, kThreads, 0, stream>>>(a);
+  else compact_kernel<false><<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -342,6 +342,18 @@ kvc_status kvc_compact_rerotate_quant(const kvc_shape* shape, const kvc_policy* 
                                       const float* rope_sin, int64_t rope_max_pos,
                                       const kvc_pools* pools, int32_t* unit_status,
                                       kvc_stream stream) {
+  return kvc_compact_rerotate_quant_ref(shape, policy, k_cache, v_cache, pos_in, kept_idx,
+                                        kept_count, rope_cos, rope_sin, rope_max_pos, nullptr,
+                                        pools, unit_status, stream);
+}
+
+kvc_status kvc_compact_rerotate_quant_ref(const kvc_shape* shape, const kvc_policy* policy,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* pos_in, const int32_t* kept_idx,
+                                          const int32_t* kept_count, const float* rope_cos,
+                                          const float* rope_sin, int64_t rope_max_pos,
+                                          const kvc_ref_store* ref, const kvc_pools* pools,
+                                          int32_t* unit_status, kvc_stream stream) {
   SelectPlan sp;
   kvc_status st = plan_select(shape, policy, &sp);
   if (st != KVC_OK) return st;
@@ -364,9 +376,16 @@ kvc_status kvc_compact_rerotate_quant(const kvc_shape* shape, const kvc_policy* 
         !aligned(pools->v_i4, 4))
       return KVC_ERR_INVALID_ARG;
   }
+  if (ref) {
+    if (!ref->ref_k || !ref->ref_pos || !ref->ref_k_out || !ref->ref_pos_out) return KVC_ERR_INVALID_ARG;
+    if (!aligned(ref->ref_k, 16) || !aligned(ref->ref_k_out, 16)) return KVC_ERR_INVALID_ARG;
+    if (!rope_cos || !rope_sin || rope_max_pos < 1 || !aligned(rope_cos, 16) || !aligned(rope_sin, 16))
+      return KVC_ERR_INVALID_ARG;
+  }
   DevInfo info;
   if ((st = check_device(&info)) != KVC_OK) return st;
   CompactArgs a = {};
+  if (ref) a.ref = *ref;
   a.U = static_cast<int32_t>(n_units(shape));
   a.d = shape->head_dim;
   a.T = shape->n_tokens;

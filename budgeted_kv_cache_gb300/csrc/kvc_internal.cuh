@@ -83,6 +83,7 @@ struct CompactArgs {
   kvc_pools pools;
   int32_t* unit_status;
   int32_t pool_lo, pool_hi;    // pools to process: [pool_lo, pool_hi)
+  kvc_ref_store ref;           // reference store (ref.ref_pos == NULL: none)
 };
 
 struct DecodeArgs {

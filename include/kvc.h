@@ -9,6 +9,7 @@
  *   kvc_select                  deterministic budgeted selection
  *   kvc_compact_rerotate_quant  gather kept K/V rows, re-rotate kept keys to
  *                               their new positions, quantise, store
+ *   kvc_compact_rerotate_quant_ref   the same through a key reference store
  *   kvc_decode_attn             one decode-attention step over the result
  *
  * Sources, cited by page title and section:
@@ -256,6 +257,49 @@ kvc_status kvc_compact_rerotate_quant(const kvc_shape* shape, const kvc_policy* 
                                       const float* rope_sin, int64_t rope_max_pos,
                                       const kvc_pools* pools, int32_t* unit_status,
                                       kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * kvc_compact_rerotate_quant_ref -- kvc_compact_rerotate_quant with a
+ * reference store for keys (non-compounding re-rotation).
+ *
+ * PACE Sec. 3.2 and App. D: re-rotating the stored bf16 key at every
+ * renumber adds one rounding per position change.  Instead, at a key's
+ * first position-changing renumber a copy of its stored bits is kept with
+ * the position p_ref it is valid at, and every later position is derived
+ * from that copy (same fp32 re-rotation as above, p_ref -> p').  Before use
+ * the copy is checked: re-rotated from p_ref to the key's current position
+ * p it must reproduce the stored key bit for bit; if it does not, the
+ * stored key is re-rotated (p -> p') and becomes the new reference, and the
+ * unit's failure counter is incremented.  A key whose position does not
+ * change keeps its stored bits and its reference (or none).  References
+ * move with the slot: the kept row's reference is written beside it.
+ *
+ * ref.ref_k        bf16 [U][T][d]: reference copy of every cached key
+ *                  (contents ignored where ref_pos < 0); 16-byte aligned.
+ * ref.ref_pos      int32 [U][T]: p_ref, or -1 for "no reference".
+ * ref.ref_k_out    bf16 [KVC_N_POOLS][U][capacity][d]: references of the
+ *                  kept rows (zeros where none); 16-byte aligned.
+ * ref.ref_pos_out  int32 [KVC_N_POOLS][U][capacity]: their p_ref (-1: none).
+ * ref.failures     optional int32 [U]: incremented once per kept key whose
+ *                  reference failed the check (the caller zeroes it).
+ * Every other argument and the behaviour of V rows, positions, pools and
+ * errors are those of kvc_compact_rerotate_quant.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* ref_k;
+  const int32_t* ref_pos;
+  void* ref_k_out;
+  int32_t* ref_pos_out;
+  int32_t* failures;
+} kvc_ref_store;
+
+kvc_status kvc_compact_rerotate_quant_ref(const kvc_shape* shape, const kvc_policy* policy,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* pos_in, const int32_t* kept_idx,
+                                          const int32_t* kept_count, const float* rope_cos,
+                                          const float* rope_sin, int64_t rope_max_pos,
+                                          const kvc_ref_store* ref, const kvc_pools* pools,
+                                          int32_t* unit_status, kvc_stream stream);
 
 /* ------------------------------------------------------------------------
  * kvc_decode_attn -- one decode-attention step over the compacted pools

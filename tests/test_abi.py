@@ -47,6 +47,18 @@ def test_status_strings(lib):
     assert f(3) == b"workspace missing or too small"
 
 
+def test_reference_store_call_checks_its_arguments(lib):
+    import budgeted_kv_cache_gb300 as kvc
+    kvc.library()
+    shape = kvc.make_shape(1, 1, 4, 2, 64, 100)
+    pol = kvc.Policy(budget_tokens=10, capacity=10, renumber=True).c()
+    rs = kvc.kvc_ref_store(None, None, None, None, None)
+    # no caches and an empty reference store: rejected before any launch
+    assert kvc.library().kvc_compact_rerotate_quant_ref(
+        ctypes.byref(shape), ctypes.byref(pol), None, None, None, None, None, None, None, 0,
+        ctypes.byref(rs), None, None, None) == 1
+
+
 def test_argument_errors_return_before_any_launch(lib):
     import budgeted_kv_cache_gb300 as kvc
     kvc.library()
