@@ -177,6 +177,46 @@ def unit_scores(k_bits, q_bits, scale: float, bonus=None, acc=None) -> np.ndarra
     return s.astype(np.float32)
 
 
+def foresight_bonus(spans, t: int, n_tokens: int, sigma: float = 1e5, lam: float = 0.35) -> np.ndarray:
+    """PACE Eq. 2: the foresight bonus of every token at step t, fp64 [T].
+
+    spans: (a, b, F) with F the future steps that read tokens [a, b).  A
+    token in a span whose next reference s* = min{s in F : s >= t} exists
+    gets sigma * (1/2 + 1/2 exp(-lambda (s* - t))); a token with no future
+    reference gets 0.  A token in several spans takes the largest bonus (its
+    soonest reference).
+    """
+    bonus = np.zeros(n_tokens, dtype=np.float64)
+    for a, b, F in spans:
+        future = [s for s in F if s >= t]
+        if not future:
+            continue
+        s_next = min(future)
+        beta = sigma * (0.5 + 0.5 * math.exp(-lam * (s_next - t)))
+        lo, hi = max(0, int(a)), min(n_tokens, int(b))
+        if lo < hi:
+            bonus[lo:hi] = np.maximum(bonus[lo:hi], beta)
+    return bonus
+
+
+def cumulative_decode_scores(k_bits, q_steps_bits, scale: float, bonus=None) -> np.ndarray:
+    """H2O cumulative attention score of one unit after several decode steps,
+    plus an optional bonus (PACE Sec. 3.1: the bonus is added to the token's
+    cumulative attention score), fp32 [T].
+
+    q_steps_bits: [n_steps][G][d] the decode queries of the G heads sharing
+    the KV head, one step each; every step attends to all T cached keys
+    (window 1 at the last row) and the weights are summed over heads and steps.
+    """
+    k = bf16_bits_to_f32(k_bits)
+    acc = np.zeros(k.shape[0], dtype=np.float64)
+    for q in np.asarray(q_steps_bits):
+        acc += window_mass(k, bf16_bits_to_f32(q)[:, None, :], scale)
+    if bonus is not None:
+        acc = acc + np.asarray(bonus, dtype=np.float64)
+    return acc.astype(np.float32)
+
+
 def page_max(scores, page_size: int) -> np.ndarray:
     """Page score = maximum token score over each page (max pooling)."""
     s = np.asarray(scores, dtype=np.float32)

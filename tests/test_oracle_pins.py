@@ -576,3 +576,38 @@ def test_reference_store_semantics_on_one_key():
     k5, ref5, pr5, bad = o.reference_rerotate(k2, 40, 7, stale, 100, cos, sin)
     assert bad and pr5 == 40 and np.array_equal(ref5, k2)
     assert np.array_equal(k5, o.rerotate_bits(k2, 40, 7, cos, sin))
+
+
+# --------------------------------------------------------------------------- foresight bonus
+
+def test_foresight_bonus_closed_form_and_floor():
+    """PACE Eq. 2: sigma at the step of the next reference, decaying by
+    exp(-lambda) per step towards the sigma/2 floor; 0 with no future reader."""
+    sig, lam = 1e5, 0.35
+    spans = [(10, 20, [5, 9]), (30, 35, [3]), (40, 50, [7, 100]), (45, 60, [6])]
+    b = o.foresight_bonus(spans, 5, 64, sig, lam)
+    assert np.all(b[10:20] == sig)                                   # s* = t
+    assert np.all(b[30:35] == 0)                                     # last reader ran
+    assert np.allclose(b[40:45], sig * (0.5 + 0.5 * math.exp(-lam * 2)))
+    assert np.allclose(b[45:50], sig * (0.5 + 0.5 * math.exp(-lam * 1)))   # soonest reference wins
+    assert np.allclose(b[50:60], sig * (0.5 + 0.5 * math.exp(-lam * 1)))
+    assert np.all(b[:10] == 0) and np.all(b[60:] == 0)
+    far = o.foresight_bonus([(0, 1, [10 ** 6])], 0, 1, sig, lam)
+    assert abs(far[0] - sig / 2) < 1e-9                              # the sigma/2 = 50K floor
+
+
+def test_bonus_floor_dominates_cumulative_attention():
+    """sigma/2 = 50K exceeds any cumulative attention score below 5e4, so every
+    referenced token outranks every unreferenced one (PACE Sec. 3.1)."""
+    rng = np.random.default_rng(3)
+    T, G, d, steps = 400, 4, 32, 6
+    kb = o.f32_to_bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    qb = o.f32_to_bf16_bits(rng.standard_normal((steps, G, d)).astype(np.float32) * 3)
+    spans = [(17, 40, [9, 30]), (200, 230, [12])]
+    cum = o.cumulative_decode_scores(kb, qb, 1 / math.sqrt(d))
+    assert cum.max() < 5e4 and abs(cum.sum() - steps * G) < 1e-2      # weights sum to 1 per head and step
+    s = o.cumulative_decode_scores(kb, qb, 1 / math.sqrt(d), o.foresight_bonus(spans, 8, T))
+    ref = np.zeros(T, bool)
+    ref[17:40] = True
+    ref[200:230] = True
+    assert s[ref].min() > s[~ref].max()
