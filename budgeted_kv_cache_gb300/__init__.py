@@ -85,6 +85,7 @@ def _load():
             "kvc_decode_workspace_bytes": (SZ, [SH, PO]),
             "kvc_decode_attn": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P, SZ, P]),
             "kvc_decode_attn_noalloc": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P]),
+            "kvc_foresight_bonus": (ctypes.c_int, [I32, I64, P, P, P, P, I32, I32, F32, F32, P, P]),
             "kvc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -244,6 +245,15 @@ def kvc_compact_rerotate_quant_ref(shape, policy: Policy, k_cache, v_cache, pos_
         ctypes.byref(shape), ctypes.byref(cp), _p(k_cache), _p(v_cache), _p(pos_in),
         _p(kept_idx), _p(kept_count), _p(rope_cos), _p(rope_sin), int(rope_max_pos),
         ctypes.byref(rs), ctypes.byref(cpools), _p(unit_status), _stream(stream)))
+
+
+def kvc_foresight_bonus(batch, n_tokens, span_seq, span_a, span_b, span_next, step, sigma, lam,
+                        bonus, stream=None):
+    """PACE Eq. 2 bonus [batch][n_tokens] from spans (device tensors; see include/kvc.h)."""
+    n = 0 if span_seq is None else int(span_seq.numel())
+    _check("kvc_foresight_bonus", _load().kvc_foresight_bonus(
+        int(batch), int(n_tokens), _p(span_seq), _p(span_a), _p(span_b), _p(span_next), n,
+        int(step), float(sigma), float(lam), _p(bonus), _stream(stream)))
 
 
 def kvc_decode_workspace_bytes(shape, policy: Policy) -> int:

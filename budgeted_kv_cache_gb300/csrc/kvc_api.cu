@@ -96,7 +96,7 @@ kvc_status plan_score(const kvc_shape* s, int32_t window, ScorePlan* p) {
   if (window < 1 || window > s->n_tokens) return KVC_ERR_INVALID_ARG;
   const int G = s->n_q_heads / s->n_kv_heads;
   const int64_t R = static_cast<int64_t>(window) * G;
-  if (R % 32 != 0 || R > 256) return KVC_ERR_UNSUPPORTED;
+  if (R < 1 || R > 256) return KVC_ERR_UNSUPPORTED;
   DevInfo info;
   if ((st = check_device(&info)) != KVC_OK) return st;
   p->grid = info.sms;
@@ -257,6 +257,7 @@ kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_
   a.W = window;
   a.G = shape->n_q_heads / shape->n_kv_heads;
   a.R = p.R;
+  a.Rp = (p.R + 15) / 16 * 16;
   a.n_tiles = p.n_tiles;
   a.chunk_tiles = p.chunk_tiles;
   a.items_per_unit = p.S;
@@ -281,6 +282,32 @@ kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(a.counters, 0, p.ws_counters, s) != cudaSuccess) return KVC_ERR_CUDA;
   if (launch_score(a, mk, mq, p.grid, p.smem, s) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+kvc_status kvc_foresight_bonus(int32_t batch, int64_t n_tokens, const int32_t* span_seq,
+                               const int64_t* span_a, const int64_t* span_b,
+                               const int32_t* span_next, int32_t n_spans, int32_t step,
+                               float sigma, float lambda, float* bonus, kvc_stream stream) {
+  if (batch < 1 || n_tokens < 1 || n_spans < 0 || !bonus) return KVC_ERR_INVALID_ARG;
+  if (n_spans > 0 && (!span_seq || !span_a || !span_b || !span_next)) return KVC_ERR_INVALID_ARG;
+  if (!(sigma > 0.f) || !(lambda >= 0.f) || !aligned(bonus, 4)) return KVC_ERR_INVALID_ARG;
+  DevInfo info;
+  kvc_status st;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  BonusArgs a = {};
+  a.batch = batch;
+  a.T = n_tokens;
+  a.n_spans = n_spans;
+  a.step = step;
+  a.sigma = sigma;
+  a.lambda = lambda;
+  a.span_seq = span_seq;
+  a.span_a = span_a;
+  a.span_b = span_b;
+  a.span_next = span_next;
+  a.bonus = bonus;
+  if (launch_bonus(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
   return KVC_OK;
 }
 

@@ -199,7 +199,10 @@ __device__ __forceinline__ void mass_accum_masked(const uint32_t (&r)[N], const 
   }
 }
 
-template <int D>
+// kAnyR: window-row counts that are not a multiple of 32 (pass 2 padded to
+// a multiple of 16 rows); a separate instantiation, so that the 16-column
+// paths do not raise the register pressure of the common one.
+template <int D, bool kAnyR>
 __global__ void __launch_bounds__(kThreads, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
              const ScoreArgs a) {
@@ -301,7 +304,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc1 = mma_idesc_bf16(128, 128);
-      const uint32_t idesc2 = mma_idesc_bf16(128, a.R);
+      const uint32_t idesc2 = mma_idesc_bf16(128, a.Rp);
       // Operand descriptors: one base descriptor per buffer, every k-step and
       // stage reached by adding its byte offset / 16 to the start-address
       // field (shared addresses stay below 2^18, so the field never carries).
@@ -391,7 +394,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     const uint32_t p1_col = rb * 128 + (grp & 1) * 64;
     // pass 2: this group's window rows
     const int p2_r0 = 64 * grp;
-    const int p2_n = max(0, min(64, a.R - p2_r0));   // 64, 32 or 0 (R is a multiple of 32)
+    const int p2_n = max(0, min(64, a.Rp - p2_r0));  // 64, 48, 32, 16 or 0 (Rp: multiple of 16)
 
     uint32_t jt = 0;           // tile counter of both passes (TMEM buffer, phase)
     uint32_t jt2 = 0;          // pass-2 tile counter (reduction slot, phase, finalizer)
@@ -478,17 +481,21 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         // log-sum-exp of every row over the whole unit (stored negated): two
         // adjacent threads per row merge the even and the odd chunks, eight
         // loads in flight each, then combine their two partial results.
-        for (int q = et; q < 2 * a.R; q += kEpiThreads) {
+        // The loop runs over whole warps (the pair exchange is a full-warp
+        // shuffle), with the threads past the last row idle inside it.
+        const int n_pairs = (2 * a.R + 31) & ~31;
+        for (int q = et; q < n_pairs; q += kEpiThreads) {
+          const bool live = q < 2 * a.R;
           const int r = q >> 1, h = q & 1;
           float M = -INFINITY, Ls = 0.f;
           const float2* st_row = a.stats + static_cast<size_t>(u) * S * a.R + r;
-          for (int c0 = h; c0 < S; c0 += 16) {
+          for (int c0 = h; live && c0 < S; c0 += 16) {
             float2 st[8];
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < 8; ++k)
               st[k] = (c0 + 2 * k < S) ? __ldcg(st_row + static_cast<size_t>(c0 + 2 * k) * a.R)
                                        : make_float2(-INFINITY, 0.f);
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < 8; ++k) {
               if (st[k].x == -INFINITY) continue;
               if (st[k].x > M) {
@@ -504,13 +511,16 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
           const float Mx = fmaxf(M, M2);
           const float Lt = (M == -INFINITY ? 0.f : Ls * ex2_approx(M - Mx)) +
                            (M2 == -INFINITY ? 0.f : L2 * ex2_approx(M2 - Mx));
-          if (h == 0) s.lam[r] = -(Mx + __log2f(Lt));
+          if (live && h == 0) s.lam[r] = -(Mx + __log2f(Lt));
         }
+        // padding rows of the pass-2 MMA (R <= r < Rp) contribute nothing
+        for (int r = a.R + et; r < a.Rp; r += kEpiThreads) s.lam[r] = -INFINITY;
         named_bar_sync(1, kEpiThreads);
       } else {
         // the caller's natural-log row statistics, in the log2 domain
         const float* rl = a.row_lse + static_cast<size_t>(u) * a.R;
         for (int r = et; r < a.R; r += kEpiThreads) s.lam[r] = -(__ldg(rl + r) * 1.44269504088896340736f);
+        for (int r = a.R + et; r < a.Rp; r += kEpiThreads) s.lam[r] = -INFINITY;
         named_bar_sync(1, kEpiThreads);
       }
 
@@ -528,7 +538,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       // tile starts; they are consumed a tile later.
       auto finalize = [&](uint32_t jtf, float own, float bon, float old, int64_t jf) {
         const int sl = jtf & 3;
-        if (fail || !mbar_wait(smem_u32(&s.redfull[sl * 4 + qr]), (jtf >> 2) & 1, abort_flag)) {
+        // the give-up decision is made for the whole warp, which then either
+        // leaves or reaches the page-max shuffle together
+        const bool ok = !fail && mbar_wait(smem_u32(&s.redfull[sl * 4 + qr]), (jtf >> 2) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
           fail = true;
           return;
         }
@@ -579,15 +592,29 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
             if (!masked) mass_accum<64>(r, s.lam + p2_r0, cs, acc);
             else mass_accum_masked<64>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
-          } else if (p2_n == 32) {
+          } else if (p2_n == 32 || (kAnyR && p2_n == 48)) {
             uint32_t r[32];
             tmem_ld32_issue(taddr, r);
             tmem_ld_wait(r);
+            uint32_t r16[16];
+            if (kAnyR && p2_n == 48) tmem_ld16(taddr + 32, r16);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
             if (!masked) mass_accum<32>(r, s.lam + p2_r0, cs, acc);
             else mass_accum_masked<32>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
+            if (kAnyR && p2_n == 48) {
+              if (!masked) mass_accum<16>(r16, s.lam + p2_r0 + 32, cs, acc);
+              else mass_accum_masked<16>(r16, s.lam + p2_r0 + 32, cs, p2_r0 + 32, j, Tq, a.W, acc);
+            }
+          } else if (kAnyR && p2_n == 16) {
+            uint32_t r[16];
+            tmem_ld16(taddr, r);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
+            if (!masked) mass_accum<16>(r, s.lam + p2_r0, cs, acc);
+            else mass_accum_masked<16>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
           } else {
             tc_fence_before();
             __syncwarp();
@@ -646,8 +673,10 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages) {
 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q,
                          int grid, size_t smem_bytes, cudaStream_t stream) {
+  const bool any_r = a.R % 32 != 0;
   void (*kern)(const CUtensorMap, const CUtensorMap, const ScoreArgs) =
-      a.d == 64 ? score_kernel<64> : score_kernel<128>;
+      a.d == 64 ? (any_r ? score_kernel<64, true> : score_kernel<64, false>)
+                : (any_r ? score_kernel<128, true> : score_kernel<128, false>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes));
   if (err != cudaSuccess) return err;

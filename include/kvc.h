@@ -113,7 +113,8 @@ typedef struct {
  * k_cache   bf16 [B][L][H_kv][T][d], keys rotated at their positions;
  *           16-byte aligned.
  * q_window  bf16 [B][L][H_q][window][d], rotated; 16-byte aligned.
- * window    W >= 1, W <= T; W * G must be a multiple of 32 and <= 256.
+ * window    W >= 1, W <= T, W * G <= 256 (W = 1 scores one decode query per
+ *           head, the H2O cumulative score with KVC_SCORE_ACCUMULATE).
  * softmax_scale  <= 0 selects 1 / sqrt(d).
  * row_lse   optional fp32 [B][L][H_q][window]: the natural-log log-sum-exp
  *           of each window row's logits q_{h,w} . k_j * scale over the keys
@@ -137,6 +138,29 @@ kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_
                      int32_t page_size, uint32_t flags, float* scores, float* page_scores,
                      int32_t* unit_status, void* workspace, size_t workspace_bytes,
                      kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * kvc_foresight_bonus -- PACE Eq. 2 foresight bonus of every token.
+ *
+ * PACE Sec. 3.1: at step t a token in a span (a, b, F) of the blueprint's
+ * forward-reference table, whose next reference is s* = min{s in F: s >= t},
+ * receives beta = sigma (1/2 + 1/2 exp(-lambda (s* - t))); tokens with no
+ * future reference receive 0 (a token in several spans takes the largest
+ * bonus).  The bonus is what kvc_score adds to each token's score (pass it
+ * as `bonus`), so that with sigma / 2 above every cumulative attention
+ * score each referenced token outranks each unreferenced one.
+ *
+ * span_seq   int32 [n_spans]: the sequence b each span belongs to.
+ * span_a, span_b  int64 [n_spans]: token range [a, b) (clipped to [0, T)).
+ * span_next  int32 [n_spans]: s* computed by the caller; a value < step
+ *            means no future reference (the span contributes nothing).
+ * step       t.  sigma > 0 (PACE: 1e5), lambda >= 0 (PACE: 0.35).
+ * bonus      fp32 [batch][n_tokens], overwritten.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_foresight_bonus(int32_t batch, int64_t n_tokens, const int32_t* span_seq,
+                               const int64_t* span_a, const int64_t* span_b,
+                               const int32_t* span_next, int32_t n_spans, int32_t step,
+                               float sigma, float lambda, float* bonus, kvc_stream stream);
 
 /* ------------------------------------------------------------------------
  * Selection policy.  Exactly one of budget_tokens / budget_bytes is > 0.
