@@ -298,6 +298,32 @@ def run_gpu(args, w, world, rank, local):
         t_dec.append(d0.elapsed_time(d1))
     t_decode = statistics.mean(t_dec)
 
+    # one H2O decode step (PACE Sec. 3.1): window-1 scoring of the decode
+    # query of every head over the whole cache, accumulated into the scores,
+    # with the row statistics computed here (two passes) or supplied by the
+    # caller's attention kernel (one pass); timed separately
+    from budgeted_kv_cache_gb300 import kvc_score, kvc_score_workspace_bytes, SCORE_ACCUMULATE
+    qd = x["q_decode"].reshape(w.batch, w.n_layers, w.n_q_heads, 1, w.head_dim)
+    ws1 = torch.empty(kvc_score_workspace_bytes(p.shape, 1), dtype=torch.uint8, device=dev)
+    lse1 = torch.full((w.n_units, w.group), 8.0, device=dev)
+    t_h2o = {}
+    for name, lse_arg in (("h2o_step_two_pass", None), ("h2o_step_caller_lse", lse1)):
+        step1 = lambda: kvc_score(p.shape, x["k_cache"], qd, 1, 0.0, None, 1, SCORE_ACCUMULATE,
+                                  p.scores, None, p.score_status, ws1, stream=stream, row_lse=lse_arg)
+        for _ in range(3):
+            step1()
+        t_s = []
+        for _ in range(10):
+            flush.fill_(1)
+            d0, d1 = ev(), ev()
+            d0.record(stream)
+            step1()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            t_s.append(d0.elapsed_time(d1))
+        t_h2o[name] = statistics.mean(t_s)
+    del ws1, lse1
+
     # compaction through the reference store (PACE Sec. 3.2), timed separately:
     # every cached key has a reference valid at its current position (the
     # stored key itself), so each kept key is checked and re-derived from it
@@ -403,7 +429,7 @@ def run_gpu(args, w, world, rank, local):
                      "tc_tflops_algorithmic": flops / (score_ms * 1e-3) / 1e12},
         "stages_ms": {"score": score_ms, "select": statistics.mean(t_select),
                       "compact": statistics.mean(t_compact), "decode": t_decode,
-                      "compact_reference_store": t_cref},
+                      "compact_reference_store": t_cref, **t_h2o},
         "pass_roofline": {"t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step,
                           "algorithmic_bytes": ab["total"], "algorithmic_flops": flops},
         "cpu_baseline": cpu, "e2e": e2e,
