@@ -217,6 +217,35 @@ def cumulative_decode_scores(k_bits, q_steps_bits, scale: float, bonus=None) -> 
     return acc.astype(np.float32)
 
 
+def pool_scores(scores, kernel: int, mode: str) -> np.ndarray:
+    """SnapKV's 1-D pooling of token scores before selection (the pooling
+    and kernel options of the SnapKV baseline in PASK's baseline table):
+    for each token the average or maximum over the `kernel` tokens centred on
+    it, stride 1.  Positions outside [0, T) count as 0 in the average
+    (divided by `kernel`) and are ignored by the maximum.  fp32 in, fp32 out
+    (the average summed in fp64).
+    """
+    s = np.asarray(scores, dtype=np.float32)
+    T = s.size
+    h = kernel // 2
+    out = np.empty(T, dtype=np.float32)
+    for j in range(T):
+        lo, hi = max(0, j - h), min(T, j + h + 1)
+        if mode == "avg":
+            out[j] = np.float32(s[lo:hi].astype(np.float64).sum() / kernel)
+        else:
+            out[j] = s[lo:hi].max()
+    return out
+
+
+def shared_scores(unit_scores_of_sequence) -> np.ndarray:
+    """CommitKV Eq. 4 applies one index set to the keys, values and positions
+    of every layer and head: the per-token score of a sequence is the sum of
+    its units' scores, fp32 [T] (summed in fp64)."""
+    a = np.asarray(unit_scores_of_sequence, dtype=np.float32).astype(np.float64)
+    return a.sum(axis=0).astype(np.float32)
+
+
 def page_max(scores, page_size: int) -> np.ndarray:
     """Page score = maximum token score over each page (max pooling)."""
     s = np.asarray(scores, dtype=np.float32)

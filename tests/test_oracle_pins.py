@@ -611,3 +611,26 @@ def test_bonus_floor_dominates_cumulative_attention():
     ref[17:40] = True
     ref[200:230] = True
     assert s[ref].min() > s[~ref].max()
+
+
+# --------------------------------------------------------------------------- selection variants
+
+@pytest.mark.parametrize("kernel", [3, 5, 7])
+def test_pool_scores_matches_library_pooling(kernel):
+    """Against torch's avg_pool1d (zero padding counted) and max_pool1d."""
+    rng = np.random.default_rng(kernel)
+    s = rng.standard_normal(301).astype(np.float32)
+    t = torch.from_numpy(s).view(1, 1, -1)
+    avg = torch.nn.functional.avg_pool1d(t.double(), kernel, 1, kernel // 2,
+                                         count_include_pad=True).view(-1).numpy()
+    mx = torch.nn.functional.max_pool1d(t, kernel, 1, kernel // 2).view(-1).numpy()
+    np.testing.assert_allclose(o.pool_scores(s, kernel, "avg"), avg.astype(np.float32), rtol=1e-6,
+                               atol=1e-7)
+    assert np.array_equal(o.pool_scores(s, kernel, "max"), mx)
+
+
+def test_shared_scores_is_the_unit_sum():
+    rng = np.random.default_rng(4)
+    u = rng.random((6, 50)).astype(np.float32)
+    brute = np.array([sum(float(u[k, j]) for k in range(6)) for j in range(50)], np.float32)
+    assert np.allclose(o.shared_scores(u), brute, rtol=1e-7)
