@@ -86,6 +86,9 @@ def _load():
             "kvc_decode_attn": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P, SZ, P]),
             "kvc_decode_attn_noalloc": (ctypes.c_int, [SH, PO, P, PL, P, F32, P, P]),
             "kvc_foresight_bonus": (ctypes.c_int, [I32, I64, P, P, P, P, I32, I32, F32, F32, P, P]),
+            "kvc_pool_scores": (ctypes.c_int, [I64, I64, P, P, I32, I32, P]),
+            "kvc_shared_scores": (ctypes.c_int, [SH, P, P, P]),
+            "kvc_broadcast_kept": (ctypes.c_int, [SH, PO, P, P, P, P, P]),
             "kvc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -254,6 +257,31 @@ def kvc_foresight_bonus(batch, n_tokens, span_seq, span_a, span_b, span_next, st
     _check("kvc_foresight_bonus", _load().kvc_foresight_bonus(
         int(batch), int(n_tokens), _p(span_seq), _p(span_a), _p(span_b), _p(span_next), n,
         int(step), float(sigma), float(lam), _p(bonus), _stream(stream)))
+
+
+SCORE_POOL_AVG, SCORE_POOL_MAX = 0, 1
+
+
+def kvc_pool_scores(scores, pooled, kernel, mode, stream=None):
+    """SnapKV pooling of fp32 [rows][T] scores into `pooled` (see include/kvc.h)."""
+    _check("kvc_pool_scores", _load().kvc_pool_scores(
+        int(scores.shape[0]), int(scores.shape[1]), _p(scores), _p(pooled), int(kernel), int(mode),
+        _stream(stream)))
+
+
+def kvc_shared_scores(shape, scores, shared, stream=None):
+    """CommitKV Eq. 4: per-sequence sum of the units' scores, fp32 [B][T]."""
+    _check("kvc_shared_scores", _load().kvc_shared_scores(ctypes.byref(shape), _p(scores),
+                                                          _p(shared), _stream(stream)))
+
+
+def kvc_broadcast_kept(shape, policy: Policy, kept_idx_seq, kept_count_seq, kept_idx, kept_count,
+                       stream=None):
+    """Copy per-sequence kept lists to every unit of the sequence."""
+    cp = policy.c()
+    _check("kvc_broadcast_kept", _load().kvc_broadcast_kept(
+        ctypes.byref(shape), ctypes.byref(cp), _p(kept_idx_seq), _p(kept_count_seq), _p(kept_idx),
+        _p(kept_count), _stream(stream)))
 
 
 def kvc_decode_workspace_bytes(shape, policy: Policy) -> int:

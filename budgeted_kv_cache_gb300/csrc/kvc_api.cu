@@ -311,6 +311,51 @@ kvc_status kvc_foresight_bonus(int32_t batch, int64_t n_tokens, const int32_t* s
   return KVC_OK;
 }
 
+kvc_status kvc_pool_scores(int64_t n_rows, int64_t n_tokens, const float* scores, float* pooled,
+                           int32_t kernel, int32_t mode, kvc_stream stream) {
+  if (n_rows < 1 || n_rows > 65535 || n_tokens < 1 || !scores || !pooled || scores == pooled)
+    return KVC_ERR_INVALID_ARG;
+  if (!(kernel == 1 || kernel == 3 || kernel == 5 || kernel == 7)) return KVC_ERR_INVALID_ARG;
+  if (mode != KVC_SCORE_POOL_AVG && mode != KVC_SCORE_POOL_MAX) return KVC_ERR_INVALID_ARG;
+  DevInfo info;
+  kvc_status st;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  if (launch_pool(scores, pooled, n_rows, n_tokens, kernel, mode, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+kvc_status kvc_shared_scores(const kvc_shape* shape, const float* scores, float* shared,
+                             kvc_stream stream) {
+  kvc_status st = check_shape(shape);
+  if (st != KVC_OK) return st;
+  if (!scores || !shared) return KVC_ERR_INVALID_ARG;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  if (launch_shared_sum(scores, shared, shape->batch, shape->n_layers * shape->n_kv_heads,
+                        shape->n_tokens, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+kvc_status kvc_broadcast_kept(const kvc_shape* shape, const kvc_policy* policy,
+                              const int32_t* kept_idx_seq, const int32_t* kept_count_seq,
+                              int32_t* kept_idx, int32_t* kept_count, kvc_stream stream) {
+  kvc_status st = check_shape(shape);
+  if (st != KVC_OK) return st;
+  if (!policy || policy->capacity < 1 || !kept_idx_seq || !kept_count_seq || !kept_idx || !kept_count)
+    return KVC_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(KVC_N_POOLS) * n_units(shape) > 65535) return KVC_ERR_UNSUPPORTED;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  if (launch_broadcast(kept_idx_seq, kept_count_seq, kept_idx, kept_count, shape->batch,
+                       shape->n_layers * shape->n_kv_heads, policy->capacity,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
 size_t kvc_select_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy) {
   (void)shape;
   (void)policy;

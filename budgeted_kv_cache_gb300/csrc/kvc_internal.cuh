@@ -117,6 +117,12 @@ struct BonusArgs {
 
 // host launchers (each returns a cudaError_t from the launch)
 cudaError_t launch_bonus(const BonusArgs& a, cudaStream_t stream);
+cudaError_t launch_pool(const float* in, float* out, int64_t rows, int64_t n, int kernel, int mode,
+                        cudaStream_t stream);
+cudaError_t launch_shared_sum(const float* scores, float* shared, int B, int units_per_seq, int64_t n,
+                              cudaStream_t stream);
+cudaError_t launch_broadcast(const int32_t* kept_seq, const int32_t* count_seq, int32_t* kept,
+                             int32_t* count, int B, int units_per_seq, int cap, cudaStream_t stream);
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q,
                          int grid, size_t smem_bytes, cudaStream_t stream);
 size_t score_smem_bytes(int d, int q_rows, int n_stages);

@@ -228,6 +228,38 @@ kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const fl
                       int64_t* floor_excess, void* workspace, size_t workspace_bytes,
                       kvc_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Selection variants on the score buffer.
+ *
+ * kvc_pool_scores -- SnapKV's pooling of token scores before selection (the
+ * pooling and kernel options of the SnapKV baseline in PASK's baseline
+ * table): pooled[r][j] = average (KVC_SCORE_POOL_AVG) or maximum
+ * (KVC_SCORE_POOL_MAX) of scores[r][j - kernel/2 .. j + kernel/2]; outside
+ * [0, n_tokens) a score counts as 0 in the average (always divided by
+ * `kernel`) and is ignored by the maximum.  kernel is 1, 3, 5 or 7.
+ * scores, pooled: fp32 [n_rows][n_tokens], distinct buffers; n_rows <= 65535.
+ *
+ * kvc_shared_scores -- CommitKV Eq. 4 applies one index set I_j to the keys,
+ * values and positions of every layer and head: shared[b][j] = sum over the
+ * sequence's units (l, g) of scores[(b, l, g)][j], summed in unit order.
+ * scores fp32 [U][T] (U = B L H_kv); shared fp32 [B][T].
+ *
+ * kvc_broadcast_kept -- copies the kept lists selected on the shared scores
+ * (kvc_select called with a shape of B units: n_layers = n_kv_heads = 1) to
+ * every unit of the sequence, ready for kvc_compact_rerotate_quant.
+ * kept_idx_seq int32 [KVC_N_POOLS][B][capacity], kept_count_seq [KVC_N_POOLS][B];
+ * kept_idx int32 [KVC_N_POOLS][U][capacity], kept_count [KVC_N_POOLS][U].
+ * ---------------------------------------------------------------------- */
+enum { KVC_SCORE_POOL_AVG = 0, KVC_SCORE_POOL_MAX = 1 };
+
+kvc_status kvc_pool_scores(int64_t n_rows, int64_t n_tokens, const float* scores, float* pooled,
+                           int32_t kernel, int32_t mode, kvc_stream stream);
+kvc_status kvc_shared_scores(const kvc_shape* shape, const float* scores, float* shared,
+                             kvc_stream stream);
+kvc_status kvc_broadcast_kept(const kvc_shape* shape, const kvc_policy* policy,
+                              const int32_t* kept_idx_seq, const int32_t* kept_count_seq,
+                              int32_t* kept_idx, int32_t* kept_count, kvc_stream stream);
+
 /* Compacted pools.  A pool's pointers may be NULL when no call will store a
  * row in it (token and page mode use only the bf16 pool). */
 typedef struct {
