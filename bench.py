@@ -324,6 +324,45 @@ def run_gpu(args, w, world, rank, local):
         t_h2o[name] = statistics.mean(t_s)
     del ws1, lse1
 
+    # selection variants, timed separately: SnapKV pooling (kernel 7, max) of
+    # the score buffer, and CommitKV Eq. 4's shared index set (per-sequence
+    # score sum, one selection per sequence, kept lists copied to the units)
+    from budgeted_kv_cache_gb300 import (kvc_pool_scores, kvc_shared_scores, kvc_select,
+                                         kvc_broadcast_kept, make_shape, SCORE_POOL_MAX)
+    pooled = torch.empty_like(p.scores)
+    shared = torch.empty((w.batch, w.n_tokens), device=dev)
+    seq_shape = make_shape(w.batch, 1, 1, 1, w.head_dim, w.n_tokens)
+    kept_s = torch.empty((3, w.batch, p.policy.capacity), dtype=torch.int32, device=dev)
+    cnt_s = torch.empty((3, w.batch), dtype=torch.int32, device=dev)
+    st_s = torch.empty(w.batch, dtype=torch.int32, device=dev)
+
+    def shared_set():
+        kvc_shared_scores(p.shape, p.scores, shared, stream=stream)
+        kvc_select(seq_shape, p.policy, shared, kept_s, cnt_s, st_s, stream=stream)
+        kvc_broadcast_kept(p.shape, p.policy, kept_s, cnt_s, p.kept_idx, p.kept_count, stream=stream)
+
+    variants = {"pool_scores_max7": lambda: kvc_pool_scores(p.scores, pooled, 7, SCORE_POOL_MAX,
+                                                            stream=stream)}
+    if not w.byte_mode and w.page_size == 1:
+        variants["shared_index_set"] = shared_set
+    t_var = {}
+    for name, fn in variants.items():
+        for _ in range(3):
+            fn()
+        t_v = []
+        for _ in range(10):
+            flush.fill_(1)
+            d0, d1 = ev(), ev()
+            d0.record(stream)
+            fn()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            t_v.append(d0.elapsed_time(d1))
+        t_var[name] = statistics.mean(t_v)
+    del pooled, shared
+    p.select(stream=stream)             # restore the per-unit kept lists
+    torch.cuda.synchronize()
+
     # compaction through the reference store (PACE Sec. 3.2), timed separately:
     # every cached key has a reference valid at its current position (the
     # stored key itself), so each kept key is checked and re-derived from it
@@ -429,7 +468,7 @@ def run_gpu(args, w, world, rank, local):
                      "tc_tflops_algorithmic": flops / (score_ms * 1e-3) / 1e12},
         "stages_ms": {"score": score_ms, "select": statistics.mean(t_select),
                       "compact": statistics.mean(t_compact), "decode": t_decode,
-                      "compact_reference_store": t_cref, **t_h2o},
+                      "compact_reference_store": t_cref, **t_h2o, **t_var},
         "pass_roofline": {"t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step,
                           "algorithmic_bytes": ab["total"], "algorithmic_flops": flops},
         "cpu_baseline": cpu, "e2e": e2e,
