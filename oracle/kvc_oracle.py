@@ -411,19 +411,28 @@ def rope_rotate(x, pos, head_dim: int, theta: float) -> np.ndarray:
     return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
 
 
-def rerotate_bits(k_bits, p: int, p_new: int, cos_tab, sin_tab) -> np.ndarray:
+def rerotate_bits(k_bits, p: int, p_new: int, cos_tab, sin_tab, layout: str = "split",
+                  rotary_dim: int = 0) -> np.ndarray:
     """Re-rotate one stored bf16 key from position p to p_new (fp32 spec).
 
     cos/sin of (p_new - p) theta_i come from the engine's own tables through
     the angle-difference identities and are normalised to unit length
     (PACE Sec. 3.2); every product, sum, root and quotient is rounded to fp32
-    once, in this order, and the rotated halves are rounded to bf16.
+    once, in this order, and the rotated elements are rounded to bf16.
     If p_new == p the stored bits are returned unchanged.
+
+    Rotary layouts (PACE Sec. 3.2: the same rotation applied to the rotated
+    dimensions only): the first `rotary_dim` elements rotate (0 = all), as
+    split halves (element i pairs with i + rotary_dim/2, layout "split") or
+    as adjacent pairs (2i with 2i + 1, layout "interleaved"); the tables are
+    [max_pos][rotary_dim / 2]; elements past rotary_dim are copied.
     """
     k_bits = np.asarray(k_bits, dtype=np.uint16)
     if p_new == p:
         return k_bits.copy()
     f = np.float32
+    d = k_bits.shape[-1]
+    rd = rotary_dim or d
     c0 = np.asarray(cos_tab[p], dtype=f)
     s0 = np.asarray(sin_tab[p], dtype=f)
     c1 = np.asarray(cos_tab[p_new], dtype=f)
@@ -433,12 +442,19 @@ def rerotate_bits(k_bits, p: int, p_new: int, cos_tab, sin_tab) -> np.ndarray:
     n = np.sqrt((C * C) + (S * S))
     C = C / n
     S = S / n
-    h = k_bits.shape[-1] // 2
-    x = bf16_bits_to_f32(k_bits[..., :h])
-    y = bf16_bits_to_f32(k_bits[..., h:])
+    h = rd // 2
+    if layout == "split":
+        xi, yi = np.arange(h), h + np.arange(h)
+    else:
+        xi, yi = 2 * np.arange(h), 2 * np.arange(h) + 1
+    x = bf16_bits_to_f32(k_bits[..., xi])
+    y = bf16_bits_to_f32(k_bits[..., yi])
     xr = (x * C) - (y * S)
     yr = (y * C) + (x * S)
-    return f32_to_bf16_bits(np.concatenate([xr, yr], axis=-1))
+    out = k_bits.copy()
+    out[..., xi] = f32_to_bf16_bits(xr)
+    out[..., yi] = f32_to_bf16_bits(yr)
+    return out
 
 
 def reference_rerotate(k_bits, p: int, p_new: int, ref_bits, p_ref: int, cos_tab, sin_tab):
@@ -676,6 +692,8 @@ class PassParams:
     quant_mode: int = QUANT_G32_BF16
     n_layer_groups: int = 3
     softmax_scale: float = 0.0
+    rope_layout: str = "split"      # "split" halves or "interleaved" pairs
+    rotary_dim: int = 0             # rotated leading dimensions (0 = all)
 
 
 def select_unit(scores, page_scores, n_tokens, head_dim, params: PassParams,
@@ -717,7 +735,8 @@ def compact_unit(k_bits, v_bits, pos_in, actions, params: PassParams, cos_tab, s
         kr = np.zeros((idx.size, d), dtype=np.uint16)
         if ref_pos is None:
             for n, (i, p, p2) in enumerate(zip(idx, pool.orig_pos, pool.pos)):
-                kr[n] = rerotate_bits(k_bits[i], int(p), int(p2), cos_tab, sin_tab)
+                kr[n] = rerotate_bits(k_bits[i], int(p), int(p2), cos_tab, sin_tab,
+                                      params.rope_layout, params.rotary_dim)
         else:
             pool.k_ref = np.zeros((idx.size, d), dtype=np.uint16)
             pool.p_ref = np.full(idx.size, -1, dtype=np.int64)

@@ -634,3 +634,53 @@ def test_shared_scores_is_the_unit_sum():
     u = rng.random((6, 50)).astype(np.float32)
     brute = np.array([sum(float(u[k, j]) for k in range(6)) for j in range(50)], np.float32)
     assert np.allclose(o.shared_scores(u), brute, rtol=1e-7)
+
+
+# --------------------------------------------------------------------------- rotary layouts
+
+def test_interleaved_rerotation_is_split_half_on_permuted_dims():
+    """Adjacent pairs (2i, 2i+1) rotate exactly as split halves once the even
+    dimensions are moved to the front: the same pairs, the same arithmetic."""
+    d = 64
+    cos, sin = wl.rope_tables(512, d, 1e4)
+    cos, sin = cos.numpy(), sin.numpy()
+    rng = np.random.default_rng(12)
+    perm = np.concatenate([np.arange(0, d, 2), np.arange(1, d, 2)])
+    for _ in range(20):
+        k = o.f32_to_bf16_bits(rng.standard_normal(d).astype(np.float32))
+        p, p2 = (int(v) for v in rng.integers(0, 512, 2))
+        inter = o.rerotate_bits(k, p, p2, cos, sin, "interleaved")
+        split = o.rerotate_bits(k[perm], p, p2, cos, sin, "split")
+        assert np.array_equal(inter[perm], split)
+
+
+@pytest.mark.parametrize("layout", ["split", "interleaved"])
+def test_partial_rotary_rotates_only_leading_dims(layout):
+    """rotary_dim < d: the leading dims rotate as a key of rotary_dim would,
+    the rest are copied; and the result is the fp64 rotation of the
+    pre-rotation key at p' to bf16 accuracy (PACE Prop. 1)."""
+    d, rd = 128, 64
+    cos, sin = wl.rope_tables(1024, rd, 1e6)
+    cos, sin = cos.numpy(), sin.numpy()
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal(d)
+    h = rd // 2
+    xi = np.arange(h) if layout == "split" else 2 * np.arange(h)
+    yi = xi + h if layout == "split" else xi + 1
+
+    def rot(vec, pos):
+        c, s_ = cos[pos].astype(np.float64), sin[pos].astype(np.float64)
+        out = vec.copy()
+        out[xi] = vec[xi] * c - vec[yi] * s_
+        out[yi] = vec[yi] * c + vec[xi] * s_
+        return out
+
+    p, p2 = 700, 13
+    k = o.f32_to_bf16_bits(rot(x, p).astype(np.float32))
+    r = o.rerotate_bits(k, p, p2, cos, sin, layout, rd)
+    assert np.array_equal(r[rd:], k[rd:])
+    sub = o.rerotate_bits(k[:rd], p, p2, cos, sin, layout)
+    assert np.array_equal(r[:rd], sub)
+    exact = rot(x, p2)
+    err = np.abs(o.bf16_bits_to_f32(r).astype(np.float64) - exact)
+    assert np.all(err <= 2 ** -7 * np.abs(exact) + 1e-3)
