@@ -47,7 +47,8 @@ class kvc_policy(ctypes.Structure):
                 ("capacity", ctypes.c_int32), ("quant_mode", ctypes.c_int32),
                 ("n_tags", ctypes.c_int32), ("n_layer_groups", ctypes.c_int32),
                 ("flags", ctypes.c_void_p), ("tags", ctypes.c_void_p),
-                ("action_table", ctypes.c_void_p)]
+                ("action_table", ctypes.c_void_p), ("rope_layout", ctypes.c_int32),
+                ("rotary_dim", ctypes.c_int32)]
 
 
 class kvc_pools(ctypes.Structure):
@@ -145,12 +146,14 @@ class Policy:
     flags: Optional[torch.Tensor] = None
     tags: Optional[torch.Tensor] = None
     action_table: Optional[torch.Tensor] = None
+    rope_layout: int = 0          # ROPE_SPLIT_HALF or ROPE_INTERLEAVED
+    rotary_dim: int = 0           # 0 = head_dim
 
     def c(self) -> kvc_policy:
         return kvc_policy(self.budget_tokens, self.budget_bytes, self.n_sink, self.n_recent,
                           self.page_size, int(bool(self.renumber)), self.capacity, self.quant_mode,
                           self.n_tags, self.n_layer_groups, _p(self.flags), _p(self.tags),
-                          _p(self.action_table))
+                          _p(self.action_table), int(self.rope_layout), int(self.rotary_dim))
 
     @property
     def byte_mode(self) -> bool:
@@ -260,6 +263,7 @@ def kvc_foresight_bonus(batch, n_tokens, span_seq, span_a, span_b, span_next, st
 
 
 SCORE_POOL_AVG, SCORE_POOL_MAX = 0, 1
+ROPE_SPLIT_HALF, ROPE_INTERLEAVED = 0, 1
 
 
 def kvc_pool_scores(scores, pooled, kernel, mode, stream=None):

@@ -43,6 +43,110 @@ __device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
   }
 }
 
+// Where this lane's 8 elements sit in the rotary pairs.  Split halves of
+// the first rd elements (i with i + rd/2): lanes hl < rd/16 hold x, lanes
+// rd/16 <= hl < rd/8 hold the partner y, and the two lanes of a pair
+// compute four of their eight (C, S) each (table columns j0 .. j0 + 3).
+// Interleaved pairs (2i, 2i + 1) lie inside one lane, which forms its own
+// four (C, S).  Lanes at or past rd copy their elements.
+struct LaneRot {
+  bool active;
+  bool inter;
+  bool first_half;
+  int src;         // warp lane holding the partner elements (split layout)
+  int j0;          // first table column of this lane's four (C, S)
+  int half;        // table width: rd / 2
+};
+
+__device__ __forceinline__ LaneRot lane_rot(int layout, int rd, int lane, int hl, int lpr) {
+  LaneRot r;
+  r.half = rd / 2;
+  r.inter = layout == KVC_ROPE_INTERLEAVED;
+  r.active = 8 * hl < rd;
+  if (r.inter) {
+    r.first_half = true;
+    r.src = lane;
+    r.j0 = 4 * hl;
+  } else {
+    const int q = rd / 16;                        // lanes per half
+    r.first_half = hl < q;
+    const int phl = !r.active ? hl : (r.first_half ? hl + q : hl - q);
+    r.src = lane - hl + phl;
+    r.j0 = (r.first_half ? hl : hl - q) * 8 + (r.first_half ? 0 : 4);
+  }
+  (void)lpr;
+  return r;
+}
+
+// Normalised (C, S) of the angle difference for four pairs (see the file
+// comment), from the cos / sin of the old (tab[0], tab[1]) and new
+// (tab[2], tab[3]) position.
+__device__ __forceinline__ void rot_cs4(const float4 (&tab)[4], float (&C4)[4], float (&S4)[4]) {
+  const float cc0[4] = {tab[0].x, tab[0].y, tab[0].z, tab[0].w};
+  const float ss0[4] = {tab[1].x, tab[1].y, tab[1].z, tab[1].w};
+  const float cc1[4] = {tab[2].x, tab[2].y, tab[2].z, tab[2].w};
+  const float ss1[4] = {tab[3].x, tab[3].y, tab[3].z, tab[3].w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float C = __fadd_rn(__fmul_rn(cc1[k], cc0[k]), __fmul_rn(ss1[k], ss0[k]));
+    float S = __fsub_rn(__fmul_rn(ss1[k], cc0[k]), __fmul_rn(cc1[k], ss0[k]));
+    const float nrm = __fsqrt_rn(__fadd_rn(__fmul_rn(C, C), __fmul_rn(S, S)));
+    C4[k] = __fdiv_rn(C, nrm);
+    S4[k] = __fdiv_rn(S, nrm);
+  }
+}
+
+// General rotary layouts (interleaved pairs, or only the first rd elements
+// rotated); same arithmetic and rounding as rerotate_lane.  Whole warps.
+__device__ __forceinline__ void rerotate_lane_general(const LaneRot& lr, bool rotate,
+                                                      const float4 (&tab)[4], float (&x)[8],
+                                                      uint4& w) {
+  const bool rot = rotate && lr.active;
+  uint32_t rb[8];
+  if (lr.inter) {
+    if (!rot) return;
+    float C4[4], S4[4];
+    rot_cs4(tab, C4, S4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float xr = __fsub_rn(__fmul_rn(x[2 * k], C4[k]), __fmul_rn(x[2 * k + 1], S4[k]));
+      const float yr = __fadd_rn(__fmul_rn(x[2 * k + 1], C4[k]), __fmul_rn(x[2 * k], S4[k]));
+      rb[2 * k] = float_to_bf16_bits(xr);
+      rb[2 * k + 1] = float_to_bf16_bits(yr);
+    }
+  } else {
+    uint4 ow;
+    ow.x = __shfl_sync(kFull, w.x, lr.src);
+    ow.y = __shfl_sync(kFull, w.y, lr.src);
+    ow.z = __shfl_sync(kFull, w.z, lr.src);
+    ow.w = __shfl_sync(kFull, w.w, lr.src);
+    float y[8];
+    unpack8(ow, y);
+    float C4[4] = {1.f, 1.f, 1.f, 1.f}, S4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (rot) rot_cs4(tab, C4, S4);
+    float Cx[4], Sx[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      Cx[k] = __shfl_sync(kFull, C4[k], lr.src);
+      Sx[k] = __shfl_sync(kFull, S4[k], lr.src);
+    }
+    if (!rot) return;
+    const bool fh = lr.first_half;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float Ck = k < 4 ? (fh ? C4[k] : Cx[k]) : (fh ? Cx[k - 4] : C4[k - 4]);
+      const float Sk = k < 4 ? (fh ? S4[k] : Sx[k]) : (fh ? Sx[k - 4] : S4[k - 4]);
+      const float r = fh ? __fsub_rn(__fmul_rn(x[k], Ck), __fmul_rn(y[k], Sk))
+                         : __fadd_rn(__fmul_rn(x[k], Ck), __fmul_rn(y[k], Sk));
+      rb[k] = float_to_bf16_bits(r);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) x[k] = bf16_bits_to_float(static_cast<uint16_t>(rb[k]));
+  w = make_uint4(rb[0] | (rb[1] << 16), rb[2] | (rb[3] << 16), rb[4] | (rb[5] << 16),
+                 rb[6] | (rb[7] << 16));
+}
+
 // Re-rotation of one key row's 8 elements held by this lane (see the file
 // comment): x holds them, w their packed bf16 bits; on return both hold the
 // rotated row.  Called by whole warps (the shuffles need every lane).
@@ -97,14 +201,15 @@ __device__ __forceinline__ void rerotate_lane(int lpr, int hl, bool rotate, cons
 
 // Re-rotation of this lane's part of one key row from position `from` to
 // `to` (rows whose `rot` is false are left as they are); whole warps call it.
-__device__ __forceinline__ void rotate_row(const CompactArgs& a, int lpr, int hl, bool rot,
-                                           int32_t from, int32_t to, uint4& w, float (&x)[8]) {
+template <bool kGeneral>
+__device__ __forceinline__ void rotate_row(const CompactArgs& a, const LaneRot& lr, int lpr, int hl,
+                                           bool rot, int32_t from, int32_t to, uint4& w,
+                                           float (&x)[8]) {
   if (!__any_sync(kFull, rot)) return;
-  const int px = lpr / 2;
-  const int j0 = (hl % px) * 8 + (hl < px ? 0 : 4);
-  const int half = a.d / 2;
+  const int j0 = lr.j0;
+  const int half = lr.half;
   float4 tab[4];
-  if (rot) {
+  if (rot && lr.active) {
     tab[0] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(from) * half + j0));
     tab[1] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(from) * half + j0));
     tab[2] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(to) * half + j0));
@@ -113,7 +218,8 @@ __device__ __forceinline__ void rotate_row(const CompactArgs& a, int lpr, int hl
 #pragma unroll
     for (int k = 0; k < 4; ++k) tab[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  rerotate_lane(lpr, hl, rot, tab, x, w);
+  if (kGeneral) rerotate_lane_general(lr, rot, tab, x, w);
+  else rerotate_lane(lpr, hl, rot, tab, x, w);
 }
 
 // Quantise this lane's 8 elements of one row and store codes and scales.
@@ -184,7 +290,7 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
 // not ordered behind a store.
 constexpr int kRows = 2;
 
-template <bool kStore>
+template <bool kStore, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs a) {
   const int d = a.d;
   const int lpr = d / 8;                        // lanes per row (16 B = 8 bf16 per lane)
@@ -279,13 +385,14 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   }
   // rotation tables: cos / sin of the old and new position for the four
   // (C, S) pairs this lane forms
-  const int px = lpr / 2;
-  const int j0 = (hl % px) * 8 + (hl < px ? 0 : 4);
-  const int half = d / 2;
+  const LaneRot lr = kGeneral ? lane_rot(a.rope_layout, a.rotary_dim, lane, hl, lpr)
+                              : lane_rot(KVC_ROPE_SPLIT_HALF, d, lane, hl, lpr);
+  const int j0 = lr.j0;
+  const int half = lr.half;
   float4 tab[kRows][4];
 #pragma unroll
   for (int n = 0; n < kRows; ++n) {
-    if (rotate[n]) {
+    if (rotate[n] && lr.active) {
       tab[n][0] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p[n]) * half + j0));
       tab[n][1] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p[n]) * half + j0));
       tab[n][2] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p2[n]) * half + j0));
@@ -300,7 +407,10 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
     float x[8];
     unpack8(w[n], x);
     // the branch is warp-uniform: key warps only, and only if a row rotates
-    if (!is_v && __any_sync(kFull, rotate[n])) rerotate_lane(lpr, hl, rotate[n], tab[n], x, w[n]);
+    if (!is_v && __any_sync(kFull, rotate[n])) {
+      if (kGeneral) rerotate_lane_general(lr, rotate[n], tab[n], x, w[n]);
+      else rerotate_lane(lpr, hl, rotate[n], tab[n], x, w[n]);
+    }
     const int64_t i = i_base + n * rows_per_warp;
     const int64_t row = static_cast<int64_t>(u) * cap + i;
     if (use_store) {
@@ -311,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
       uint4 chk = wr[n];
       float xc[8];
       unpack8(chk, xc);
-      rotate_row(a, lpr, hl, chg[n] && has_ref && pr[n] != p[n], pr[n], p[n], chk, xc);
+      rotate_row<kGeneral>(a, lr, lpr, hl, chg[n] && has_ref && pr[n] != p[n], pr[n], p[n], chk, xc);
       const bool lane_ok = chk.x == w[n].x && chk.y == w[n].y && chk.z == w[n].z && chk.w == w[n].w;
       const unsigned gmask = (lpr == 32 ? kFull : ((1u << lpr) - 1u)) << (sub * lpr);
       const bool ok = (__ballot_sync(kFull, lane_ok) & gmask) == gmask;
@@ -321,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
       const int32_t from = use_ref ? pr[n] : p[n];
       float xs[8];
       unpack8(nw, xs);
-      rotate_row(a, lpr, hl, chg[n] && from != p2[n], from, p2[n], nw, xs);
+      rotate_row<kGeneral>(a, lr, lpr, hl, chg[n] && from != p2[n], from, p2[n], nw, xs);
       uint4 rw = has_ref ? wr[n] : make_uint4(0, 0, 0, 0);
       int32_t rp = has_ref ? pr[n] : -1;
       if (chg[n] && !use_ref) {            // first renumber, or a failed copy: the stored key
@@ -363,8 +473,14 @@ cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
   const int n_pools = a.pool_hi - a.pool_lo;
   if (bx == 0 || n_pools <= 0) return cudaSuccess;
   dim3 grid(bx, a.U, 2 * n_pools);            // z: (pool, K or V)
-  if (a.ref.ref_pos != nullptr) compact_kernel<true><<<grid, kThreads, 0, stream>>>(a);
-  else compact_kernel<false><<<grid, kThreads, 0, stream>>>(a);
+  const bool general = a.rope_layout != KVC_ROPE_SPLIT_HALF || a.rotary_dim != a.d;
+  if (a.ref.ref_pos != nullptr) {
+    if (general) compact_kernel<true, true><<<grid, kThreads, 0, stream>>>(a);
+    else compact_kernel<true, false><<<grid, kThreads, 0, stream>>>(a);
+  } else {
+    if (general) compact_kernel<false, true><<<grid, kThreads, 0, stream>>>(a);
+    else compact_kernel<false, false><<<grid, kThreads, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

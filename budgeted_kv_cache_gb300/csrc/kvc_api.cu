@@ -454,10 +454,16 @@ kvc_status kvc_compact_rerotate_quant_ref(const kvc_shape* shape, const kvc_poli
     if (!rope_cos || !rope_sin || rope_max_pos < 1 || !aligned(rope_cos, 16) || !aligned(rope_sin, 16))
       return KVC_ERR_INVALID_ARG;
   }
+  if (policy->rope_layout != KVC_ROPE_SPLIT_HALF && policy->rope_layout != KVC_ROPE_INTERLEAVED)
+    return KVC_ERR_INVALID_ARG;
+  const int32_t rd = policy->rotary_dim ? policy->rotary_dim : shape->head_dim;
+  if (rd < 16 || rd > shape->head_dim || rd % 16 != 0) return KVC_ERR_INVALID_ARG;
   DevInfo info;
   if ((st = check_device(&info)) != KVC_OK) return st;
   CompactArgs a = {};
   if (ref) a.ref = *ref;
+  a.rope_layout = policy->rope_layout;
+  a.rotary_dim = rd;
   a.U = static_cast<int32_t>(n_units(shape));
   a.d = shape->head_dim;
   a.T = shape->n_tokens;

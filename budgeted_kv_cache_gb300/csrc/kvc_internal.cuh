@@ -85,6 +85,8 @@ struct CompactArgs {
   int32_t* unit_status;
   int32_t pool_lo, pool_hi;    // pools to process: [pool_lo, pool_hi)
   kvc_ref_store ref;           // reference store (ref.ref_pos == NULL: none)
+  int32_t rope_layout;         // KVC_ROPE_*
+  int32_t rotary_dim;          // rotated leading elements (a multiple of 16, <= d)
 };
 
 struct DecodeArgs {

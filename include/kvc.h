@@ -83,6 +83,12 @@ enum {
   KVC_QUANT_ROW_FP16 = 1    /* one fp16 scale per row (PASK App. B.5)      */
 };
 
+/* Rotary layouts of the stored keys (PACE Sec. 3.2: re-rotation applies the
+ * same rotation to the rotated dimensions only).  Split halves pair element
+ * i with i + rotary_dim/2; interleaved pairs 2i with 2i + 1.  The cos / sin
+ * tables hold rotary_dim / 2 columns. */
+enum { KVC_ROPE_SPLIT_HALF = 0, KVC_ROPE_INTERLEAVED = 1 };
+
 /* kvc_score flags. */
 enum { KVC_SCORE_ACCUMULATE = 1 };
 
@@ -208,6 +214,8 @@ typedef struct {
   const uint8_t* flags;    /* optional uint8 [B][T] (token mode) or [B][T/P] (page mode) */
   const uint8_t* tags;     /* byte mode: uint8 [B][T], each < n_tags      */
   const uint8_t* action_table; /* byte mode: uint8 [n_tags][n_layer_groups] of KVC_ACT_* */
+  int32_t rope_layout;     /* KVC_ROPE_SPLIT_HALF (0) or KVC_ROPE_INTERLEAVED */
+  int32_t rotary_dim;      /* rotated leading dimensions, a multiple of 16; 0 = head_dim */
 } kvc_policy;
 
 /* ------------------------------------------------------------------------
@@ -290,7 +298,9 @@ typedef struct {
  * element i pairs with i + d/2.  Fixed fp32 order, no fused multiply-add:
  *   C = c'c + s's,  S = s'c - c's,  n = sqrt(C C + S S),  C /= n,  S /= n,
  *   x' = x C - y S,  y' = y C + x S,  then round to bf16 (nearest even);
- * p' == p copies the stored bits.  V rows are copied.
+ * p' == p copies the stored bits.  V rows are copied.  policy->rope_layout
+ * and policy->rotary_dim select the pairs (see KVC_ROPE_*): only the first
+ * rotary_dim elements rotate, the rest are copied.
  * PASK App. B.5: a quantised pool stores symmetric codes of the bf16 row:
  * per group a = max|x|, scale = a / qmax rounded to the scale format
  * (nearest even) and raised to its smallest positive value, code =

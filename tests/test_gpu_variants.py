@@ -88,3 +88,32 @@ def test_shared_index_set_end_to_end(kvc):
             ref_pools = o.compact_unit(ui["k"], ui["v"], ui["pos"], act, prm, cos, sin)
             assert np.array_equal(bits(p.pools.k_bf16[u, :n]), ref_pools[o.ACT_BF16].k)
             assert np.array_equal(bits(p.pools.v_bf16[u, :n]), ref_pools[o.ACT_BF16].v)
+
+
+@pytest.mark.parametrize("layout,rd", [("interleaved", 0), ("split", 64), ("interleaved", 64),
+                                       ("split", 0)])
+def test_rotary_layouts_bit_exact(kvc, layout, rd):
+    """Interleaved and partial rotary layouts (PACE Sec. 3.2: the same
+    rotation on the rotated dimensions only): compacted keys bit for bit."""
+    w = wl.tiny().replace(head_dim=128, n_tokens=900, budget_tokens=250)
+    x = wl.make_inputs(w, device="cuda", with_tables=False)
+    rdim = rd or w.head_dim
+    cos, sin = wl.rope_tables(w.capacity() + w.n_tokens, rdim, 1e4, device="cuda")
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    p = pass_for_workload(w, inputs=x)
+    p.policy.rope_layout = kvc.ROPE_INTERLEAVED if layout == "interleaved" else kvc.ROPE_SPLIT_HALF
+    p.policy.rotary_dim = rd
+    p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], cos, sin, x.get("bonus"))
+    torch.cuda.synchronize()
+    assert int(p.compact_status.abs().sum()) == 0
+    prm = params_of(w)
+    prm.rope_layout, prm.rotary_dim = layout, rd
+    cos_h, sin_h = cos.cpu().numpy(), sin.cpu().numpy()
+    for u in range(w.n_units):
+        ui = unit_inputs(w, x, u)
+        n = int(p.kept_count[2, u])
+        act = np.zeros(w.n_tokens, np.int64)
+        act[p.kept_idx[2, u, :n].cpu().numpy()] = o.ACT_BF16
+        ref = o.compact_unit(ui["k"], ui["v"], ui["pos"], act, prm, cos_h, sin_h)[o.ACT_BF16]
+        assert np.array_equal(bits(p.pools.k_bf16[u, :n]), ref.k)
+        assert np.array_equal(p.pools.pos_out[2, u, :n].cpu().numpy(), ref.pos)
