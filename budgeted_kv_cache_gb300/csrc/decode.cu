@@ -53,11 +53,11 @@ __device__ __forceinline__ float load_scale(const void* sp, int64_t row, int gro
 
 // FMAs of 8 consecutive key elements (starting at element e0) with every
 // query head; the query rows in shared memory are pre-scaled to log2 units.
-template <int D>
+template <int D, int GG>
 __device__ __forceinline__ void dot8(const float (&x)[8], const float (*qs)[D], int e0, int G,
-                                     float (&s)[kMaxG]) {
+                                     float (&s)[GG]) {
 #pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
+  for (int h = 0; h < GG; ++h) {
     if (h < G) {
       const float4 q0 = *reinterpret_cast<const float4*>(&qs[h][e0]);
       const float4 q1 = *reinterpret_cast<const float4*>(&qs[h][e0 + 4]);
@@ -78,10 +78,10 @@ __device__ __forceinline__ void dot8(const float (&x)[8], const float (*qs)[D], 
 // Scores of key row `row` of `pool` against every query head.  All loads
 // of a batch (half a bf16 row, or a whole int8 / int4 row and its scales)
 // are issued before any is used.
-template <int D>
+template <int D, int GG, bool BF>
 __device__ __forceinline__ void key_dot(int pool, const PoolPtrs& pp, int64_t row, bool row_mode,
-                                        const float (*qs)[D], int G, float (&s)[kMaxG]) {
-  if (pool == KVC_POOL_BF16) {
+                                        const float (*qs)[D], int G, float (&s)[GG]) {
+  if (BF || pool == KVC_POOL_BF16) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(pp.k) + row * D);
 #pragma unroll
     for (int half = 0; half < D / 64; ++half) {
@@ -97,7 +97,7 @@ __device__ __forceinline__ void key_dot(int pool, const PoolPtrs& pp, int64_t ro
           x[2 * k] = __uint_as_float(r[k] << 16);
           x[2 * k + 1] = __uint_as_float(r[k] & 0xffff0000u);
         }
-        dot8<D>(x, qs, half * 64 + v * 8, G, s);
+        dot8<D, GG>(x, qs, half * 64 + v * 8, G, s);
       }
     }
   } else {
@@ -126,7 +126,7 @@ __device__ __forceinline__ void key_dot(int pool, const PoolPtrs& pp, int64_t ro
           for (int k = 0; k < 8; ++k)
             x[k] = static_cast<float>(static_cast<int8_t>(r[2 * hlf + (k >> 2)] >> (8 * (k & 3)))) *
                    sc[(v * 16) / 32];
-          dot8<D>(x, qs, v * 16 + hlf * 8, G, s);
+          dot8<D, GG>(x, qs, v * 16 + hlf * 8, G, s);
         }
       }
     } else {
@@ -143,7 +143,7 @@ __device__ __forceinline__ void key_dot(int pool, const PoolPtrs& pp, int64_t ro
 #pragma unroll
           for (int k = 0; k < 8; ++k)      // low nibble = even element; sign-extended
             x[k] = static_cast<float>(static_cast<int32_t>(r[k4] << (28 - 4 * k)) >> 28) * sc[v];
-          dot8<D>(x, qs, v * 32 + k4 * 8, G, s);
+          dot8<D, GG>(x, qs, v * 32 + k4 * 8, G, s);
         }
       }
     }
@@ -151,12 +151,12 @@ __device__ __forceinline__ void key_dot(int pool, const PoolPtrs& pp, int64_t ro
 }
 
 // This lane's d / 32 columns of value row `row` of `pool`, dequantised.
-template <int D>
+template <int D, bool BF>
 __device__ __forceinline__ void load_value_cols(int pool, const PoolPtrs& pp, int64_t row, int lane,
                                                 bool row_mode, float (&v)[D / 32]) {
   constexpr int NC = D / 32;
   const int c0 = lane * NC;
-  if (pool == KVC_POOL_BF16) {
+  if (BF || pool == KVC_POOL_BF16) {
     const uint16_t* src = static_cast<const uint16_t*>(pp.v) + row * D + c0;
     if (NC == 4) {
       const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
@@ -193,12 +193,16 @@ __device__ __forceinline__ void load_value_cols(int pool, const PoolPtrs& pp, in
   }
 }
 
-template <int D>
+// GG: query heads per KV head rounded up to 1, 2, 4 or 8 (the loops over
+// heads are unrolled for GG); BF: only the bf16 pool holds rows (token and
+// page mode), so the int8 / int4 paths are not compiled in.
+template <int D, int GG, bool BF>
 __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeArgs a) {
   constexpr int NC = D / 32;
-  __shared__ __align__(16) float qs[kMaxG][D];
-  __shared__ float wm[kWarps][kMaxG], wl[kWarps][kMaxG];
-  __shared__ float wacc[kWarps][kMaxG][D];
+  constexpr int VB = 16;                         // value rows whose loads are in flight together
+  __shared__ __align__(16) float qs[GG][D];
+  __shared__ float wm[kWarps][GG], wl[kWarps][GG];
+  __shared__ float wacc[kWarps][GG][D];
 
   const int u = blockIdx.x, split = blockIdx.y;
   const int G = a.G, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -219,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeArgs a)
   const int lo = min(n, split * per), hi = min(n, lo + per);
   __syncthreads();
 
-  float m[kMaxG], l[kMaxG], acc[kMaxG][NC];
+  float m[GG], l[GG], acc[GG][NC];
 #pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
+  for (int h = 0; h < GG; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
 #pragma unroll
@@ -242,14 +246,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeArgs a)
       }
     }
     const int64_t row = static_cast<int64_t>(u) * a.capacity + rr;
-    float s[kMaxG];
+    float s[GG];
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) s[h] = 0.f;
-    if (pool >= 0) key_dot<D>(pool, pool_ptrs(a.pools, pool), row, row_mode, qs, G, s);
+    for (int h = 0; h < GG; ++h) s[h] = 0.f;
+    if (pool >= 0) key_dot<D, GG, BF>(pool, pool_ptrs(a.pools, pool), row, row_mode, qs, G, s);
     // ---- online softmax per head over this step's 32 rows (log2 domain)
-    float pr[kMaxG];
+    float pr[GG];
 #pragma unroll
-    for (int h = 0; h < kMaxG; ++h) {
+    for (int h = 0; h < GG; ++h) {
       if (h < G) {
         const float sv = pool >= 0 ? s[h] : -INFINITY;
         float mx = sv;
@@ -267,26 +271,26 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeArgs a)
         for (int c = 0; c < NC; ++c) acc[h][c] *= corr;
       }
     }
-    // ---- P V: lane = columns; the step's rows eight at a time, their loads
+    // ---- P V: lane = columns; the step's rows VB at a time, their loads
     // issued together; row j's pool and place come from lane j
 #pragma unroll 1
-    for (int j0 = 0; j0 < 32; j0 += 8) {
+    for (int j0 = 0; j0 < 32; j0 += VB) {
       if (base + j0 >= hi) break;                 // uniform across the warp
-      float v[8][NC];
+      float v[VB][NC];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < VB; ++k) {
         const int pk = __shfl_sync(kFull, pool, j0 + k);
         const int rk = __shfl_sync(kFull, rr, j0 + k);
 #pragma unroll
         for (int c = 0; c < NC; ++c) v[k][c] = 0.f;
         if (pk >= 0)
-          load_value_cols<D>(pk, pool_ptrs(a.pools, pk), static_cast<int64_t>(u) * a.capacity + rk,
-                             lane, row_mode, v[k]);
+          load_value_cols<D, BF>(pk, pool_ptrs(a.pools, pk), static_cast<int64_t>(u) * a.capacity + rk,
+                                 lane, row_mode, v[k]);
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < VB; ++k) {
 #pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
+        for (int h = 0; h < GG; ++h) {
           if (h < G) {
             const float pj = __shfl_sync(kFull, pr[h], j0 + k);
 #pragma unroll
@@ -299,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeArgs a)
 
   // ---- merge the warps of the CTA (Eq. 15), then write out or publish
 #pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
+  for (int h = 0; h < GG; ++h) {
     if (h < G) {
       if (lane == 0) {
         wm[warp][h] = m[h];
@@ -366,8 +370,23 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.d == 64) decode_kernel<64><<<dim3(a.U, a.splits), kThreads, 0, stream>>>(a);
-  else decode_kernel<128><<<dim3(a.U, a.splits), kThreads, 0, stream>>>(a);
+  const dim3 grid(a.U, a.splits);
+  const bool bf = a.pool_lo == KVC_POOL_BF16;
+  const int gg = a.G <= 1 ? 1 : a.G <= 2 ? 2 : a.G <= 4 ? 4 : 8;
+#define KVC_DECODE_LAUNCH(DD, GGV)                                                         \
+  if (a.d == DD && gg == GGV) {                                                           \
+    if (bf) decode_kernel<DD, GGV, true><<<grid, kThreads, 0, stream>>>(a);               \
+    else decode_kernel<DD, GGV, false><<<grid, kThreads, 0, stream>>>(a);                 \
+  }
+  KVC_DECODE_LAUNCH(64, 1)
+  KVC_DECODE_LAUNCH(64, 2)
+  KVC_DECODE_LAUNCH(64, 4)
+  KVC_DECODE_LAUNCH(64, 8)
+  KVC_DECODE_LAUNCH(128, 1)
+  KVC_DECODE_LAUNCH(128, 2)
+  KVC_DECODE_LAUNCH(128, 4)
+  KVC_DECODE_LAUNCH(128, 8)
+#undef KVC_DECODE_LAUNCH
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || a.splits == 1) return err;
   merge_kernel<<<dim3(a.U, a.G), 128, 0, stream>>>(a);
