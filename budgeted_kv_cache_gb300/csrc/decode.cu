@@ -197,7 +197,7 @@ __device__ __forceinline__ void load_value_cols(int pool, const PoolPtrs& pp, in
 // heads are unrolled for GG); BF: only the bf16 pool holds rows (token and
 // page mode), so the int8 / int4 paths are not compiled in.
 template <int D, int GG, bool BF>
-__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeArgs a) {
   constexpr int NC = D / 32;
   constexpr int VB = 16;                         // value rows whose loads are in flight together
   __shared__ __align__(16) float qs[GG][D];
