@@ -42,7 +42,7 @@ METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or
 # number of units (each unit's keys are read once), so a launch moves
 # bytes_per_unit x units.  Valid only for the kernel source with this SHA-1;
 # after any change the bench reports traffic as null until it is measured again.
-SCORE_TRAFFIC = {"sha1": "7c91166e90f737a3db81ecf5f2a202dfd5b615fe", "bytes_per_unit": (275705344 + 7645440) / 32}
+SCORE_TRAFFIC = {"sha1": "a80fb9d505362f2abb3058f0e76bf5d5e68e41c2", "bytes_per_unit": (275224064 + 7888640) / 32}
 UNIT = "tokens/s (summed over layer x KV-head units)"
 L2_FLUSH_BYTES = 256 << 20
 
