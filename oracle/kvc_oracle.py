@@ -809,3 +809,236 @@ def cache_bytes(n_tokens: int, n_layers: int, n_kv_heads: int, head_dim: int,
                 action: int = ACT_BF16, quant_mode: int = QUANT_G32_BF16) -> int:
     """Bytes of K and V payload for n_tokens tokens across all layers and KV heads."""
     return n_tokens * n_layers * n_kv_heads * row_bytes(action, head_dim, quant_mode)
+
+
+# ----------------------------------------------------------------------------
+# CommitKV Sec. 3.2-3.3: deletion effect of event pages, lifecycle states,
+# joint validation of completion candidates, protection of pending pages.
+# One layer of one sequence: k, v [H_kv][T][d]; window queries q [H_q][W][d];
+# query head h reads KV head h // (H_q / H_kv).  A page is an array of cache
+# indices.  The W window queries are the last W cache entries (row w at index
+# T - W + w) and see indices <= T - W + w, which is the page's p_i <= p for a
+# cache kept in position order.
+# ----------------------------------------------------------------------------
+
+STATE_UNCERTAIN, STATE_COMPLETION, STATE_DORMANT, STATE_NEWLY_ACTIVE, STATE_STILL_ACTIVE = 0, 1, 2, 3, 4
+STATE_NOT_COMPARED = 255
+
+
+def window_attention(k, v, q, scale: float):
+    """Attention weights a[r][j] and outputs o[r] of the window rows r = h W + w, fp64.
+
+    CommitKV Sec. 3.2 ("Deletion effect for event page"): a_pj is the weight
+    query p gives resident token j, o_p the head output.  k, v: [T][d] of one
+    KV head; q: [G][W][d] of the query heads that read it.
+    """
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    q = np.asarray(q, np.float64)
+    T = k.shape[0]
+    G, W, d = q.shape
+    rows = q.reshape(G * W, d)
+    last = np.tile(T - W + np.arange(W), G)
+    z = rows @ k.T * scale
+    z = np.where(np.arange(T)[None, :] <= last[:, None], z, -np.inf)
+    m = z.max(axis=1, keepdims=True)
+    e = np.exp(z - m)
+    a = e / e.sum(axis=1, keepdims=True)
+    return a, a @ v
+
+
+def deletion_ratio(a_row, o_row, v, tokens) -> float:
+    """Relative output change of one query row when `tokens` are deleted.
+
+    CommitKV Eq. 6: o^{\\E} = (o - sum_{i in E} a_i v_i) / (1 - sum_{i in E} a_i),
+    masked tokens having a_i = 0; Eq. 7's ratio ||o - o^{\\E}|| / ||o||.
+    Readings for the cases Eq. 6 leaves undefined: if the deleted tokens
+    hold all of the row's weight (1 - s <= 0) nothing is left to attend to
+    and the change is +inf; if ||o|| = 0 the ratio is 0 when the output does
+    not change and +inf otherwise.
+    """
+    tokens = np.asarray(tokens, dtype=np.int64)
+    o = np.asarray(o_row, np.float64)
+    if tokens.size == 0:
+        return 0.0
+    s = float(np.asarray(a_row, np.float64)[tokens].sum())
+    u = np.asarray(a_row, np.float64)[tokens] @ np.asarray(v, np.float64)[tokens]
+    if 1.0 - s <= 0.0:
+        return math.inf
+    o_del = (o - u) / (1.0 - s)
+    num = float(np.linalg.norm(o - o_del))
+    den = float(np.linalg.norm(o))
+    if den == 0.0:
+        return 0.0 if num == 0.0 else math.inf
+    return num / den
+
+
+def deletion_effect(k, v, q, scale: float, token_sets) -> np.ndarray:
+    """R(E; Q) of CommitKV Eq. 7 for each token set E, fp64.
+
+    k, v: [H_kv][T][d] of one layer; q: [H_q][W][d] (the window Q of Eq. 5).
+    R_h(E; Q) is the largest ratio over the window queries of head h, and
+    R(E; Q) the largest over the heads.
+    """
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    q = np.asarray(q, np.float64)
+    Hkv = k.shape[0]
+    G = q.shape[0] // Hkv
+    out = np.zeros(len(token_sets), dtype=np.float64)
+    for g in range(Hkv):
+        a, o = window_attention(k[g], v[g], q[g * G:(g + 1) * G], scale)
+        for p, E in enumerate(token_sets):
+            for r in range(a.shape[0]):
+                out[p] = max(out[p], deletion_ratio(a[r], o[r], v[g], E))
+    return out
+
+
+def page_tokens(start: int, length: int) -> np.ndarray:
+    """Cache indices of the contiguous event page [start, start + length)."""
+    return np.arange(start, start + length, dtype=np.int64)
+
+
+def percentile_ranks(values, compared) -> np.ndarray:
+    """Percentile rank of each compared page among the compared pages.
+
+    CommitKV Sec. 3.2 ("Influence comparison across a commit"), reading:
+    P(E) = |{E' in E_c : R(E') < R(E)}| / |E_c|, the fraction of the
+    comparison pages that E is more influential than (0 for pages outside E_c).
+    """
+    values = np.asarray(values, np.float64)
+    compared = np.asarray(compared, dtype=bool)
+    n = int(compared.sum())
+    out = np.zeros(values.shape[0], dtype=np.float64)
+    if n == 0:
+        return out
+    pool = values[compared]
+    for i in np.nonzero(compared)[0]:
+        out[i] = float((pool < values[i]).sum()) / n
+    return out
+
+
+@dataclass
+class CommitThresholds:
+    """CommitKV Sec. 4.1 settings."""
+    tau_use: float = 0.05
+    tau_dead: float = 0.01
+    rho_use: float = 0.75
+    rho_dead: float = 0.25
+    tau_joint: float = 0.01
+
+
+def lifecycle_states(r_minus, r_plus, compared, th: CommitThresholds):
+    """Eq. 9 indicators and the Eq. 10 state of each page.
+
+    Returns (state uint8, p_minus, p_plus); pages outside E_c get
+    STATE_NOT_COMPARED.
+    """
+    r_minus = np.asarray(r_minus, np.float64)
+    r_plus = np.asarray(r_plus, np.float64)
+    compared = np.asarray(compared, dtype=bool)
+    p_minus = percentile_ranks(r_minus, compared)
+    p_plus = percentile_ranks(r_plus, compared)
+    state = np.full(r_minus.shape[0], STATE_NOT_COMPARED, dtype=np.uint8)
+    for i in np.nonzero(compared)[0]:
+        hm = r_minus[i] >= th.tau_use and p_minus[i] >= th.rho_use
+        lm = r_minus[i] <= th.tau_dead and p_minus[i] <= th.rho_dead
+        hp = r_plus[i] >= th.tau_use and p_plus[i] >= th.rho_use
+        lp = r_plus[i] <= th.tau_dead and p_plus[i] <= th.rho_dead
+        if hm and lp:
+            state[i] = STATE_COMPLETION
+        elif lm and lp:
+            state[i] = STATE_DORMANT
+        elif lm and hp:
+            state[i] = STATE_NEWLY_ACTIVE
+        elif hm and hp:
+            state[i] = STATE_STILL_ACTIVE
+        else:
+            state[i] = STATE_UNCERTAIN
+    return state, p_minus, p_plus
+
+
+def candidate_order(state, r_minus, r_plus) -> list:
+    """Completion candidates by increasing R+, then decreasing R- (Sec. 3.3);
+    remaining ties by lower page index (reading)."""
+    cands = [i for i in range(len(state)) if state[i] == STATE_COMPLETION]
+    return sorted(cands, key=lambda i: (float(r_plus[i]), -float(r_minus[i]), i))
+
+
+def joint_validation(order, joint_effect, tau_joint: float):
+    """Greedy retirement-set construction of Eq. 11.
+
+    order: candidate pages in test order; joint_effect(list of pages) returns
+    R+ of deleting all their tokens at once.  A candidate joins D_c when the
+    joint effect of D_c with it stays <= tau_joint.  Returns (accepted pages,
+    the joint effect evaluated for each candidate in order).
+    """
+    accepted, tried = [], []
+    for p in order:
+        r = float(joint_effect(accepted + [p]))
+        tried.append(r)
+        if r <= tau_joint:
+            accepted.append(p)
+    return accepted, tried
+
+
+def commit_transition(k_plus, v_plus, q_plus, scale: float, pages, r_minus, r_plus, compared,
+                      th: CommitThresholds = CommitThresholds()):
+    """Lifecycle states and retirement set of one commit (Eqs. 8-11, Alg. 1).
+
+    pages: list of (start, length) in the post-commit cache (k_plus, v_plus,
+    window q_plus); r_minus, r_plus: per-page deletion effects of the two
+    windows.  The joint effect of Eq. 11 deletes the union of the pages'
+    tokens and evaluates Eqs. 6-7 on the post-commit window.
+    Returns (state, retire uint8, joint effects tried).
+    """
+    state, _, _ = lifecycle_states(r_minus, r_plus, compared, th)
+    order = candidate_order(state, r_minus, r_plus)
+
+    def joint(sel):
+        toks = np.concatenate([page_tokens(*pages[p]) for p in sel])
+        return deletion_effect(k_plus, v_plus, q_plus, scale, [toks])[0]
+
+    accepted, tried = joint_validation(order, joint, th.tau_joint)
+    retire = np.zeros(len(pages), dtype=np.uint8)
+    retire[accepted] = 1
+    return state, retire, tried
+
+
+def protect_pending(r_minus, page_len, pending, budget_tokens: int, max_pages: int) -> np.ndarray:
+    """Pages protected while awaiting their post-commit measurement (Eq. 12).
+
+    Pending pages are taken by decreasing R- (ties: lower index) while the
+    protected token count stays <= B_N = floor(eta B) and the page count <=
+    max_pages (CommitKV Sec. 4.1: 16); reading of "protected first until":
+    the walk stops at the first page that does not fit.
+    """
+    r_minus = np.asarray(r_minus, np.float64)
+    order = sorted((i for i in range(len(r_minus)) if pending[i]), key=lambda i: (-r_minus[i], i))
+    out = np.zeros(len(r_minus), dtype=np.uint8)
+    used = 0
+    n = 0
+    for i in order:
+        if n + 1 > max_pages or used + int(page_len[i]) > budget_tokens:
+            break
+        out[i] = 1
+        used += int(page_len[i])
+        n += 1
+    return out
+
+
+def commit_flags(n_tokens: int, pages, retire, protect, flags=None) -> np.ndarray:
+    """Selection flags of a checkpoint (Alg. 1, checkpoint step; Eq. 13).
+
+    Tokens of protected pages become PROTECT (not EXCLUDE), tokens of retired
+    pages that are not protected become EXCLUDE (not PROTECT); the decision
+    replaces the page's earlier protect / exclude state, other tokens keep
+    their flags.
+    """
+    out = np.zeros(n_tokens, np.uint8) if flags is None else np.array(flags, np.uint8, copy=True)
+    for p, (s, ln) in enumerate(pages):
+        if protect[p]:
+            out[s:s + ln] = (out[s:s + ln] & ~np.uint8(FLAG_EXCLUDE)) | FLAG_PROTECT
+        elif retire[p]:
+            out[s:s + ln] = (out[s:s + ln] & ~np.uint8(FLAG_PROTECT)) | FLAG_EXCLUDE
+    return out
