@@ -65,6 +65,16 @@ class kvc_ref_store(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("ref_k", "ref_pos", "ref_k_out", "ref_pos_out", "failures")]
 
 
+class kvc_effect_record(ctypes.Structure):
+    """Window record of kvc_deletion_effect (device pointers: o, lse, s, u)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("o", "lse", "s", "u")]
+
+
+class kvc_commit_thresholds(ctypes.Structure):
+    """CommitKV Sec. 4.1 thresholds."""
+    _fields_ = [(n, ctypes.c_float) for n in ("tau_use", "tau_dead", "rho_use", "rho_dead", "tau_joint")]
+
+
 def _load():
     global _LIB
     if _LIB is None:
@@ -75,6 +85,7 @@ def _load():
                                      ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t)
         SH, PO, PL = ctypes.POINTER(kvc_shape), ctypes.POINTER(kvc_policy), ctypes.POINTER(kvc_pools)
         RS = ctypes.POINTER(kvc_ref_store)
+        ER, CT = ctypes.POINTER(kvc_effect_record), ctypes.POINTER(kvc_commit_thresholds)
         sig = {
             "kvc_score_workspace_bytes": (SZ, [SH, I32]),
             "kvc_score": (ctypes.c_int, [SH, P, P, I32, F32, P, P, I32, U32, P, P, P, P, SZ, P]),
@@ -90,6 +101,13 @@ def _load():
             "kvc_pool_scores": (ctypes.c_int, [I64, I64, P, P, I32, I32, P]),
             "kvc_shared_scores": (ctypes.c_int, [SH, P, P, P]),
             "kvc_broadcast_kept": (ctypes.c_int, [SH, PO, P, P, P, P, P]),
+            "kvc_deletion_effect_workspace_bytes": (SZ, [SH, I32]),
+            "kvc_deletion_effect": (ctypes.c_int, [SH, P, P, P, I32, F32, P, P, I32, P, ER, P, P, SZ, P]),
+            "kvc_commit_workspace_bytes": (SZ, [SH, I32]),
+            "kvc_commit_transition": (ctypes.c_int, [SH, I32, I32, I32, P, P, P, CT, ER, P, P, P, P, SZ,
+                                                     P]),
+            "kvc_protect_pending": (ctypes.c_int, [SH, I32, I32, P, P, P, I32, I32, P, P]),
+            "kvc_commit_flags": (ctypes.c_int, [I32, I64, I32, P, P, P, P, P, P]),
             "kvc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -310,3 +328,74 @@ def kvc_decode_attn_noalloc(shape, policy: Policy, q, pools: Pools, kept_count, 
     _check("kvc_decode_attn_noalloc", _load().kvc_decode_attn_noalloc(
         ctypes.byref(shape), ctypes.byref(cp), _p(q), ctypes.byref(cpools), _p(kept_count),
         float(softmax_scale), _p(out), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- CommitKV
+
+STATE_UNCERTAIN, STATE_COMPLETION, STATE_DORMANT, STATE_NEWLY_ACTIVE, STATE_STILL_ACTIVE = 0, 1, 2, 3, 4
+STATE_NOT_COMPARED = 255
+
+
+class EffectRecord:
+    """Device buffers of a kvc_deletion_effect record (see include/kvc.h)."""
+
+    def __init__(self, shape: kvc_shape, window: int, n_pages: int, device="cuda"):
+        B, L, Hq = shape.batch, shape.n_layers, shape.n_q_heads
+        f32 = torch.float32
+        self.o = torch.empty((B, L, Hq, window, 128), dtype=f32, device=device)
+        self.lse = torch.empty((B, L, Hq, window), dtype=f32, device=device)
+        self.s = torch.empty((B, L, max(n_pages, 1), Hq, window), dtype=f32, device=device)
+        self.u = torch.empty((B, L, max(n_pages, 1), Hq, window, 128), dtype=f32, device=device)
+
+    def c(self) -> kvc_effect_record:
+        return kvc_effect_record(_p(self.o), _p(self.lse), _p(self.s), _p(self.u))
+
+
+def kvc_deletion_effect_workspace_bytes(shape: kvc_shape, window: int) -> int:
+    return _load().kvc_deletion_effect_workspace_bytes(ctypes.byref(shape), window)
+
+
+def kvc_deletion_effect(shape, k_cache, v_cache, q_window, window, softmax_scale, page_start,
+                        page_len, effect, record: EffectRecord, workspace, unit_status=None,
+                        stream=None):
+    """CommitKV Eqs. 6-7 per page: effect fp32 [B][L][n_pages] (see include/kvc.h)."""
+    n = 0 if page_start is None else int(page_start.shape[-1])
+    rec = record.c()
+    _check("kvc_deletion_effect", _load().kvc_deletion_effect(
+        ctypes.byref(shape), _p(k_cache), _p(v_cache), _p(q_window), int(window),
+        float(softmax_scale), _p(page_start), _p(page_len), n, _p(effect), ctypes.byref(rec),
+        _p(unit_status), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def kvc_commit_workspace_bytes(shape: kvc_shape, window: int) -> int:
+    return _load().kvc_commit_workspace_bytes(ctypes.byref(shape), window)
+
+
+def kvc_commit_transition(shape, window, layer, effect_minus, effect_plus, compared,
+                          record_plus: EffectRecord, state, retire, workspace, joint=None,
+                          tau_use=0.05, tau_dead=0.01, rho_use=0.75, rho_dead=0.25, tau_joint=0.01,
+                          stream=None):
+    """CommitKV Eqs. 8-11 on layer `layer`: lifecycle states and the retirement set."""
+    th = kvc_commit_thresholds(tau_use, tau_dead, rho_use, rho_dead, tau_joint)
+    rec = record_plus.c()
+    _check("kvc_commit_transition", _load().kvc_commit_transition(
+        ctypes.byref(shape), int(window), int(layer), int(effect_minus.shape[-1]), _p(effect_minus),
+        _p(effect_plus), _p(compared), ctypes.byref(th), ctypes.byref(rec), _p(state), _p(retire),
+        _p(joint), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kvc_protect_pending(shape, layer, effect_minus, pending, page_len, budget_tokens, max_pages,
+                        protect, stream=None):
+    """CommitKV Eq. 12: pending pages protected within B_N tokens and max_pages pages."""
+    _check("kvc_protect_pending", _load().kvc_protect_pending(
+        ctypes.byref(shape), int(layer), int(effect_minus.shape[-1]), _p(effect_minus), _p(pending),
+        _p(page_len), int(budget_tokens), int(max_pages), _p(protect), _stream(stream)))
+
+
+def kvc_commit_flags(batch, n_tokens, page_start, page_len, retire, protect, flags, stream=None):
+    """Checkpoint flags (Eq. 13) painted over the pages' tokens, in place."""
+    n = 0 if page_start is None else int(page_start.shape[-1])
+    _check("kvc_commit_flags", _load().kvc_commit_flags(
+        int(batch), int(n_tokens), n, _p(page_start), _p(page_len), _p(retire), _p(protect),
+        _p(flags), _stream(stream)))

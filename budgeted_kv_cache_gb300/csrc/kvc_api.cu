@@ -211,6 +211,44 @@ int decode_splits(const kvc_shape* s, const kvc_policy* pol, int sms) {
 
 }  // namespace
 
+// ---------------------------------------------------------------- CommitKV plans
+struct EffectPlan {
+  int R = 0, Rp = 0, n_tiles = 0, chunk = 0, splits = 0, n_items = 0, grid = 0, nk = 0, nv = 0;
+  size_t smem = 0, ws_part_u = 0, ws_total = 0;
+};
+
+kvc_status plan_effect(const kvc_shape* s, int32_t window, EffectPlan* p) {
+  kvc_status st = check_shape(s);
+  if (st != KVC_OK) return st;
+  if (s->head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (window < 1 || window > s->n_tokens) return KVC_ERR_INVALID_ARG;
+  const int64_t R = static_cast<int64_t>(window) * (s->n_q_heads / s->n_kv_heads);
+  if (R > 64) return KVC_ERR_UNSUPPORTED;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  p->R = static_cast<int>(R);
+  p->Rp = (p->R + 15) / 16 * 16;
+  p->n_tiles = static_cast<int>((s->n_tokens + kTileTokens - 1) / kTileTokens);
+  const int64_t U = n_units(s);
+  // chunks of 2..8 tiles: the keys of all resident items stay in L2 between
+  // the two passes, and there are about two items per SM
+  const int64_t want = (U * p->n_tiles + 2 * info.sms - 1) / (2 * info.sms);
+  p->chunk = static_cast<int>(std::min<int64_t>(std::max<int64_t>(want, 2), 8));
+  p->chunk = std::min(p->chunk, p->n_tiles);
+  p->splits = (p->n_tiles + p->chunk - 1) / p->chunk;
+  const int64_t items = U * p->splits;
+  if (items > 0x7fffffffLL || U * p->R > 0x7fffffffLL || U > 65535) return KVC_ERR_UNSUPPORTED;
+  p->n_items = static_cast<int>(items);
+  p->grid = static_cast<int>(std::min<int64_t>(items, info.sms));
+  p->nk = 2;
+  p->nv = p->Rp <= 32 ? 3 : 2;
+  p->smem = effect_smem_bytes(p->Rp, p->nk, p->nv);
+  if (p->smem > 232448) return KVC_ERR_UNSUPPORTED;
+  p->ws_part_u = (static_cast<size_t>(items) * p->R * 128 * 4 + 255) / 256 * 256;
+  p->ws_total = p->ws_part_u + (static_cast<size_t>(items) * p->R * 8 + 255) / 256 * 256;
+  return KVC_OK;
+}
+
 extern "C" {
 
 const char* kvc_status_string(kvc_status status) {
@@ -544,6 +582,175 @@ kvc_status kvc_decode_attn(const kvc_shape* shape, const kvc_policy* policy, con
   a.pool_lo = sp.byte_mode ? KVC_POOL_INT4 : KVC_POOL_BF16;
   a.pool_hi = KVC_N_POOLS;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+size_t kvc_deletion_effect_workspace_bytes(const kvc_shape* shape, int32_t window) {
+  EffectPlan p;
+  if (plan_effect(shape, window, &p) != KVC_OK) return 0;
+  return p.ws_total;
+}
+
+kvc_status kvc_deletion_effect(const kvc_shape* shape, const void* k_cache, const void* v_cache,
+                               const void* q_window, int32_t window, float softmax_scale,
+                               const int32_t* page_start, const int32_t* page_len,
+                               int32_t n_pages, float* effect, const kvc_effect_record* record,
+                               int32_t* unit_status, void* workspace, size_t workspace_bytes,
+                               kvc_stream stream) {
+  EffectPlan p;
+  kvc_status st = plan_effect(shape, window, &p);
+  if (st != KVC_OK) return st;
+  if (!k_cache || !v_cache || !q_window || !record || !record->o || !record->lse) return KVC_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q_window, 16)) return KVC_ERR_INVALID_ARG;
+  if (n_pages < 0) return KVC_ERR_INVALID_ARG;
+  if (n_pages > 0 && (!page_start || !page_len || !effect || !record->s || !record->u))
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned(record->o, 16) || (n_pages > 0 && !aligned(record->u, 16))) return KVC_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < p.ws_total || !aligned(workspace, 256)) return KVC_ERR_WORKSPACE;
+  if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / sqrtf(static_cast<float>(shape->head_dim));
+
+  EffectArgs a = {};
+  a.U = static_cast<int32_t>(n_units(shape));
+  a.L = shape->n_layers;
+  a.Hkv = shape->n_kv_heads;
+  a.B = shape->batch;
+  a.G = shape->n_q_heads / shape->n_kv_heads;
+  a.W = window;
+  a.R = p.R;
+  a.Rp = p.Rp;
+  a.T = shape->n_tokens;
+  a.n_tiles = p.n_tiles;
+  a.chunk_tiles = p.chunk;
+  a.splits = p.splits;
+  a.n_items = p.n_items;
+  a.nk = p.nk;
+  a.nv = p.nv;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.part_u = static_cast<float*>(workspace);
+  a.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + p.ws_part_u);
+  a.o = record->o;
+  a.lse = record->lse;
+  a.s = record->s;
+  a.u = record->u;
+  a.page_start = page_start;
+  a.page_len = page_len;
+  a.n_pages = n_pages;
+  a.k = static_cast<const __nv_bfloat16*>(k_cache);
+  a.v = static_cast<const __nv_bfloat16*>(v_cache);
+  a.q = static_cast<const __nv_bfloat16*>(q_window);
+  a.effect = effect;
+  a.unit_status = unit_status;
+
+  CUtensorMap mk, mv, mq;
+  if ((st = encode_3d(&mk, k_cache, 128, shape->n_tokens, a.U, 64, kTileTokens)) != KVC_OK) return st;
+  if ((st = encode_3d(&mv, v_cache, 128, shape->n_tokens, a.U, 64, kTileTokens)) != KVC_OK) return st;
+  if ((st = encode_3d(&mq, q_window, 128, p.R, a.U, 64, p.R)) != KVC_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (n_pages > 0 &&
+      cudaMemsetAsync(effect, 0, static_cast<size_t>(shape->batch) * shape->n_layers * n_pages * 4, cs) !=
+          cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (launch_effect(a, mk, mv, mq, p.grid, p.smem, cs) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+size_t kvc_commit_workspace_bytes(const kvc_shape* shape, int32_t window) {
+  if (check_shape(shape) != KVC_OK || window < 1) return 0;
+  return (static_cast<size_t>(shape->batch) * shape->n_q_heads * window * 128 * 4 + 255) / 256 * 256;
+}
+
+kvc_status kvc_commit_transition(const kvc_shape* shape, int32_t window, int32_t layer,
+                                 int32_t n_pages, const float* effect_minus,
+                                 const float* effect_plus, const uint8_t* compared,
+                                 const kvc_commit_thresholds* thresholds,
+                                 const kvc_effect_record* record_plus, uint8_t* state,
+                                 uint8_t* retire, float* joint, void* workspace,
+                                 size_t workspace_bytes, kvc_stream stream) {
+  kvc_status st = check_shape(shape);
+  if (st != KVC_OK) return st;
+  if (shape->head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (window < 1 || layer < 0 || layer >= shape->n_layers) return KVC_ERR_INVALID_ARG;
+  if (n_pages < 1 || n_pages > 1024) return KVC_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(shape->n_q_heads) * window > 4096) return KVC_ERR_UNSUPPORTED;
+  if (!effect_minus || !effect_plus || !compared || !thresholds || !record_plus || !record_plus->o ||
+      !record_plus->s || !record_plus->u || !state || !retire)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned(record_plus->o, 16) || !aligned(record_plus->u, 16)) return KVC_ERR_INVALID_ARG;
+  const size_t need = kvc_commit_workspace_bytes(shape, window);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVC_ERR_WORKSPACE;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  CommitArgs a = {};
+  a.B = shape->batch;
+  a.L = shape->n_layers;
+  a.Hq = shape->n_q_heads;
+  a.W = window;
+  a.n_pages = n_pages;
+  a.layer = layer;
+  a.tau_use = thresholds->tau_use;
+  a.tau_dead = thresholds->tau_dead;
+  a.rho_use = thresholds->rho_use;
+  a.rho_dead = thresholds->rho_dead;
+  a.tau_joint = thresholds->tau_joint;
+  a.r_minus = effect_minus;
+  a.r_plus = effect_plus;
+  a.compared = compared;
+  a.o = record_plus->o;
+  a.s = record_plus->s;
+  a.u = record_plus->u;
+  a.acc = static_cast<float*>(workspace);
+  a.state = state;
+  a.retire = retire;
+  a.joint = joint;
+  if (launch_commit(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+kvc_status kvc_protect_pending(const kvc_shape* shape, int32_t layer, int32_t n_pages,
+                               const float* effect_minus, const uint8_t* pending,
+                               const int32_t* page_len, int32_t budget_tokens, int32_t max_pages,
+                               uint8_t* protect, kvc_stream stream) {
+  kvc_status st = check_shape(shape);
+  if (st != KVC_OK) return st;
+  if (layer < 0 || layer >= shape->n_layers || n_pages < 1 || n_pages > 1024) return KVC_ERR_INVALID_ARG;
+  if (budget_tokens < 0 || max_pages < 0) return KVC_ERR_INVALID_ARG;
+  if (!effect_minus || !pending || !page_len || !protect) return KVC_ERR_INVALID_ARG;
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  ProtectArgs a = {};
+  a.B = shape->batch;
+  a.L = shape->n_layers;
+  a.n_pages = n_pages;
+  a.layer = layer;
+  a.budget_tokens = budget_tokens;
+  a.max_pages = max_pages;
+  a.r_minus = effect_minus;
+  a.pending = pending;
+  a.page_len = page_len;
+  a.protect = protect;
+  if (launch_protect(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+kvc_status kvc_commit_flags(int32_t batch, int64_t n_tokens, int32_t n_pages,
+                            const int32_t* page_start, const int32_t* page_len,
+                            const uint8_t* retire, const uint8_t* protect, uint8_t* flags,
+                            kvc_stream stream) {
+  if (batch < 1 || batch > 65535 || n_tokens < 1 || n_pages < 0 || n_pages > (1 << 30)) return KVC_ERR_INVALID_ARG;
+  if (n_pages > 0 && (!page_start || !page_len || !flags)) return KVC_ERR_INVALID_ARG;
+  DevInfo info;
+  kvc_status st;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  FlagArgs a = {};
+  a.B = batch;
+  a.n_pages = n_pages;
+  a.T = n_tokens;
+  a.page_start = page_start;
+  a.page_len = page_len;
+  a.retire = retire;
+  a.protect = protect;
+  a.flags = flags;
+  if (launch_flags(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
   return KVC_OK;
 }
 

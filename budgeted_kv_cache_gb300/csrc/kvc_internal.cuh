@@ -117,6 +117,66 @@ struct BonusArgs {
   float* bonus;                // [B][T]
 };
 
+// CommitKV deletion effect (Sec. 3.2): window attention of a unit's R = G W
+// rows, split into work items of chunk_tiles key tiles; then the per-page
+// weights and value sums.
+struct EffectArgs {
+  int32_t U, L, Hkv, B, G, W, R, Rp;
+  int64_t T;
+  int32_t n_tiles, chunk_tiles, splits, n_items;
+  int32_t nk, nv;              // key / value stage counts
+  float scale_log2;            // softmax scale * log2(e)
+  float* part_u;               // [n_items][R][128] unnormalised value sums of a split
+  float2* part_ml;             // [n_items][R] (max, exp2-sum) of y = z * scale_log2
+  float* o;                    // [U][R][128] window outputs
+  float* lse;                  // [U][R] natural-log softmax denominators
+  float* s;                    // [B][L][n_pages][H_q][W] page weights
+  float* u;                    // [B][L][n_pages][H_q][W][128] page value sums
+  const int32_t* page_start;   // [B][n_pages]
+  const int32_t* page_len;     // [B][n_pages]
+  int32_t n_pages;
+  const __nv_bfloat16* k;      // [U][T][128]
+  const __nv_bfloat16* v;      // [U][T][128]
+  const __nv_bfloat16* q;      // [U][R][128]
+  float* effect;               // [B][L][n_pages] (zeroed before the page kernel)
+  int32_t* unit_status;        // optional [U]
+};
+
+// CommitKV Eqs. 9-11 for one layer of each sequence.
+struct CommitArgs {
+  int32_t B, L, Hq, W, n_pages, layer;
+  float tau_use, tau_dead, rho_use, rho_dead, tau_joint;
+  const float* r_minus;        // [B][L][n_pages]
+  const float* r_plus;         // [B][L][n_pages]
+  const uint8_t* compared;     // [B][n_pages]
+  const float* o;              // record of the post-commit window: [B][L][H_q][W][128]
+  const float* s;              // [B][L][n_pages][H_q][W]
+  const float* u;              // [B][L][n_pages][H_q][W][128]
+  float* acc;                  // workspace [B][H_q W][128]
+  uint8_t* state;              // [B][n_pages]
+  uint8_t* retire;             // [B][n_pages]
+  float* joint;                // optional [B][n_pages]
+};
+
+struct ProtectArgs {
+  int32_t B, L, n_pages, layer;
+  int32_t budget_tokens, max_pages;
+  const float* r_minus;        // [B][L][n_pages]
+  const uint8_t* pending;      // [B][n_pages]
+  const int32_t* page_len;     // [B][n_pages]
+  uint8_t* protect;            // [B][n_pages]
+};
+
+struct FlagArgs {
+  int32_t B, n_pages;
+  int64_t T;
+  const int32_t* page_start;   // [B][n_pages]
+  const int32_t* page_len;     // [B][n_pages]
+  const uint8_t* retire;       // optional [B][n_pages]
+  const uint8_t* protect;      // optional [B][n_pages]
+  uint8_t* flags;              // [B][T]
+};
+
 // host launchers (each returns a cudaError_t from the launch)
 cudaError_t launch_bonus(const BonusArgs& a, cudaStream_t stream);
 cudaError_t launch_pool(const float* in, float* out, int64_t rows, int64_t n, int kernel, int mode,
@@ -131,6 +191,12 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes);
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+size_t effect_smem_bytes(int Rp, int nk, int nv);
+cudaError_t launch_effect(const EffectArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                          const CUtensorMap& tmap_q, int grid, size_t smem_bytes, cudaStream_t stream);
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
+cudaError_t launch_protect(const ProtectArgs& a, cudaStream_t stream);
+cudaError_t launch_flags(const FlagArgs& a, cudaStream_t stream);
 
 // ----------------------------------------------------------------------------
 // device helpers

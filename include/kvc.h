@@ -411,6 +411,133 @@ kvc_status kvc_decode_attn_noalloc(const kvc_shape* shape, const kvc_policy* pol
                                    const int32_t* kept_count, float softmax_scale, void* out,
                                    kvc_stream stream);
 
+/* ------------------------------------------------------------------------
+ * CommitKV lifecycle-aware retirement ("CommitKV: Lifecycle-Aware KV Cache
+ * Compression via Commit Transitions for Multi-Turn Agents", Sec. 3.2-3.3).
+ *
+ * An event page is a span [start, start + len) of cache indices, 0 <= len
+ * <= 64 (the pages use G = 16); the pages of one call are disjoint.  A
+ * window is the last W cache entries (Eq. 5: Q- ends at the tool call's
+ * completion, Q+ holds the first W queries of the next turn): row w of query
+ * head h sits at index T - W + w and sees indices <= T - W + w, which is
+ * "p_i <= p" of Eq. 6 for a cache kept in position order.
+ *
+ * kvc_deletion_effect -- Eqs. 6-7 for every page and every layer given:
+ *   a_rj = softmax_j(q_r . k_j * scale) over the visible keys, o_r = sum a_rj v_j,
+ *   s_rE = sum_{j in E} a_rj, u_rE = sum_{j in E} a_rj v_j,
+ *   effect[b][l][E] = max over the layer's H_q heads and W rows of
+ *       || o_r - (o_r - u_rE) / (1 - s_rE) || / || o_r ||
+ *   (+inf if 1 - s_rE <= 0; 0 / +inf if ||o_r|| = 0 and the change is zero /
+ *   not zero).  fp32 throughout; the value products use P with 16
+ *   significant bits (bf16 head + bf16 tail).
+ * k_cache, v_cache  bf16 [B][L][H_kv][T][128]; q_window bf16 [B][L][H_q][W][128]
+ *   (rotated); all 16-byte aligned.  head_dim must be 128, W (H_q / H_kv)
+ *   <= 64, W <= T.
+ * page_start, page_len  int32 [B][n_pages] (the same pages for every layer);
+ *   a page outside [0, T) or longer than 64 marks every unit of its sequence
+ *   KVC_UNIT_BAD_INDEX in unit_status and counts as empty.
+ * effect  fp32 [B][L][n_pages], overwritten.
+ * record  caller buffers, all required, overwritten (inputs of
+ *   kvc_commit_transition for the post-commit window):
+ *     o    fp32 [B][L][H_q][W][128]   window outputs
+ *     lse  fp32 [B][L][H_q][W]        natural-log softmax denominators
+ *     s    fp32 [B][L][n_pages][H_q][W]
+ *     u    fp32 [B][L][n_pages][H_q][W][128]
+ * unit_status  optional int32 [U]; KVC_UNIT_TIMEOUT / KVC_UNIT_BAD_INDEX on
+ *   failure, untouched otherwise.
+ * workspace >= kvc_deletion_effect_workspace_bytes(shape, W), 256-byte
+ *   aligned, contents need not be initialised.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  float* o;
+  float* lse;
+  float* s;
+  float* u;
+} kvc_effect_record;
+
+size_t kvc_deletion_effect_workspace_bytes(const kvc_shape* shape, int32_t window);
+kvc_status kvc_deletion_effect(const kvc_shape* shape, const void* k_cache, const void* v_cache,
+                               const void* q_window, int32_t window, float softmax_scale,
+                               const int32_t* page_start, const int32_t* page_len,
+                               int32_t n_pages, float* effect, const kvc_effect_record* record,
+                               int32_t* unit_status, void* workspace, size_t workspace_bytes,
+                               kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * kvc_commit_transition -- Eqs. 8-11 on one layer of every sequence.
+ *
+ * effect_minus, effect_plus  fp32 [B][L][n_pages]: R- and R+ of the same
+ *   pages (kvc_deletion_effect over Q- and over Q+); `layer` selects the
+ *   attention layer whose effects decide (the page measures one layer).
+ * compared  uint8 [B][n_pages]: nonzero = the page is in E_c (both effects
+ *   computable).  Percentile rank P(E) = |{E' in E_c : R(E') < R(E)}| / |E_c|.
+ * Eq. 9: H = R >= tau_use and P >= rho_use, L = R <= tau_dead and P <= rho_dead.
+ * state  uint8 [B][n_pages]: KVC_STATE_* (Eq. 10); KVC_STATE_NOT_COMPARED
+ *   outside E_c.
+ * retire uint8 [B][n_pages]: 1 = the page joins D_c.  Completion candidates
+ *   are tested by increasing R+, then decreasing R-, then lower index; a
+ *   candidate joins if R+ of deleting D_c and it together (Eqs. 6-7 on the
+ *   combined token set, from record_plus) is <= tau_joint (Eq. 11).
+ * joint  optional fp32 [B][n_pages]: the joint R+ each candidate was tested
+ *   with; -1 for pages that were not tested.
+ * record_plus  the record of the kvc_deletion_effect call over Q+ (same
+ *   shape, window and pages).  n_pages <= 1024, H_q W <= 4096.
+ * workspace >= kvc_commit_workspace_bytes(shape, W), 256-byte aligned.
+ * ---------------------------------------------------------------------- */
+enum {
+  KVC_STATE_UNCERTAIN = 0,
+  KVC_STATE_COMPLETION_CANDIDATE = 1,
+  KVC_STATE_DORMANT = 2,
+  KVC_STATE_NEWLY_ACTIVE = 3,
+  KVC_STATE_STILL_ACTIVE = 4,
+  KVC_STATE_NOT_COMPARED = 255
+};
+
+typedef struct {
+  float tau_use;    /* 0.05 (CommitKV Sec. 4.1) */
+  float tau_dead;   /* 0.01 */
+  float rho_use;    /* 0.75 */
+  float rho_dead;   /* 0.25 */
+  float tau_joint;  /* 0.01 */
+} kvc_commit_thresholds;
+
+size_t kvc_commit_workspace_bytes(const kvc_shape* shape, int32_t window);
+kvc_status kvc_commit_transition(const kvc_shape* shape, int32_t window, int32_t layer,
+                                 int32_t n_pages, const float* effect_minus,
+                                 const float* effect_plus, const uint8_t* compared,
+                                 const kvc_commit_thresholds* thresholds,
+                                 const kvc_effect_record* record_plus, uint8_t* state,
+                                 uint8_t* retire, float* joint, void* workspace,
+                                 size_t workspace_bytes, kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * kvc_protect_pending -- Eq. 12: pages awaiting their post-commit
+ * measurement (pending != 0) are protected by decreasing R- of layer
+ * `layer` (ties: lower index) while the protected token count stays
+ * <= budget_tokens (B_N = floor(eta B)) and the page count <= max_pages
+ * (the page uses 16); the walk stops at the first page that does not fit.
+ * effect_minus fp32 [B][L][n_pages]; pending uint8 [B][n_pages];
+ * page_len int32 [B][n_pages]; protect uint8 [B][n_pages] (0 / 1).
+ * n_pages <= 1024.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_protect_pending(const kvc_shape* shape, int32_t layer, int32_t n_pages,
+                               const float* effect_minus, const uint8_t* pending,
+                               const int32_t* page_len, int32_t budget_tokens, int32_t max_pages,
+                               uint8_t* protect, kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * kvc_commit_flags -- the checkpoint's selection flags (Alg. 1, Eq. 13):
+ * tokens of protected pages become KVC_FLAG_PROTECT (EXCLUDE cleared), tokens
+ * of retired pages that are not protected become KVC_FLAG_EXCLUDE (PROTECT
+ * cleared); every other token keeps its flags.  flags uint8 [B][n_tokens]
+ * (kvc_policy.flags of token mode), updated in place; retire / protect
+ * optional uint8 [B][n_pages]; pages as in kvc_deletion_effect.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_commit_flags(int32_t batch, int64_t n_tokens, int32_t n_pages,
+                            const int32_t* page_start, const int32_t* page_len,
+                            const uint8_t* retire, const uint8_t* protect, uint8_t* flags,
+                            kvc_stream stream);
+
 /* Static text for a status code. */
 const char* kvc_status_string(kvc_status status);
 

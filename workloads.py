@@ -278,3 +278,120 @@ def unit_coords(w: Workload, u: int):
     l = (u // w.n_kv_heads) % w.n_layers
     b = u // (w.n_kv_heads * w.n_layers)
     return b, l, g
+
+
+# --------------------------------------------------------------------------
+# CommitKV deletion-effect measurements
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class EffectWorkload:
+    """One attention layer's window measurement over scanned event pages.
+
+    CommitKV Sec. 4.1: query window W = 8, event pages of at most G = 16
+    tokens, at most 64 pages scanned per commit.  Two windows are drawn
+    over the same cache: the pre-commit one leans toward one set of "heavy"
+    pages and the post-commit one toward another, partly overlapping set, so
+    that all lifecycle transitions occur.
+    """
+    name: str
+    batch: int
+    n_layers: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    n_tokens: int
+    seed: int
+    window: int = 8
+    n_pages: int = 64
+    page_len: int = 16
+    heavy_pages: int = 12        # heavy pages of each window (a third shared)
+    lean: float = 7.5            # size of the shared direction added to queries / heavy keys
+    away: float = 3.0            # post-commit queries lean away from the pre-commit direction
+    value_mean: float = 1.0      # norm of a per-head mean added to every value, in units of sqrt(d)
+    ragged_pages: bool = False   # one short page, one empty page, one over the window rows
+
+    @property
+    def group(self) -> int:
+        return self.n_q_heads // self.n_kv_heads
+
+    @property
+    def n_units(self) -> int:
+        return self.batch * self.n_layers * self.n_kv_heads
+
+
+def commitkv_effect_128k() -> EffectWorkload:
+    """Qwen3-8B layout, one layer, T=131072, W=8, 64 pages of 16 tokens."""
+    return EffectWorkload(name="commitkv_effect_qwen3_8b_T131072", batch=1, n_layers=1,
+                          n_q_heads=32, n_kv_heads=8, head_dim=128, n_tokens=131072,
+                          seed=BASE_SEED + 5)
+
+
+def commitkv_effect_small(n_q_heads=8, n_kv_heads=2, window=8, n_tokens=1000) -> EffectWorkload:
+    """Two sequences, two layers, a ragged T: parity-sized."""
+    return EffectWorkload(name=f"commitkv_effect_small_H{n_q_heads}_{n_kv_heads}_W{window}",
+                          batch=2, n_layers=2, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads,
+                          head_dim=128, n_tokens=n_tokens, seed=BASE_SEED + 6, window=window,
+                          n_pages=12, heavy_pages=4, lean=6.0, ragged_pages=True)
+
+
+def make_effect_inputs(w: EffectWorkload, device="cpu") -> dict:
+    """K, V [B][L][H_kv][T][d], windows q_minus / q_plus [B][L][H_q][W][d] (bf16),
+    pages page_start / page_len int32 [B][n_pages] (disjoint, ascending), and
+    the heavy page ids of each window (host lists)."""
+    dev = torch.device(device)
+    g = _gen(w.seed, dev)
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    B, L, Hq, Hkv, d, T, W = (w.batch, w.n_layers, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                              w.n_tokens, w.window)
+    G = w.group
+    k = _randn_bf16((B, L, Hkv, T, d), g, dev).float()
+    v = _randn_bf16((B, L, Hkv, T, d), g, dev).float()
+    if w.value_mean > 0:
+        mu = torch.randn((B, L, Hkv, 1, d), generator=g, device=dev)
+        v += mu / mu.norm(dim=-1, keepdim=True) * (w.value_mean * math.sqrt(d))
+    qm = _randn_bf16((B, L, Hq, W, d), g, dev).float()
+    qp = _randn_bf16((B, L, Hq, W, d), g, dev).float()
+
+    P = w.page_len
+    # the ragged layout's last page covers the window rows: random pages end before it
+    slots = ((T - W - 3) if w.ragged_pages else T) // P
+    starts = np.zeros((B, w.n_pages), dtype=np.int32)
+    lens = np.full((B, w.n_pages), P, dtype=np.int32)
+    heavy_minus, heavy_plus = [], []
+    for b in range(B):
+        pick = np.sort(rng.choice(slots, size=w.n_pages, replace=False))
+        starts[b] = pick * P
+        if w.ragged_pages:
+            lens[b, 1] = 5                                # a short page
+            lens[b, 2] = 0                                # an empty slot
+            starts[b, -1] = T - W - 3                     # over the window rows (last page)
+            lens[b, -1] = min(P, W + 3)
+            order = np.argsort(starts[b], kind="stable")
+            starts[b], lens[b] = starts[b][order], lens[b][order]
+        ids = rng.permutation(w.n_pages)
+        n_h = min(w.heavy_pages, w.n_pages // 3)
+        shared = n_h // 3
+        hm = ids[:n_h]
+        hp = np.concatenate([ids[:shared], ids[n_h:2 * n_h - shared]])
+        heavy_minus.append(sorted(int(i) for i in hm))
+        heavy_plus.append(sorted(int(i) for i in hp))
+        # a unit direction per (layer, KV head) and window; heavy pages' keys
+        # and the window's queries both lean along it, and the post-commit
+        # queries lean away from the pre-commit direction
+        for l in range(L):
+            for gk in range(Hkv):
+                dirs = []
+                for q, heavy in ((qm, hm), (qp, hp)):
+                    u = torch.randn(d, generator=g, device=dev)
+                    u = u / u.norm()
+                    dirs.append(u)
+                    q[b, l, gk * G:(gk + 1) * G] += w.lean * u
+                    for pid in heavy:
+                        s0, n0 = int(starts[b, pid]), int(lens[b, pid])
+                        k[b, l, gk, s0:s0 + n0] += w.lean * u
+                qp[b, l, gk * G:(gk + 1) * G] -= w.away * dirs[0]
+    return dict(k_cache=k.to(torch.bfloat16), v_cache=v.to(torch.bfloat16), q_minus=qm.to(torch.bfloat16),
+                q_plus=qp.to(torch.bfloat16), page_start=torch.from_numpy(starts).to(dev),
+                page_len=torch.from_numpy(lens).to(dev), heavy_minus=heavy_minus,
+                heavy_plus=heavy_plus)
