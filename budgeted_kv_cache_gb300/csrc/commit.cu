@@ -54,13 +54,10 @@ constexpr uint32_t kSleepNs = 64;
 
 struct EffSmem {
   uint8_t* q;          // 2 chunks x 128 rows x 128 B
-  uint8_t* k;          // nk stages x kTile
-  uint8_t* v;          // nv stages x kTile
+  uint8_t* k;          // ring of n_stages tiles, key and value tiles alike
   uint8_t* p;          // [2 buffers][2 parts][2 chunks][Rp rows][128 B]
-  uint64_t* kfull;
-  uint64_t* kempty;
-  uint64_t* vfull;
-  uint64_t* vempty;
+  uint64_t* kfull;     // [n_stages]
+  uint64_t* kempty;    // [n_stages]
   uint64_t* tfull;     // [2]
   uint64_t* tempty;    // [2]
   uint64_t* pfull;     // [2]
@@ -76,18 +73,15 @@ struct EffSmem {
   float* sl;           // [128] pass-1 sum per TMEM lane
 };
 
-__device__ __forceinline__ EffSmem eff_carve(uint8_t* base, int Rp, int nk, int nv) {
+__device__ __forceinline__ EffSmem eff_carve(uint8_t* base, int Rp, int ns) {
   EffSmem s;
   s.q = base;
   s.k = s.q + 2 * kChunk;
-  s.v = s.k + nk * kTile;
-  s.p = s.v + nv * kTile;
+  s.p = s.k + ns * kTile;
   uint64_t* b = reinterpret_cast<uint64_t*>(s.p + 8 * Rp * 128);
   s.kfull = b;
-  s.kempty = b + nk;
-  s.vfull = b + 2 * nk;
-  s.vempty = b + 2 * nk + nv;
-  b += 2 * nk + 2 * nv;
+  s.kempty = b + ns;
+  b += 2 * ns;
   s.tfull = b;
   s.tempty = b + 2;
   s.pfull = b + 4;
@@ -140,7 +134,8 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
                    const __grid_constant__ CUtensorMap tmap_q, const EffectArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const EffSmem s = eff_carve(base, a.Rp, a.nk, a.nv);
+  const EffSmem s = eff_carve(base, a.Rp, a.nk);
+  const uint32_t NS = static_cast<uint32_t>(a.nk);
   constexpr int kRep = 128 / S;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -151,10 +146,6 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
     for (int i = 0; i < a.nk; ++i) {
       mbar_init(smem_u32(&s.kfull[i]), 1);
       mbar_init(smem_u32(&s.kempty[i]), 1);
-    }
-    for (int i = 0; i < a.nv; ++i) {
-      mbar_init(smem_u32(&s.vfull[i]), 1);
-      mbar_init(smem_u32(&s.vempty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.tfull[i]), 1);
@@ -192,58 +183,55 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
   tc_fence_after();
   const uint32_t tmem_base = *s.tmem_slot;
   const int SP = a.splits;
+  // a contiguous range of items per CTA, so that consecutive items mostly
+  // share a unit and its window queries stay in shared memory
+  const int it0 = static_cast<int>(static_cast<int64_t>(a.n_items) * blockIdx.x / gridDim.x);
+  const int it1 = static_cast<int>(static_cast<int64_t>(a.n_items) * (blockIdx.x + 1) / gridDim.x);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();
       const uint64_t stream = l2_policy_evict_first();
-      uint32_t jk = 0, jv = 0;
-      int li = 0, q_loads = 0;
+      uint32_t jr = 0;           // ring loads issued (key tiles of both passes, value tiles of pass 2)
+      int q_loads = 0, prev_u = -1;
       bool ok = true;
-      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++li) {
+      for (int it = it0; it < it1 && ok; ++it) {
         const int u = it / SP, c = it % SP;
         const int t0 = c * a.chunk_tiles;
         const int nt = min(a.chunk_tiles, a.n_tiles - t0);
-        if (li > 0 && !mbar_wait_backoff(smem_u32(s.qempty), (li - 1) & 1, abort_flag, kSleepNs)) break;
-        mbar_arrive_expect_tx(smem_u32(s.qfull), static_cast<uint32_t>(kRep * 2 * a.R * 128));
-        for (int rk = 0; rk < kRep; ++rk)
-          for (int kc = 0; kc < 2; ++kc)
-            tma_load_3d(smem_u32(s.q + kc * kChunk + rk * S * 128), &tmap_q, smem_u32(s.qfull), kc * 64,
-                        0, u, keep);
-        ++q_loads;
-        for (int pass = 0; pass < 2 && ok; ++pass) {
-          for (int t = 0; t < nt; ++t) {
-            const uint32_t sk = jk % a.nk, pk = (jk / a.nk) & 1;
-            if (!mbar_wait_backoff(smem_u32(&s.kempty[sk]), pk ^ 1, abort_flag, kSleepNs)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(smem_u32(&s.kfull[sk]), kTile);
+        if (u != prev_u) {
+          // a new unit: its queries replace the previous unit's once every MMA reading them is done
+          if (q_loads > 0 && !mbar_wait_backoff(smem_u32(s.qempty), (q_loads - 1) & 1, abort_flag, kSleepNs))
+            break;
+          mbar_arrive_expect_tx(smem_u32(s.qfull), static_cast<uint32_t>(kRep * 2 * a.R * 128));
+          for (int rk = 0; rk < kRep; ++rk)
             for (int kc = 0; kc < 2; ++kc)
-              tma_load_3d(smem_u32(s.k + sk * kTile + kc * kChunk), &tmap_k, smem_u32(&s.kfull[sk]),
-                          kc * 64, (t0 + t) * kTileTokens, u, pass == 0 ? keep : stream);
-            ++jk;
-            if (pass == 1) {
-              const uint32_t sv = jv % a.nv, pv = (jv / a.nv) & 1;
-              if (!mbar_wait_backoff(smem_u32(&s.vempty[sv]), pv ^ 1, abort_flag, kSleepNs)) {
+              tma_load_3d(smem_u32(s.q + kc * kChunk + rk * S * 128), &tmap_q, smem_u32(s.qfull),
+                          kc * 64, 0, u, keep);
+          ++q_loads;
+          prev_u = u;
+        }
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+          for (int t = 0; t < nt && ok; ++t) {
+            for (int kv = 0; kv <= pass; ++kv) {          // pass 1: the key tile; pass 2: key, value
+              const uint32_t st = jr % NS, ph = (jr / NS) & 1;
+              if (!mbar_wait_backoff(smem_u32(&s.kempty[st]), ph ^ 1, abort_flag, kSleepNs)) {
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(smem_u32(&s.vfull[sv]), kTile);
+              mbar_arrive_expect_tx(smem_u32(&s.kfull[st]), kTile);
               for (int kc = 0; kc < 2; ++kc)
-                tma_load_3d(smem_u32(s.v + sv * kTile + kc * kChunk), &tmap_v, smem_u32(&s.vfull[sv]),
-                            kc * 64, (t0 + t) * kTileTokens, u, stream);
-              ++jv;
+                tma_load_3d(smem_u32(s.k + st * kTile + kc * kChunk), kv ? &tmap_v : &tmap_k,
+                            smem_u32(&s.kfull[st]), kc * 64, (t0 + t) * kTileTokens, u,
+                            (pass == 0) ? keep : stream);
+              ++jr;
             }
           }
         }
       }
       // every copy issued above lands before the CTA exits
-      for (uint32_t j = jk > static_cast<uint32_t>(a.nk) ? jk - a.nk : 0; j < jk; ++j)
-        eff_drain(smem_u32(&s.kfull[j % a.nk]), (j / a.nk) & 1);
-      for (uint32_t j = jv > static_cast<uint32_t>(a.nv) ? jv - a.nv : 0; j < jv; ++j)
-        eff_drain(smem_u32(&s.vfull[j % a.nv]), (j / a.nv) & 1);
+      for (uint32_t j = jr > NS ? jr - NS : 0; j < jr; ++j) eff_drain(smem_u32(&s.kfull[j % NS]), (j / NS) & 1);
       if (q_loads > 0) eff_drain(smem_u32(s.qfull), (q_loads - 1) & 1);
     }
   } else if (warp == 1) {
@@ -253,18 +241,20 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
       const uint32_t idesc2 = mma_idesc_bf16(128, a.Rp) | (1u << 15);   // A (values) MN-major
       const uint64_t qdesc0 = sw128_desc(smem_u32(s.q));
       const uint64_t kdesc0 = sw128_desc(smem_u32(s.k));
-      const uint64_t vdesc0 = sw128_mn_desc(smem_u32(s.v), kChunk);
+      const uint64_t vdesc0 = sw128_mn_desc(smem_u32(s.k), kChunk);
       const uint64_t pdesc0 = sw128_desc(smem_u32(s.p));
       const uint32_t pchunk16 = (static_cast<uint32_t>(a.Rp) * 128u) >> 4;
-      uint32_t jk = 0, jv = 0, jt = 0, jp = 0;
-      int li = 0;
+      uint32_t jr = 0, jt = 0, jp = 0;
+      uint32_t vslot0 = 0, vslot1 = 0;   // ring index of the value tile of even / odd pass-2 tiles
+      int li = 0, q_segs = 0, prev_u = -1;
       bool ok = true;
-      // MMA2 of pass-2 tile `tile` (P in buffer jp % 2, values in stage jv % nv)
+      // MMA2 of pass-2 tile `tile` (P in buffer jp % 2, values at ring index vslot[tile % 2])
       auto mma2 = [&](int tile) -> bool {
         const uint32_t pb = jp & 1, pph = (jp >> 1) & 1;
-        const uint32_t sv = jv % a.nv, pv = (jv / a.nv) & 1;
+        const uint32_t jv = (tile & 1) ? vslot1 : vslot0;
+        const uint32_t sv = jv % NS, pv = (jv / NS) & 1;
         if (!mbar_wait_backoff(smem_u32(&s.pfull[pb]), pph, abort_flag, kSleepNs) ||
-            !mbar_wait_backoff(smem_u32(&s.vfull[sv]), pv, abort_flag, kSleepNs))
+            !mbar_wait_backoff(smem_u32(&s.kfull[sv]), pv, abort_flag, kSleepNs))
           return false;
         if (tile == 0 && li > 0 &&
             !mbar_wait_backoff(smem_u32(s.d2empty), (li - 1) & 1, abort_flag, kSleepNs))
@@ -281,21 +271,25 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
             tc_mma_bf16(tmem_base + kD2Col, ad, bd, idesc2, (tile > 0 || ks > 0 || part > 0) ? 1u : 0u);
           }
         }
-        tc_commit(smem_u32(&s.vempty[sv]));
+        tc_commit(smem_u32(&s.kempty[sv]));
         tc_commit(smem_u32(&s.pempty[pb]));
-        ++jv;
         ++jp;
         return true;
       };
-      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, ++li) {
-        const int c = it % SP;
+      for (int it = it0; it < it1 && ok; ++it, ++li) {
+        const int u = it / SP, c = it % SP;
         const int t0 = c * a.chunk_tiles;
         const int nt = min(a.chunk_tiles, a.n_tiles - t0);
-        if (!mbar_wait_backoff(smem_u32(s.qfull), li & 1, abort_flag, kSleepNs)) break;
+        if (u != prev_u) {
+          if (q_segs > 0) tc_commit(smem_u32(s.qempty));   // the previous unit's queries are done with
+          if (!mbar_wait_backoff(smem_u32(s.qfull), q_segs & 1, abort_flag, kSleepNs)) break;
+          ++q_segs;
+          prev_u = u;
+        }
         tc_fence_after();
         for (int pass = 0; pass < 2 && ok; ++pass) {
           for (int t = 0; t < nt; ++t) {
-            const uint32_t sk = jk % a.nk, pk = (jk / a.nk) & 1;
+            const uint32_t sk = jr % NS, pk = (jr / NS) & 1;
             const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
             if (!mbar_wait_backoff(smem_u32(&s.kfull[sk]), pk, abort_flag, kSleepNs) ||
                 !mbar_wait_backoff(smem_u32(&s.tempty[tb]), tph ^ 1, abort_flag, kSleepNs)) {
@@ -312,13 +306,17 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
             }
             tc_commit(smem_u32(&s.kempty[sk]));
             tc_commit(smem_u32(&s.tfull[tb]));
-            ++jk;
+            ++jr;
             ++jt;
+            if (pass == 1) {                         // the value tile follows its key tile in the ring
+              if (t & 1) vslot1 = jr;
+              else vslot0 = jr;
+              ++jr;
+            }
             if (pass == 1 && t > 0 && !mma2(t - 1)) ok = false;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(s.qempty));
         if (!mma2(nt - 1)) break;
         tc_commit(smem_u32(s.d2full));
       }
@@ -343,7 +341,7 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
     int li = 0;
     bool fail = false;
     int cur_u = -1;
-    for (int it = blockIdx.x; it < a.n_items; it += gridDim.x, ++li) {
+    for (int it = it0; it < it1; ++it, ++li) {
       const int u = it / SP, c = it % SP;
       const int t0 = c * a.chunk_tiles;
       const int nt = min(a.chunk_tiles, a.n_tiles - t0);
@@ -475,43 +473,107 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
 
 // PASK Eq. 15 over the work items of a unit: o = sum_c 2^(m_c - M) u_c /
 // sum_c 2^(m_c - M) l_c, and the natural-log denominator lse = (M + log2 den) ln 2.
-// One block per (unit, row), thread = dimension.
+// One block per (unit, row); each lane owns four dimensions, the four warps
+// take every fourth item and meet in shared memory.
 __global__ void __launch_bounds__(128) effect_merge_kernel(const EffectArgs a) {
+  __shared__ float red[4];
+  __shared__ float4 part[4][32];
+  __shared__ float s_M, s_den;
   const int u = blockIdx.x / a.R, r = blockIdx.x % a.R;
-  const int d = threadIdx.x;
-  const float2* ml = a.part_ml + static_cast<int64_t>(u) * a.splits * a.R + r;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int SP = a.splits;
+  const float2* ml = a.part_ml + static_cast<int64_t>(u) * SP * a.R + r;
   float M = -INFINITY;
-  for (int c = 0; c < a.splits; ++c) M = fmaxf(M, ml[static_cast<int64_t>(c) * a.R].x);
-  float den = 0.f, num = 0.f;
-  for (int c = 0; c < a.splits; ++c) {
+  for (int c = tid; c < SP; c += 128) M = fmaxf(M, ml[static_cast<int64_t>(c) * a.R].x);
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  if (tid == 0) s_M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  M = s_M;
+  float den = 0.f;
+  for (int c = tid; c < SP; c += 128) {
     const float2 st = ml[static_cast<int64_t>(c) * a.R];
-    if (st.x == -INFINITY) continue;                  // an empty partition contributes nothing
-    const float f = ex2_approx(st.x - M);
-    den += f * st.y;
-    num += f * a.part_u[((static_cast<int64_t>(u) * a.splits + c) * a.R + r) * 128 + d];
+    if (st.x != -INFINITY) den += ex2_approx(st.x - M) * st.y;   // empty partitions add nothing
   }
-  a.o[(static_cast<int64_t>(u) * a.R + r) * 128 + d] = num / den;
-  if (d == 0) a.lse[static_cast<int64_t>(u) * a.R + r] = (M + log2f(den)) * 0.69314718055994531f;
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
+  __syncthreads();
+  if (lane == 0) red[warp] = den;
+  const float4* pu = reinterpret_cast<const float4*>(a.part_u + (static_cast<int64_t>(u) * SP * a.R + r) * 128) + lane;
+  const int64_t cstride = static_cast<int64_t>(a.R) * 32;       // float4 units between items
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  int c = warp;
+  for (; c + 12 < SP; c += 16) {
+    float4 v4[4];
+    float f4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float mc = ml[static_cast<int64_t>(c + 4 * i) * a.R].x;
+      f4[i] = mc == -INFINITY ? 0.f : ex2_approx(mc - M);
+      v4[i] = pu[(c + 4 * i) * cstride];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      num.x = fmaf(f4[i], v4[i].x, num.x);
+      num.y = fmaf(f4[i], v4[i].y, num.y);
+      num.z = fmaf(f4[i], v4[i].z, num.z);
+      num.w = fmaf(f4[i], v4[i].w, num.w);
+    }
+  }
+  for (; c < SP; c += 4) {
+    const float mc = ml[static_cast<int64_t>(c) * a.R].x;
+    if (mc == -INFINITY) continue;
+    const float f = ex2_approx(mc - M);
+    const float4 v = pu[c * cstride];
+    num.x = fmaf(f, v.x, num.x);
+    num.y = fmaf(f, v.y, num.y);
+    num.z = fmaf(f, v.z, num.z);
+    num.w = fmaf(f, v.w, num.w);
+  }
+  part[warp][lane] = num;
+  __syncthreads();
+  if (tid == 0) s_den = (red[0] + red[1]) + (red[2] + red[3]);
+  if (warp == 0) {
+    float4 t = part[0][lane];
+#pragma unroll
+    for (int w2 = 1; w2 < 4; ++w2) {
+      t.x += part[w2][lane].x;
+      t.y += part[w2][lane].y;
+      t.z += part[w2][lane].z;
+      t.w += part[w2][lane].w;
+    }
+    part[0][lane] = t;
+  }
+  __syncthreads();
+  den = s_den;
+  if (warp == 0) {
+    const float4 t = part[0][lane];
+    reinterpret_cast<float4*>(a.o + (static_cast<int64_t>(u) * a.R + r) * 128)[lane] =
+        make_float4(t.x / den, t.y / den, t.z / den, t.w / den);
+  }
+  if (tid == 0) a.lse[static_cast<int64_t>(u) * a.R + r] = (M + log2f(den)) * 0.69314718055994531f;
 }
 
-// Page weights, value sums and Eq. 7 ratios: one block per (page, unit).
+// Page weights, value sums and Eq. 7 ratios: one block per (page, unit), one
+// warp per window row at a time (rows r = warp, warp + 8, ...): the row's
+// logits over the page's keys (lane = key), its weights and their sum, its
+// value sum (lane = four dimensions) and the ratio, all inside the warp.
 constexpr int kMaxPage = 64;
 constexpr int kMaxRows = 64;
+constexpr int kPageThreads = 256;
 
 size_t page_smem_bytes() {
-  return static_cast<size_t>(kMaxRows + 2 * kMaxPage) * 128 * 2 + kMaxRows * kMaxPage * 4 +
-         2 * 4 * kMaxRows * 4;
+  return static_cast<size_t>(kMaxRows + 2 * kMaxPage) * 128 * 2;   // q, k, v rows (bf16)
 }
 
-__global__ void __launch_bounds__(128) effect_page_kernel(const EffectArgs a) {
+__global__ void __launch_bounds__(kPageThreads) effect_page_kernel(const EffectArgs a) {
   extern __shared__ uint8_t psm_raw[];
   __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(psm_raw);             // [R][128]
   __nv_bfloat16* ks = qs + kMaxRows * 128;                                    // [len][128]
   __nv_bfloat16* vs = ks + kMaxPage * 128;                                    // [len][128]
-  float* aw = reinterpret_cast<float*>(vs + kMaxPage * 128);                  // [R][len]
-  float* red_n = aw + kMaxRows * kMaxPage;                                    // [4][R]
-  float* red_o = red_n + 4 * kMaxRows;                                        // [4][R]
-  __shared__ float wmax[4];
+  __shared__ float wmax[kPageThreads / 32];
   const int p = blockIdx.x, u = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int per_b = a.L * a.Hkv;
@@ -523,7 +585,7 @@ __global__ void __launch_bounds__(128) effect_page_kernel(const EffectArgs a) {
   const bool bad = len < 0 || len > kMaxPage || start < 0 || static_cast<int64_t>(start) + len > a.T;
   if (bad || len == 0) {
     // an empty or malformed page deletes nothing: s = 0, u = 0, no ratio
-    for (int r = 0; r < R; ++r) a.u[(row0 + r) * 128 + tid] = 0.f;
+    for (int i = tid; i < R * 128; i += kPageThreads) a.u[row0 * 128 + i] = 0.f;
     if (tid < R) a.s[row0 + tid] = 0.f;
     if (bad && tid == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
     return;
@@ -531,83 +593,85 @@ __global__ void __launch_bounds__(128) effect_page_kernel(const EffectArgs a) {
   {
     const uint4* qg = reinterpret_cast<const uint4*>(a.q + static_cast<int64_t>(u) * R * 128);
     uint4* q4 = reinterpret_cast<uint4*>(qs);
-    for (int i = tid; i < R * 16; i += 128) q4[i] = __ldg(qg + i);
+    for (int i = tid; i < R * 16; i += kPageThreads) q4[i] = __ldg(qg + i);
     const int64_t off = (static_cast<int64_t>(u) * a.T + start) * 128;
     const uint4* kg = reinterpret_cast<const uint4*>(a.k + off);
     const uint4* vg = reinterpret_cast<const uint4*>(a.v + off);
     uint4* k4 = reinterpret_cast<uint4*>(ks);
     uint4* v4 = reinterpret_cast<uint4*>(vs);
-    for (int i = tid; i < len * 16; i += 128) {
+    for (int i = tid; i < len * 16; i += kPageThreads) {
       k4[i] = __ldg(kg + i);
       v4[i] = __ldg(vg + i);
     }
   }
   __syncthreads();
-  // a_rj = exp2(z_rj * scale_log2 - lse_r log2 e) for visible j, else 0
-  const float l2e = 1.4426950408889634f;
-  for (int e = tid; e < R * len; e += 128) {
-    const int r = e / len, i = e % len;
+  const int64_t last0 = a.T - a.W;          // row w sees indices <= last0 + w
+  float mx = 0.f;
+  for (int r = warp; r < R; r += kPageThreads / 32) {
+    const float lse2 = a.lse[static_cast<int64_t>(u) * R + r] * 1.4426950408889634f;
+    const int64_t last = last0 + (r % a.W);
     const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(qs + r * 128);
-    const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(ks + i * 128);
-    float z = 0.f;
+    // weights of keys lane and lane + 32; each lane starts its dot product at
+    // a different pair, so the 256-byte-strided key rows hit different banks
+    float aw[2] = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lane + 32 * h;
+      if (i < len && static_cast<int64_t>(start) + i <= last) {
+        const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(ks + i * 128);
+        float z0 = 0.f, z1 = 0.f;
 #pragma unroll 8
-    for (int t = 0; t < 64; ++t) {
-      const float2 qf = __bfloat1622float2(q2[t]);
-      const float2 kf = __bfloat1622float2(k2[t]);
-      z = fmaf(qf.x, kf.x, z);
-      z = fmaf(qf.y, kf.y, z);
+        for (int t = 0; t < 64; ++t) {
+          const int tt = (t + lane) & 63;
+          const float2 qf = __bfloat1622float2(q2[tt]);
+          const float2 kf = __bfloat1622float2(k2[tt]);
+          z0 = fmaf(qf.x, kf.x, z0);
+          z1 = fmaf(qf.y, kf.y, z1);
+        }
+        aw[h] = ex2_approx((z0 + z1) * a.scale_log2 - lse2);
+      }
     }
-    const int64_t j = static_cast<int64_t>(start) + i;
-    const bool vis = j <= a.T - a.W + (r % a.W);
-    const float lse2 = a.lse[static_cast<int64_t>(u) * R + r] * l2e;
-    aw[r * kMaxPage + i] = vis ? ex2_approx(z * a.scale_log2 - lse2) : 0.f;
-  }
-  __syncthreads();
-  // thread = dimension d: u_r[d], and the parts of ||u_r - s_r o_r||^2 and ||o_r||^2
-  const int d = tid;
-  for (int r = 0; r < R; ++r) {
-    float sr = 0.f, ur = 0.f;
+    float sr = aw[0] + aw[1];
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, o2);
+    // value sum: lane owns dimensions 4 lane .. 4 lane + 3
+    float4 ur = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i = 0; i < len; ++i) {
-      const float w = aw[r * kMaxPage + i];
-      sr += w;
-      ur = fmaf(w, __bfloat162float(vs[i * 128 + d]), ur);
+      const float w = __shfl_sync(0xffffffffu, aw[i >> 5], i & 31);
+      const uint2 vv = *reinterpret_cast<const uint2*>(vs + i * 128 + 4 * lane);
+      const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv.x));
+      const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv.y));
+      ur.x = fmaf(w, v01.x, ur.x);
+      ur.y = fmaf(w, v01.y, ur.y);
+      ur.z = fmaf(w, v23.x, ur.z);
+      ur.w = fmaf(w, v23.y, ur.w);
     }
-    const float od = a.o[(static_cast<int64_t>(u) * R + r) * 128 + d];
-    const float df = ur - sr * od;
-    float nn = df * df, oo = od * od;
+    const float4 od = reinterpret_cast<const float4*>(a.o + (static_cast<int64_t>(u) * R + r) * 128)[lane];
+    const float dx = ur.x - sr * od.x, dy = ur.y - sr * od.y, dz = ur.z - sr * od.z, dw = ur.w - sr * od.w;
+    float nn = dx * dx + dy * dy + dz * dz + dw * dw;
+    float oo = od.x * od.x + od.y * od.y + od.z * od.z + od.w * od.w;
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) {
       nn += __shfl_xor_sync(0xffffffffu, nn, o2);
       oo += __shfl_xor_sync(0xffffffffu, oo, o2);
     }
-    if (lane == 0) {
-      red_n[warp * kMaxRows + r] = nn;
-      red_o[warp * kMaxRows + r] = oo;
-    }
-    a.u[(row0 + r) * 128 + d] = ur;
-    if (d == 0) a.s[row0 + r] = sr;
-  }
-  __syncthreads();
-  float ratio = 0.f;
-  if (tid < R) {
-    float sr = 0.f;
-    for (int i = 0; i < len; ++i) sr += aw[tid * kMaxPage + i];
-    const float nn = red_n[tid] + red_n[kMaxRows + tid] + red_n[2 * kMaxRows + tid] + red_n[3 * kMaxRows + tid];
-    const float oo = red_o[tid] + red_o[kMaxRows + tid] + red_o[2 * kMaxRows + tid] + red_o[3 * kMaxRows + tid];
+    reinterpret_cast<float4*>(a.u + (row0 + r) * 128)[lane] = ur;
+    if (lane == 0) a.s[row0 + r] = sr;
     const float om = 1.f - sr;
+    float ratio;
     if (om <= 0.f) ratio = INFINITY;
     else if (oo == 0.f) ratio = nn == 0.f ? 0.f : INFINITY;
     else ratio = sqrtf(nn) / (om * sqrtf(oo));
+    mx = fmaxf(mx, ratio);
   }
-#pragma unroll
-  for (int o2 = 16; o2 > 0; o2 >>= 1) ratio = fmaxf(ratio, __shfl_xor_sync(0xffffffffu, ratio, o2));
-  if (lane == 0) wmax[warp] = ratio;
+  if (lane == 0) wmax[warp] = mx;
   __syncthreads();
   if (tid == 0) {
-    const float mx = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    float m = 0.f;
+    for (int w2 = 0; w2 < kPageThreads / 32; ++w2) m = fmaxf(m, wmax[w2]);
     // ratios are >= 0, so their bit patterns order like the values
     atomicMax(reinterpret_cast<int*>(a.effect + static_cast<int64_t>(b * a.L + l) * a.n_pages + p),
-              __float_as_int(mx));
+              __float_as_int(m));
   }
 }
 
@@ -795,9 +859,9 @@ __global__ void __launch_bounds__(64) flags_kernel(const FlagArgs a) {
 
 }  // namespace
 
-size_t effect_smem_bytes(int Rp, int nk, int nv) {
-  return static_cast<size_t>(2 * kChunk) + static_cast<size_t>(nk + nv) * kTile +
-         static_cast<size_t>(8) * Rp * 128 + static_cast<size_t>(2 * nk + 2 * nv + 13) * 8 + 16 +
+size_t effect_smem_bytes(int Rp, int n_stages) {
+  return static_cast<size_t>(2 * kChunk) + static_cast<size_t>(n_stages) * kTile +
+         static_cast<size_t>(8) * Rp * 128 + static_cast<size_t>(2 * n_stages + 13) * 8 + 16 +
          2 * 128 * 4 + 1024;
 }
 
@@ -816,7 +880,7 @@ cudaError_t launch_effect(const EffectArgs& a, const CUtensorMap& tmap_k, const 
   if ((err = cudaFuncSetAttribute(effect_page_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(psm))) != cudaSuccess)
     return err;
-  if (a.n_pages > 0) effect_page_kernel<<<dim3(a.n_pages, a.U), 128, psm, stream>>>(a);
+  if (a.n_pages > 0) effect_page_kernel<<<dim3(a.n_pages, a.U), kPageThreads, psm, stream>>>(a);
   return cudaGetLastError();
 }
 

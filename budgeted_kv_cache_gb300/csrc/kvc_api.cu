@@ -240,10 +240,16 @@ kvc_status plan_effect(const kvc_shape* s, int32_t window, EffectPlan* p) {
   if (items > 0x7fffffffLL || U * p->R > 0x7fffffffLL || U > 65535) return KVC_ERR_UNSUPPORTED;
   p->n_items = static_cast<int>(items);
   p->grid = static_cast<int>(std::min<int64_t>(items, info.sms));
-  p->nk = 2;
-  p->nv = p->Rp <= 32 ? 3 : 2;
-  p->smem = effect_smem_bytes(p->Rp, p->nk, p->nv);
-  if (p->smem > 232448) return KVC_ERR_UNSUPPORTED;
+  // as many 32 KB key / value stages as fit beside the queries and P buffers
+  p->nk = 0;
+  for (int ns = 8; ns >= 2; --ns)
+    if (effect_smem_bytes(p->Rp, ns) <= 232448) {
+      p->nk = ns;
+      break;
+    }
+  if (p->nk == 0) return KVC_ERR_UNSUPPORTED;
+  p->nv = 0;
+  p->smem = effect_smem_bytes(p->Rp, p->nk);
   p->ws_part_u = (static_cast<size_t>(items) * p->R * 128 * 4 + 255) / 256 * 256;
   p->ws_total = p->ws_part_u + (static_cast<size_t>(items) * p->R * 8 + 255) / 256 * 256;
   return KVC_OK;

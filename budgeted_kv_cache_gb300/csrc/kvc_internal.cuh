@@ -124,7 +124,7 @@ struct EffectArgs {
   int32_t U, L, Hkv, B, G, W, R, Rp;
   int64_t T;
   int32_t n_tiles, chunk_tiles, splits, n_items;
-  int32_t nk, nv;              // key / value stage counts
+  int32_t nk, nv;              // nk: tiles in the key / value stage ring; nv unused
   float scale_log2;            // softmax scale * log2(e)
   float* part_u;               // [n_items][R][128] unnormalised value sums of a split
   float2* part_ml;             // [n_items][R] (max, exp2-sum) of y = z * scale_log2
@@ -191,7 +191,7 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes);
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
-size_t effect_smem_bytes(int Rp, int nk, int nv);
+size_t effect_smem_bytes(int Rp, int n_stages);
 cudaError_t launch_effect(const EffectArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                           const CUtensorMap& tmap_q, int grid, size_t smem_bytes, cudaStream_t stream);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
