@@ -227,6 +227,55 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def commitkv_stage(dev, stream, flush, repeats: int = 10) -> dict:
+    """CommitKV (Sec. 3.2-3.3): deletion effects of 64 pages over the
+    post-commit window of one layer (Qwen3-8B heads, T = 131072, W = 8) and the
+    commit call (states + greedy joint validation), each timed after three
+    warm-ups as the mean of `repeats` calls with L2 flushed before each."""
+    import budgeted_kv_cache_gb300 as kvc_mod
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    we = wl.commitkv_effect_128k()
+    xe = wl.make_effect_inputs(we, dev)
+    es = kvc_mod.make_shape(we.batch, we.n_layers, we.n_q_heads, we.n_kv_heads, 128, we.n_tokens)
+    ews = torch.empty(kvc_mod.kvc_deletion_effect_workspace_bytes(es, we.window), dtype=torch.uint8,
+                      device=dev)
+    rec_m = kvc_mod.EffectRecord(es, we.window, we.n_pages, dev)
+    rec_p = kvc_mod.EffectRecord(es, we.window, we.n_pages, dev)
+    eff_m = torch.empty((we.batch, we.n_layers, we.n_pages), device=dev)
+    eff_p = torch.empty_like(eff_m)
+    cws = torch.empty(kvc_mod.kvc_commit_workspace_bytes(es, we.window), dtype=torch.uint8, device=dev)
+    cmp_ = torch.ones((we.batch, we.n_pages), dtype=torch.uint8, device=dev)
+    st_ = torch.empty((we.batch, we.n_pages), dtype=torch.uint8, device=dev)
+    rt_ = torch.empty_like(st_)
+    kvc_mod.kvc_deletion_effect(es, xe["k_cache"], xe["v_cache"], xe["q_minus"], we.window, 0.0,
+                                xe["page_start"], xe["page_len"], eff_m, rec_m, ews, stream=stream)
+    fns = {
+        "commitkv_effect": lambda: kvc_mod.kvc_deletion_effect(
+            es, xe["k_cache"], xe["v_cache"], xe["q_plus"], we.window, 0.0, xe["page_start"],
+            xe["page_len"], eff_p, rec_p, ews, stream=stream),
+        "commitkv_commit": lambda: kvc_mod.kvc_commit_transition(
+            es, we.window, 0, eff_m, eff_p, cmp_, rec_p, st_, rt_, cws, stream=stream),
+    }
+    out = {}
+    for name, fn in fns.items():
+        for _ in range(3):
+            fn()
+        t_v = []
+        for _ in range(repeats):
+            flush.fill_(1)
+            d0, d1 = ev(), ev()
+            d0.record(stream)
+            fn()
+            d1.record(stream)
+            torch.cuda.synchronize()
+            t_v.append(d0.elapsed_time(d1))
+        out[name] = statistics.mean(t_v)
+    kv_bytes = 2 * we.n_units * we.n_tokens * 128 * 2
+    out["commitkv_effect_gbs"] = kv_bytes / (out["commitkv_effect"] * 1e-3) / 1e9
+    out["commitkv_retired_pages"] = int(rt_.sum().item())
+    return out
+
+
 # ---------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, w, world, rank, local):
@@ -390,52 +439,8 @@ def run_gpu(args, w, world, rank, local):
         t_cref = statistics.mean(t_c)
         del rk_out, rp_out
 
-    # CommitKV (Sec. 3.2-3.3), timed separately: deletion effects of 64 pages
-    # over the post-commit window of one layer (Qwen3-8B heads, T = 131072,
-    # W = 8) and the commit call (states + greedy joint validation)
-    t_eff = None
-    if not args.no_commitkv:
-        import budgeted_kv_cache_gb300 as kvc_mod
-        we = wl.commitkv_effect_128k()
-        xe = wl.make_effect_inputs(we, dev)
-        es = kvc_mod.make_shape(we.batch, we.n_layers, we.n_q_heads, we.n_kv_heads, 128, we.n_tokens)
-        ews = torch.empty(kvc_mod.kvc_deletion_effect_workspace_bytes(es, we.window), dtype=torch.uint8,
-                          device=dev)
-        rec_m = kvc_mod.EffectRecord(es, we.window, we.n_pages, dev)
-        rec_p = kvc_mod.EffectRecord(es, we.window, we.n_pages, dev)
-        eff_m = torch.empty((we.batch, we.n_layers, we.n_pages), device=dev)
-        eff_p = torch.empty_like(eff_m)
-        cws = torch.empty(kvc_mod.kvc_commit_workspace_bytes(es, we.window), dtype=torch.uint8, device=dev)
-        cmp_ = torch.ones((we.batch, we.n_pages), dtype=torch.uint8, device=dev)
-        st_ = torch.empty((we.batch, we.n_pages), dtype=torch.uint8, device=dev)
-        rt_ = torch.empty_like(st_)
-        kvc_mod.kvc_deletion_effect(es, xe["k_cache"], xe["v_cache"], xe["q_minus"], we.window, 0.0,
-                                    xe["page_start"], xe["page_len"], eff_m, rec_m, ews, stream=stream)
-        fns = {
-            "commitkv_effect": lambda: kvc_mod.kvc_deletion_effect(
-                es, xe["k_cache"], xe["v_cache"], xe["q_plus"], we.window, 0.0, xe["page_start"],
-                xe["page_len"], eff_p, rec_p, ews, stream=stream),
-            "commitkv_commit": lambda: kvc_mod.kvc_commit_transition(
-                es, we.window, 0, eff_m, eff_p, cmp_, rec_p, st_, rt_, cws, stream=stream),
-        }
-        t_eff = {}
-        for name, fn in fns.items():
-            for _ in range(3):
-                fn()
-            t_v = []
-            for _ in range(10):
-                flush.fill_(1)
-                d0, d1 = ev(), ev()
-                d0.record(stream)
-                fn()
-                d1.record(stream)
-                torch.cuda.synchronize()
-                t_v.append(d0.elapsed_time(d1))
-            t_eff[name] = statistics.mean(t_v)
-        kv_bytes = 2 * we.n_units * we.n_tokens * 128 * 2
-        t_eff["commitkv_effect_gbs"] = kv_bytes / (t_eff["commitkv_effect"] * 1e-3) / 1e9
-        t_eff["commitkv_retired_pages"] = int(rt_.sum().item())
-        del xe, ews, rec_m, rec_p, eff_m, eff_p, cws
+    # CommitKV (Sec. 3.2-3.3), timed separately
+    t_eff = None if args.no_commitkv else commitkv_stage(dev, stream, flush)
 
     # end to end through the C-ABI with host buffers: pinned host inputs are
     # copied in, the pass runs, the compacted cache comes back, every step
@@ -536,6 +541,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-commitkv", action="store_true",
                     help="skip the CommitKV deletion-effect and commit stages")
+    ap.add_argument("--commitkv-only", action="store_true",
+                    help="run only the CommitKV stages (one GPU) and print their timings")
     ap.add_argument("--layers", type=int, default=0,
                     help="use only this many layers of the workload (small profiling case)")
     args = ap.parse_args()
@@ -545,7 +552,20 @@ def main():
     if args.layers > 0:
         w = w.replace(n_layers=min(args.layers, w.n_layers),
                       name=f"{w.name}_{min(args.layers, w.n_layers)}layers")
-    if args.impl == "reference":
+    if args.commitkv_only:
+        # the CommitKV stages alone (a small profiling case: one layer, 0.5 GB)
+        import budgeted_kv_cache_gb300 as kvc
+        from budgeted_kv_cache_gb300 import build
+        build.build()
+        kvc.library()
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        out = commitkv_stage(dev, torch.cuda.current_stream(dev), flush, repeats=args.steps)
+        if rank == 0:
+            print(json.dumps({"stage": "commitkv", "workload": wl.commitkv_effect_128k().name,
+                              "stages_ms": out}), flush=True)
+    elif args.impl == "reference":
         run_reference(args, w, world, rank)
     else:
         run_gpu(args, w, world, rank, local)
