@@ -1042,3 +1042,44 @@ def commit_flags(n_tokens: int, pages, retire, protect, flags=None) -> np.ndarra
         elif retire[p]:
             out[s:s + ln] = (out[s:s + ln] & ~np.uint8(FLAG_PROTECT)) | FLAG_EXCLUDE
     return out
+
+
+# ----------------------------------------------------------------------------
+# PASK App. B.5: the engine's attention over persistent (compacted, mixed
+# precision), recent and current storage
+# ----------------------------------------------------------------------------
+
+
+def engine_attention(q_rows, q_pos, stores, scale: float) -> np.ndarray:
+    """Outputs [R][d] (fp64) of R query rows over the union of the storages.
+
+    PASK App. B.5: each visible key appears once across persistent, recent
+    and current storage, and logical positions and the causal mask survive
+    storage gaps: a key at position p_k is visible to a query at position
+    p_q iff p_k <= p_q.  One softmax runs over all visible keys of all
+    storages (the partitions share one normalisation, Eq. 15; they are not
+    normalised and averaged separately).
+    q_rows: [R][d]; q_pos: [R] or None (every key visible); stores: list of
+    (K [n][d], V [n][d], positions [n] or None).  A row that sees no key
+    outputs 0 (reading: empty partitions contribute nothing).
+    """
+    q = np.asarray(q_rows, np.float64)
+    R, d = q.shape
+    ks, vs, ps = [], [], []
+    for k, v, pos in stores:
+        k = np.asarray(k, np.float64).reshape(-1, d)
+        if k.shape[0] == 0:
+            continue
+        ks.append(k)
+        vs.append(np.asarray(v, np.float64).reshape(-1, d))
+        ps.append(np.full(k.shape[0], np.iinfo(np.int64).min) if pos is None
+                  else np.asarray(pos, np.int64))
+    out = np.zeros((R, d), dtype=np.float64)
+    if not ks:
+        return out
+    K, V, P = np.concatenate(ks), np.concatenate(vs), np.concatenate(ps)
+    for r in range(R):
+        vis = np.ones(K.shape[0], dtype=bool) if q_pos is None else P <= int(q_pos[r])
+        if vis.any():
+            out[r] = attend(q[r], K[vis], V[vis], scale)
+    return out
