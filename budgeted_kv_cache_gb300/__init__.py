@@ -65,6 +65,12 @@ class kvc_ref_store(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("ref_k", "ref_pos", "ref_k_out", "ref_pos_out", "failures")]
 
 
+class kvc_bf16_rows(ctypes.Structure):
+    """A bf16 row store of kvc_engine_attn (device pointers)."""
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("count", ctypes.c_void_p), ("capacity", ctypes.c_int32)]
+
+
 class kvc_effect_record(ctypes.Structure):
     """Window record of kvc_deletion_effect (device pointers: o, lse, s, u)."""
     _fields_ = [(n, ctypes.c_void_p) for n in ("o", "lse", "s", "u")]
@@ -86,6 +92,7 @@ def _load():
         SH, PO, PL = ctypes.POINTER(kvc_shape), ctypes.POINTER(kvc_policy), ctypes.POINTER(kvc_pools)
         RS = ctypes.POINTER(kvc_ref_store)
         ER, CT = ctypes.POINTER(kvc_effect_record), ctypes.POINTER(kvc_commit_thresholds)
+        BR = ctypes.POINTER(kvc_bf16_rows)
         sig = {
             "kvc_score_workspace_bytes": (SZ, [SH, I32]),
             "kvc_score": (ctypes.c_int, [SH, P, P, I32, F32, P, P, I32, U32, P, P, P, P, SZ, P]),
@@ -101,6 +108,8 @@ def _load():
             "kvc_pool_scores": (ctypes.c_int, [I64, I64, P, P, I32, I32, P]),
             "kvc_shared_scores": (ctypes.c_int, [SH, P, P, P]),
             "kvc_broadcast_kept": (ctypes.c_int, [SH, PO, P, P, P, P, P]),
+            "kvc_engine_attn_workspace_bytes": (SZ, [SH, PO, I32, BR, BR]),
+            "kvc_engine_attn": (ctypes.c_int, [SH, PO, P, I32, P, PL, P, BR, BR, F32, P, P, SZ, P]),
             "kvc_deletion_effect_workspace_bytes": (SZ, [SH, I32]),
             "kvc_deletion_effect": (ctypes.c_int, [SH, P, P, P, I32, F32, P, P, I32, P, ER, P, P, SZ, P]),
             "kvc_commit_workspace_bytes": (SZ, [SH, I32]),
@@ -399,3 +408,33 @@ def kvc_commit_flags(batch, n_tokens, page_start, page_len, retire, protect, fla
     _check("kvc_commit_flags", _load().kvc_commit_flags(
         int(batch), int(n_tokens), n, _p(page_start), _p(page_len), _p(retire), _p(protect),
         _p(flags), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- engine attention
+
+def bf16_rows(k, v, pos, count) -> kvc_bf16_rows:
+    """A recent / current row store: k, v bf16 [U][capacity][d], pos int32 [U][capacity] or None,
+    count int32 [U]."""
+    return kvc_bf16_rows(_p(k), _p(v), _p(pos), _p(count), int(k.shape[-2]))
+
+
+def kvc_engine_attn_workspace_bytes(shape, policy: Optional[Policy], n_q, recent=None, current=None) -> int:
+    cp = policy.c() if policy is not None else None
+    return _load().kvc_engine_attn_workspace_bytes(
+        ctypes.byref(shape), ctypes.byref(cp) if cp is not None else None, int(n_q),
+        ctypes.byref(recent) if recent is not None else None,
+        ctypes.byref(current) if current is not None else None)
+
+
+def kvc_engine_attn(shape, policy: Optional[Policy], q, n_q, q_pos, pools: Optional[Pools], kept_count,
+                    recent, current, softmax_scale, out, workspace=None, stream=None):
+    """PASK App. B.5 attention over persistent pools, recent and current bf16 rows (see include/kvc.h)."""
+    cp = policy.c() if policy is not None else None
+    cpools = pools.c() if pools is not None else None
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("kvc_engine_attn", _load().kvc_engine_attn(
+        ctypes.byref(shape), ctypes.byref(cp) if cp is not None else None, _p(q), int(n_q), _p(q_pos),
+        ctypes.byref(cpools) if cpools is not None else None, _p(kept_count),
+        ctypes.byref(recent) if recent is not None else None,
+        ctypes.byref(current) if current is not None else None, float(softmax_scale), _p(out),
+        _p(workspace), wb, _stream(stream)))

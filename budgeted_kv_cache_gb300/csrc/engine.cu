@@ -1,0 +1,261 @@
+// The engine's attention over persistent, recent and current storage.
+//
+// PASK App. B.5 ("Packed attention and quantization"): the kernel reads the
+// disjoint high / low maps of the persistent storage (here the bf16, int8
+// and int4 pools of a compaction pass, dequantised inline as code * scale),
+// the recent storage and the current KV (bf16 rows), with logical positions:
+// a key at position p_k is visible to a query at position p_q iff
+// p_k <= p_q, whatever storage holds it, so positions and the causal mask
+// survive the gaps between storages.  Query heads map to their KV head (one
+// head, GQA-2, GQA-4, GQA-8); a unit's rows are split across CTAs (split-KV)
+// and every partition is merged with Eq. 15.  Scores, softmax statistics and
+// value sums are fp32; the output is bf16.
+//
+// Work layout: one unit per blockIdx.x, a split of the unit's rows (the
+// storages concatenated: int4, int8, bf16 pools, recent, current) per
+// blockIdx.y.  A warp takes 32 consecutive rows per step; for the scores each
+// lane owns one key row (16-byte loads, the unit's query rows in shared
+// memory as broadcasts) and applies the causal test of every query row; for
+// P V each lane owns d / 32 columns and the step's probabilities arrive by
+// shuffles.  Each warp keeps an online (max, sum, value sum) per query row;
+// the warps, then the splits, are merged with Eq. 15.
+#include <limits.h>
+#include <math.h>
+
+#include "decode_rows.cuh"
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int kEngThreads = 128;
+constexpr int kEngWarps = kEngThreads / 32;
+constexpr unsigned kAll = 0xffffffffu;
+constexpr int kClasses = KVC_N_POOLS + 2;     // pools, recent, current
+
+struct RowRef {
+  PoolPtrs pp;
+  int kind;          // KVC_POOL_* of the row's encoding
+  int64_t row;       // row index in the storage's arrays
+  const int32_t* pos;
+};
+
+__device__ __forceinline__ RowRef row_ref(const DecodeArgs& a, int u, int cls, int rr) {
+  RowRef r;
+  if (cls < KVC_N_POOLS) {
+    r.pp = pool_ptrs(a.pools, cls);
+    r.kind = cls;
+    r.row = static_cast<int64_t>(u) * a.capacity + rr;
+    r.pos = a.pool_pos ? a.pool_pos + (static_cast<int64_t>(cls) * a.U + u) * a.capacity + rr : nullptr;
+  } else if (cls == KVC_N_POOLS) {
+    r.pp = {a.rec_k, a.rec_v, nullptr, nullptr};
+    r.kind = KVC_POOL_BF16;
+    r.row = static_cast<int64_t>(u) * a.rec_cap + rr;
+    r.pos = a.rec_pos ? a.rec_pos + r.row : nullptr;
+  } else {
+    r.pp = {a.cur_k, a.cur_v, nullptr, nullptr};
+    r.kind = KVC_POOL_BF16;
+    r.row = static_cast<int64_t>(u) * a.cur_cap + rr;
+    r.pos = a.cur_pos ? a.cur_pos + r.row : nullptr;
+  }
+  return r;
+}
+
+// RR: query rows per unit (G heads x n_q queries) rounded up to 1, 2, 4, 8
+// or 16; BF: every storage holds bf16 rows (the int8 / int4 paths are not
+// compiled in).
+template <int D, int RR, bool BF>
+__global__ void __launch_bounds__(kEngThreads, RR >= 8 ? 2 : (RR >= 4 ? 3 : 4))
+engine_attn_kernel(const DecodeArgs a) {
+  constexpr int NC = D / 32;
+  constexpr int VB = RR >= 16 ? 4 : (RR >= 8 ? 8 : 16);   // value rows in flight together
+  __shared__ __align__(16) float qs[RR][D];
+  __shared__ int qp[RR];
+  __shared__ float wm[kEngWarps][RR], wl[kEngWarps][RR];
+  __shared__ float wacc[kEngWarps][RR][D];
+
+  const int u = blockIdx.x, split = blockIdx.y;
+  const int R = a.G, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = u / (a.L * a.Hkv);
+  const bool row_mode = a.quant_mode == KVC_QUANT_ROW_FP16;
+  const float cs = a.scale * 1.4426950408889634f;
+  {
+    const __nv_bfloat16* q = a.q + static_cast<int64_t>(u) * R * D;
+    for (int idx = tid; idx < RR * D; idx += kEngThreads)
+      qs[idx / D][idx % D] = idx / D < R ? __bfloat162float(q[idx]) * cs : 0.f;
+    if (tid < RR)
+      qp[tid] = (tid < R && a.q_pos) ? a.q_pos[static_cast<int64_t>(b) * a.n_q + tid % a.n_q] : INT_MAX;
+  }
+  int cnt[kClasses];
+  int n = 0;
+#pragma unroll
+  for (int c = 0; c < kClasses; ++c) {
+    int v = 0;
+    if (c < KVC_N_POOLS) v = (a.has_pools && c >= a.pool_lo && c < a.pool_hi) ? a.kept_count[c * a.U + u] : 0;
+    else if (c == KVC_N_POOLS) v = a.rec_count ? a.rec_count[u] : 0;
+    else v = a.cur_count ? a.cur_count[u] : 0;
+    cnt[c] = v;
+    n += v;
+  }
+  const int per = (n + a.splits - 1) / a.splits;
+  const int lo = min(n, split * per), hi = min(n, lo + per);
+  __syncthreads();
+
+  float m[RR], l[RR], acc[RR][NC];
+#pragma unroll
+  for (int h = 0; h < RR; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[h][c] = 0.f;
+  }
+
+  for (int base = lo + warp * 32; base < hi; base += kEngThreads) {
+    // ---- scores: lane = row; the row's storage class and index
+    const int r = base + lane;
+    int cls = -1, rr = r;
+    if (r < hi) {
+#pragma unroll
+      for (int c = 0; c < kClasses; ++c) {
+        if (cls < 0) {
+          if (rr < cnt[c]) cls = c;
+          else rr -= cnt[c];
+        }
+      }
+    }
+    float s[RR];
+#pragma unroll
+    for (int h = 0; h < RR; ++h) s[h] = 0.f;
+    int kp = INT_MIN;
+    if (cls >= 0) {
+      const RowRef ref = row_ref(a, u, cls, rr);
+      if (ref.pos) kp = __ldg(ref.pos);
+      key_dot<D, RR, BF>(ref.kind, ref.pp, ref.row, row_mode, qs, R, s);
+    }
+    // ---- online softmax per query row over this step's visible keys (log2 domain)
+    float pr[RR];
+#pragma unroll
+    for (int h = 0; h < RR; ++h) {
+      pr[h] = 0.f;
+      if (h < R) {
+        const bool vis = cls >= 0 && kp <= qp[h];
+        const float sv = vis ? s[h] : -INFINITY;
+        float mx = sv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, o));
+        const float mn = fmaxf(m[h], mx);
+        if (mn != -INFINITY) {                     // uniform: some key so far is visible to row h
+          const float corr = m[h] == -INFINITY ? 0.f : exp2f(m[h] - mn);
+          pr[h] = vis ? exp2f(sv - mn) : 0.f;
+          float sm = pr[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kAll, sm, o);
+          l[h] = l[h] * corr + sm;
+          m[h] = mn;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) acc[h][c] *= corr;
+        }
+      }
+    }
+    // ---- P V: lane = columns; VB rows' loads issued together; row j's
+    // storage and index come from lane j
+#pragma unroll 1
+    for (int j0 = 0; j0 < 32; j0 += VB) {
+      if (base + j0 >= hi) break;                  // uniform across the warp
+      float v[VB][NC];
+#pragma unroll
+      for (int k = 0; k < VB; ++k) {
+        const int ck = __shfl_sync(kAll, cls, j0 + k);
+        const int rk = __shfl_sync(kAll, rr, j0 + k);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) v[k][c] = 0.f;
+        if (ck >= 0) {
+          const RowRef ref = row_ref(a, u, ck, rk);
+          load_value_cols<D, BF>(ref.kind, ref.pp, ref.row, lane, row_mode, v[k]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < VB; ++k) {
+#pragma unroll
+        for (int h = 0; h < RR; ++h) {
+          if (h < R) {
+            const float pj = __shfl_sync(kAll, pr[h], j0 + k);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[h][c] = fmaf(pj, v[k][c], acc[h][c]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- merge the warps of the CTA (Eq. 15), then write out or publish
+#pragma unroll
+  for (int h = 0; h < RR; ++h) {
+    if (h < R) {
+      if (lane == 0) {
+        wm[warp][h] = m[h];
+        wl[warp][h] = l[h];
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c) wacc[warp][h][lane * NC + c] = acc[h][c];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < R * D; idx += kEngThreads) {
+    const int h = idx / D, col = idx % D;
+    float v = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kEngWarps; ++w) v = fmaxf(v, wm[w][h]);
+    float num = 0.f, den = 0.f;
+    if (v != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kEngWarps; ++w) {
+        if (wm[w][h] == -INFINITY) continue;       // a warp that saw no visible key
+        const float f = exp2f(wm[w][h] - v);
+        num += f * wacc[w][h][col];
+        den += f * wl[w][h];
+      }
+    }
+    if (a.splits == 1) {
+      const float o = den > 0.f ? num / den : 0.f;  // a row that sees no key outputs 0
+      a.out[(static_cast<int64_t>(u) * R + h) * D + col] = __float2bfloat16_rn(o);
+    } else {
+      const int64_t slot = (static_cast<int64_t>(u) * a.splits + split) * R + h;
+      a.ws_acc[slot * D + col] = num;
+      if (col == 0) {
+        a.ws_ml[slot * 2] = v;
+        a.ws_ml[slot * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_engine(const DecodeArgs& a, cudaStream_t stream) {
+  const dim3 grid(a.U, a.splits);
+  const bool bf = !a.has_pools || a.pool_lo == KVC_POOL_BF16;
+  const int rr = a.G <= 1 ? 1 : a.G <= 2 ? 2 : a.G <= 4 ? 4 : a.G <= 8 ? 8 : 16;
+#define KVC_ENGINE_LAUNCH(DD, RRV)                                                          \
+  if (a.d == DD && rr == RRV) {                                                            \
+    if (bf) engine_attn_kernel<DD, RRV, true><<<grid, kEngThreads, 0, stream>>>(a);        \
+    else engine_attn_kernel<DD, RRV, false><<<grid, kEngThreads, 0, stream>>>(a);          \
+  }
+  KVC_ENGINE_LAUNCH(64, 1)
+  KVC_ENGINE_LAUNCH(64, 2)
+  KVC_ENGINE_LAUNCH(64, 4)
+  KVC_ENGINE_LAUNCH(64, 8)
+  KVC_ENGINE_LAUNCH(64, 16)
+  KVC_ENGINE_LAUNCH(128, 1)
+  KVC_ENGINE_LAUNCH(128, 2)
+  KVC_ENGINE_LAUNCH(128, 4)
+  KVC_ENGINE_LAUNCH(128, 8)
+  KVC_ENGINE_LAUNCH(128, 16)
+#undef KVC_ENGINE_LAUNCH
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || a.splits == 1) return err;
+  return launch_decode_merge(a, stream);
+}
+
+}  // namespace kvc

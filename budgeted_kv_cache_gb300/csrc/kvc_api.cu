@@ -209,6 +209,46 @@ int decode_splits(const kvc_shape* s, const kvc_policy* pol, int sms) {
   return static_cast<int>(std::max<int64_t>(want, 1));
 }
 
+struct EnginePlan {
+  int splits = 1, rows = 0;
+  bool byte_mode = false;
+  size_t ws = 0;
+};
+
+kvc_status plan_engine(const kvc_shape* s, const kvc_policy* pol, int32_t n_q, bool with_pools,
+                       const kvc_bf16_rows* rec, const kvc_bf16_rows* cur, EnginePlan* p) {
+  kvc_status st = check_shape(s);
+  if (st != KVC_OK) return st;
+  if (n_q < 1) return KVC_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(s->n_q_heads / s->n_kv_heads) * n_q;
+  if (rows > 16) return KVC_ERR_UNSUPPORTED;
+  int64_t keys = 0;
+  if (with_pools) {
+    SelectPlan sp;
+    if ((st = plan_select(s, pol, &sp)) != KVC_OK) return st;
+    p->byte_mode = sp.byte_mode;
+    keys += static_cast<int64_t>(pol->capacity) * (sp.byte_mode ? 3 : 1);
+  }
+  for (const kvc_bf16_rows* r : {rec, cur}) {
+    if (r && r->count) {
+      if (r->capacity < 1 || !r->k || !r->v) return KVC_ERR_INVALID_ARG;
+      keys += r->capacity;
+    }
+  }
+  DevInfo info;
+  if ((st = check_device(&info)) != KVC_OK) return st;
+  const int64_t U = n_units(s);
+  int64_t want = (8LL * info.sms + U - 1) / U;
+  want = std::min<int64_t>(std::min<int64_t>(want, std::max<int64_t>(1, (keys + 127) / 128)), 32);
+  p->splits = static_cast<int>(std::max<int64_t>(want, 1));
+  p->rows = static_cast<int>(rows);
+  if (p->splits > 1) {
+    const size_t slots = static_cast<size_t>(U) * p->splits * rows;
+    p->ws = (slots * 2 * sizeof(float) + 255) / 256 * 256 + slots * s->head_dim * sizeof(float);
+  }
+  return KVC_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- CommitKV plans
@@ -588,6 +628,79 @@ kvc_status kvc_decode_attn(const kvc_shape* shape, const kvc_policy* policy, con
   a.pool_lo = sp.byte_mode ? KVC_POOL_INT4 : KVC_POOL_BF16;
   a.pool_hi = KVC_N_POOLS;
   if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+  return KVC_OK;
+}
+
+size_t kvc_engine_attn_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy, int32_t n_q,
+                                       const kvc_bf16_rows* recent, const kvc_bf16_rows* current) {
+  EnginePlan p;
+  if (plan_engine(shape, policy, n_q, policy != nullptr, recent, current, &p) != KVC_OK) return 0;
+  return p.ws;
+}
+
+kvc_status kvc_engine_attn(const kvc_shape* shape, const kvc_policy* policy, const void* q,
+                           int32_t n_q, const int32_t* q_pos, const kvc_pools* pools,
+                           const int32_t* kept_count, const kvc_bf16_rows* recent,
+                           const kvc_bf16_rows* current, float softmax_scale, void* out,
+                           void* workspace, size_t workspace_bytes, kvc_stream stream) {
+  const bool with_pools = pools != nullptr;
+  if (with_pools && !policy) return KVC_ERR_INVALID_ARG;
+  EnginePlan p;
+  kvc_status st = plan_engine(shape, policy, n_q, with_pools, recent, current, &p);
+  if (st != KVC_OK) return st;
+  if (!q || !out) return KVC_ERR_INVALID_ARG;
+  if (with_pools) {
+    if (!kept_count || !pools->k_bf16 || !pools->v_bf16) return KVC_ERR_INVALID_ARG;
+    if (p.byte_mode && (!pools->k_i8 || !pools->v_i8 || !pools->k_i4 || !pools->v_i4 ||
+                        !pools->k_i8_scale || !pools->v_i8_scale || !pools->k_i4_scale ||
+                        !pools->v_i4_scale))
+      return KVC_ERR_INVALID_ARG;
+    if (q_pos && !pools->pos_out) return KVC_ERR_INVALID_ARG;   // positions decide visibility
+  }
+  if (p.ws > 0 && (!workspace || workspace_bytes < p.ws || !aligned(workspace, 256))) return KVC_ERR_WORKSPACE;
+  if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / sqrtf(static_cast<float>(shape->head_dim));
+  DecodeArgs a = {};
+  a.U = static_cast<int32_t>(n_units(shape));
+  a.G = p.rows;
+  a.d = shape->head_dim;
+  a.Hkv = shape->n_kv_heads;
+  a.L = shape->n_layers;
+  a.B = shape->batch;
+  a.capacity = with_pools ? policy->capacity : 0;
+  a.quant_mode = with_pools ? policy->quant_mode : 0;
+  a.splits = p.splits;
+  a.scale = softmax_scale;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  if (with_pools) a.pools = *pools;
+  a.kept_count = kept_count;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  if (p.splits > 1) {
+    const size_t slots = static_cast<size_t>(a.U) * p.splits * p.rows;
+    a.ws_ml = static_cast<float*>(workspace);
+    a.ws_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        (slots * 2 * sizeof(float) + 255) / 256 * 256);
+  }
+  a.pool_lo = p.byte_mode ? KVC_POOL_INT4 : KVC_POOL_BF16;
+  a.pool_hi = KVC_N_POOLS;
+  a.n_q = n_q;
+  a.q_pos = q_pos;
+  a.pool_pos = with_pools ? pools->pos_out : nullptr;
+  a.has_pools = with_pools;
+  if (recent && recent->count) {
+    a.rec_k = static_cast<const __nv_bfloat16*>(recent->k);
+    a.rec_v = static_cast<const __nv_bfloat16*>(recent->v);
+    a.rec_pos = recent->pos;
+    a.rec_count = recent->count;
+    a.rec_cap = recent->capacity;
+  }
+  if (current && current->count) {
+    a.cur_k = static_cast<const __nv_bfloat16*>(current->k);
+    a.cur_v = static_cast<const __nv_bfloat16*>(current->v);
+    a.cur_pos = current->pos;
+    a.cur_count = current->count;
+    a.cur_cap = current->capacity;
+  }
+  if (launch_engine(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
   return KVC_OK;
 }
 

@@ -102,6 +102,21 @@ struct DecodeArgs {
   float* ws_ml;                // [U][splits][G][2]
   float* ws_acc;               // [U][splits][G][d]
   int32_t pool_lo, pool_hi;
+  // engine attention (PASK App. B.5): G then counts rows per unit, G_heads n_q
+  int32_t n_q;                 // queries per head
+  const int32_t* q_pos;        // [B][n_q] logical query positions, or null: every key visible
+  const int32_t* pool_pos;     // [KVC_N_POOLS][U][capacity] key positions of the pools, or null
+  bool has_pools;
+  const __nv_bfloat16* rec_k;  // recent storage: bf16 [U][rec_cap][d]
+  const __nv_bfloat16* rec_v;
+  const int32_t* rec_pos;      // [U][rec_cap] or null
+  const int32_t* rec_count;    // [U] or null (empty)
+  int32_t rec_cap;
+  const __nv_bfloat16* cur_k;  // current storage: bf16 [U][cur_cap][d]
+  const __nv_bfloat16* cur_v;
+  const int32_t* cur_pos;
+  const int32_t* cur_count;
+  int32_t cur_cap;
 };
 
 struct BonusArgs {
@@ -191,6 +206,8 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes);
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_engine(const DecodeArgs& a, cudaStream_t stream);
 size_t effect_smem_bytes(int Rp, int n_stages);
 cudaError_t launch_effect(const EffectArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                           const CUtensorMap& tmap_q, int grid, size_t smem_bytes, cudaStream_t stream);

@@ -412,6 +412,49 @@ kvc_status kvc_decode_attn_noalloc(const kvc_shape* shape, const kvc_policy* pol
                                    kvc_stream stream);
 
 /* ------------------------------------------------------------------------
+ * kvc_engine_attn -- the engine's attention over persistent, recent and
+ * current storage (PASK App. B.5, "Packed attention and quantization").
+ *
+ * Every visible key appears once across the storages: the persistent pools
+ * of a compaction pass (bf16 high map, int8 / int4 low maps dequantised
+ * inline as code * scale), the recent storage and the current KV (bf16).  A
+ * key at logical position p_k is visible to a query at position p_q iff
+ * p_k <= p_q, whatever storage holds it.  For query head h (reading KV head
+ * h / G) and query i:
+ *   out[h][i] = sum_j softmax_j(q_hi . k_j * scale) v_j over the visible keys,
+ * one softmax over all storages (partitions merged by Eq. 15); fp32
+ * arithmetic, bf16 output; a query that sees no key outputs 0.  G n_q <= 16
+ * (one head, GQA-2, GQA-4, GQA-8; several queries per head for chunked or
+ * speculative decoding); rows are split across CTAs (split-KV).
+ *
+ * q        bf16 [B][L][H_q][n_q][d]; out bf16, same layout.
+ * q_pos    optional int32 [B][n_q] (NULL: every key visible).
+ * pools    optional (NULL: no persistent storage): the pools of
+ *          kvc_compact_rerotate_quant with `policy` (its quant_mode and mode
+ *          decide which pools hold rows) and kept_count int32 [KVC_N_POOLS][U];
+ *          pools->pos_out gives their positions (required when q_pos is given).
+ * recent, current  optional bf16 row stores (NULL or count NULL: empty);
+ *          pos NULL = every row visible.
+ * workspace >= kvc_engine_attn_workspace_bytes(...), 256-byte aligned (may
+ *          be 0 bytes: then NULL is accepted).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* k;          /* bf16 [U][capacity][d] */
+  const void* v;          /* bf16 [U][capacity][d] */
+  const int32_t* pos;     /* optional int32 [U][capacity]: logical positions */
+  const int32_t* count;   /* int32 [U]: rows in use (<= capacity) */
+  int32_t capacity;
+} kvc_bf16_rows;
+
+size_t kvc_engine_attn_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy, int32_t n_q,
+                                       const kvc_bf16_rows* recent, const kvc_bf16_rows* current);
+kvc_status kvc_engine_attn(const kvc_shape* shape, const kvc_policy* policy, const void* q,
+                           int32_t n_q, const int32_t* q_pos, const kvc_pools* pools,
+                           const int32_t* kept_count, const kvc_bf16_rows* recent,
+                           const kvc_bf16_rows* current, float softmax_scale, void* out,
+                           void* workspace, size_t workspace_bytes, kvc_stream stream);
+
+/* ------------------------------------------------------------------------
  * CommitKV lifecycle-aware retirement ("CommitKV: Lifecycle-Aware KV Cache
  * Compression via Commit Transitions for Multi-Turn Agents", Sec. 3.2-3.3).
  *
