@@ -347,6 +347,50 @@ def run_gpu(args, w, world, rank, local):
         t_dec.append(d0.elapsed_time(d1))
     t_decode = statistics.mean(t_dec)
 
+    # the engine's attention (PASK App. B.5) over the compacted pools plus 128
+    # recent rows and the current rows, one and four queries per head, timed
+    # separately like the decode step
+    t_eng = {}
+    if not w.byte_mode:
+        import budgeted_kv_cache_gb300 as kvc_e
+        ge = torch.Generator(device=dev)
+        ge.manual_seed(7)
+        Ue = w.n_units
+        rec_cap = 128
+        rk = torch.randn((Ue, rec_cap, w.head_dim), generator=ge, device=dev).to(torch.bfloat16)
+        rv = torch.randn((Ue, rec_cap, w.head_dim), generator=ge, device=dev).to(torch.bfloat16)
+        base_pos = w.n_tokens + 1
+        rpos = (base_pos + torch.arange(rec_cap, device=dev, dtype=torch.int32)).expand(Ue, rec_cap).contiguous()
+        rcnt = torch.full((Ue,), rec_cap, dtype=torch.int32, device=dev)
+        for nq in (1, 4):
+            ck = torch.randn((Ue, nq, w.head_dim), generator=ge, device=dev).to(torch.bfloat16)
+            cv = torch.randn((Ue, nq, w.head_dim), generator=ge, device=dev).to(torch.bfloat16)
+            cpos = (base_pos + rec_cap + torch.arange(nq, device=dev, dtype=torch.int32)).expand(Ue, nq).contiguous()
+            ccnt = torch.full((Ue,), nq, dtype=torch.int32, device=dev)
+            qe = torch.randn((w.batch, w.n_layers, w.n_q_heads, nq, w.head_dim), generator=ge,
+                             device=dev).to(torch.bfloat16)
+            qpos = (base_pos + rec_cap + torch.arange(nq, device=dev, dtype=torch.int32)).expand(w.batch, nq).contiguous()
+            oute = torch.empty_like(qe)
+            rec = kvc_e.bf16_rows(rk, rv, rpos, rcnt)
+            cur = kvc_e.bf16_rows(ck, cv, cpos, ccnt)
+            wsb = kvc_e.kvc_engine_attn_workspace_bytes(p.shape, p.policy, nq, rec, cur)
+            wse = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+            fe = lambda: kvc_e.kvc_engine_attn(p.shape, p.policy, qe, nq, qpos, p.pools, p.kept_count,
+                                               rec, cur, 0.0, oute, wse, stream=stream)
+            for _ in range(3):
+                fe()
+            t_v = []
+            for _ in range(10):
+                flush.fill_(1)
+                d0, d1 = ev(), ev()
+                d0.record(stream)
+                fe()
+                d1.record(stream)
+                torch.cuda.synchronize()
+                t_v.append(d0.elapsed_time(d1))
+            t_eng[f"engine_attn_{nq}q"] = statistics.mean(t_v)
+        del rk, rv
+
     # one H2O decode step (PACE Sec. 3.1): window-1 scoring of the decode
     # query of every head over the whole cache, accumulated into the scores,
     # with the row statistics computed here (two passes) or supplied by the
@@ -520,7 +564,7 @@ def run_gpu(args, w, world, rank, local):
                      "tc_tflops_algorithmic": flops / (score_ms * 1e-3) / 1e12},
         "stages_ms": {"score": score_ms, "select": statistics.mean(t_select),
                       "compact": statistics.mean(t_compact), "decode": t_decode,
-                      "compact_reference_store": t_cref, **t_h2o, **t_var, **(t_eff or {})},
+                      "compact_reference_store": t_cref, **t_eng, **t_h2o, **t_var, **(t_eff or {})},
         "pass_roofline": {"t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step,
                           "algorithmic_bytes": ab["total"], "algorithmic_flops": flops},
         "cpu_baseline": cpu, "e2e": e2e,

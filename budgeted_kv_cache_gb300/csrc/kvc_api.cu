@@ -656,7 +656,10 @@ kvc_status kvc_engine_attn(const kvc_shape* shape, const kvc_policy* policy, con
                         !pools->v_i4_scale))
       return KVC_ERR_INVALID_ARG;
     if (q_pos && !pools->pos_out) return KVC_ERR_INVALID_ARG;   // positions decide visibility
+    if (!aligned(pools->k_bf16, 16) || !aligned(pools->v_bf16, 16)) return KVC_ERR_INVALID_ARG;
   }
+  for (const kvc_bf16_rows* r : {recent, current})
+    if (r && r->count && (!aligned(r->k, 16) || !aligned(r->v, 16))) return KVC_ERR_INVALID_ARG;
   if (p.ws > 0 && (!workspace || workspace_bytes < p.ws || !aligned(workspace, 256))) return KVC_ERR_WORKSPACE;
   if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / sqrtf(static_cast<float>(shape->head_dim));
   DecodeArgs a = {};

@@ -434,7 +434,7 @@ kvc_status kvc_decode_attn_noalloc(const kvc_shape* shape, const kvc_policy* pol
  *          decide which pools hold rows) and kept_count int32 [KVC_N_POOLS][U];
  *          pools->pos_out gives their positions (required when q_pos is given).
  * recent, current  optional bf16 row stores (NULL or count NULL: empty);
- *          pos NULL = every row visible.
+ *          pos NULL = every row visible; k, v 16-byte aligned.
  * workspace >= kvc_engine_attn_workspace_bytes(...), 256-byte aligned (may
  *          be 0 bytes: then NULL is accepted).
  * ---------------------------------------------------------------------- */
