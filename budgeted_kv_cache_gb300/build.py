@@ -12,7 +12,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvc.so")
 SOURCES = ["kvc_api.cu", "score_tc.cu", "select.cu", "compact.cu", "decode.cu", "bonus.cu", "variants.cu",
-           "commit.cu", "engine.cu"]
+           "commit.cu", "engine.cu", "score_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast-math: quantisation and re-rotation need IEEE division, square
 # root and subnormals exactly as written.

@@ -83,6 +83,9 @@ int64_t n_units(const kvc_shape* s) {
 
 // ---------------------------------------------------------------- scoring plan
 struct ScorePlan {
+  bool small = false;          // R <= 16: the CUDA-core path
+  int small_splits = 0;
+  size_t ws_logits = 0, ws_split = 0;
   int grid = 0;
   int n_tiles = 0, chunk_tiles = 0, S = 0;
   int R = 0, q_rows = 0, n_stages = 0;
@@ -101,6 +104,19 @@ kvc_status plan_score(const kvc_shape* s, int32_t window, ScorePlan* p) {
   if ((st = check_device(&info)) != KVC_OK) return st;
   p->grid = info.sms;
   p->R = static_cast<int>(R);
+  if (R <= 16 && n_units(s) <= 65535) {
+    // a thin contraction: the CUDA-core path reads the keys once
+    const int64_t U = n_units(s);
+    const int RR = small_rows(p->R);
+    int64_t want = (8LL * info.sms + U - 1) / U;
+    want = std::min<int64_t>(want, (s->n_tokens + 2047) / 2048);
+    p->small = true;
+    p->small_splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 64)));
+    p->ws_logits = (static_cast<size_t>(U) * s->n_tokens * RR * 4 + 255) / 256 * 256;
+    p->ws_split = (static_cast<size_t>(U) * p->small_splits * RR * 8 + 255) / 256 * 256;
+    p->ws_total = p->ws_logits + p->ws_split + (static_cast<size_t>(U) * RR * 4 + 255) / 256 * 256;
+    return KVC_OK;
+  }
   p->n_tiles = static_cast<int>((s->n_tokens + kTileTokens - 1) / kTileTokens);
   int chunk = 16;
   if (const char* e = getenv("KVC_SCORE_CHUNK_TILES")) {
@@ -359,6 +375,17 @@ kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_
   a.counters = static_cast<uint32_t*>(workspace);
   a.stats = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + p.ws_counters);
 
+  if (p.small) {
+    a.k_small = static_cast<const __nv_bfloat16*>(k_cache);
+    a.q_small = static_cast<const __nv_bfloat16*>(q_window);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (launch_score_small(a, p.small_splits, reinterpret_cast<float*>(ws),
+                           reinterpret_cast<float2*>(ws + p.ws_logits),
+                           reinterpret_cast<float*>(ws + p.ws_logits + p.ws_split),
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return KVC_ERR_CUDA;
+    return KVC_OK;
+  }
   CUtensorMap mk, mq;
   if ((st = encode_3d(&mk, k_cache, shape->head_dim, shape->n_tokens, a.U, 64, kTileTokens)) != KVC_OK)
     return st;

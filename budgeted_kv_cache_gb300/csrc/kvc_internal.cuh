@@ -41,6 +41,8 @@ struct ScoreArgs {
   int32_t* unit_status;
   uint32_t* counters;          // [U] pass-1 chunks finished per unit
   float2* stats;               // [U][S][R] (max, sum) in the log2 domain
+  const __nv_bfloat16* k_small;  // small-window path: keys [U][T][d]
+  const __nv_bfloat16* q_small;  // small-window path: window rows [U][R][d]
 };
 
 struct SelectArgs {
@@ -203,6 +205,10 @@ cudaError_t launch_broadcast(const int32_t* kept_seq, const int32_t* count_seq, 
 cudaError_t launch_score(const ScoreArgs& a, const CUtensorMap& tmap_k, const CUtensorMap& tmap_q,
                          int grid, size_t smem_bytes, cudaStream_t stream);
 size_t score_smem_bytes(int d, int q_rows, int n_stages);
+int small_rows(int R);
+size_t score_small_smem_bytes(int d);
+cudaError_t launch_score_small(const ScoreArgs& a, int splits, float* logits, float2* split_stats,
+                               float* lse2, cudaStream_t stream);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes);
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
