@@ -182,20 +182,23 @@ __global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeArgs a)
 }
 
 // bf16 pools only (token and page mode): each warp's 32 rows per step are
-// contiguous in the pool, so one bulk copy per step brings the 32 key rows
-// and one the 32 value rows into the warp's shared-memory buffers (the copy
-// engine moves whole rows; no per-lane gathers reach L1).  Scores: lane =
-// row, its 16-byte chunks read in an order rotated by the lane so that the
-// 32 lanes hit different banks; P V: lane = d/32 columns.  Online softmax
-// per warp and Eq. 15 merges as in decode_kernel.
+// contiguous in the pool, so bulk copies bring them into the warp's
+// shared-memory buffers (the copy engine moves whole rows; no per-lane
+// gathers reach L1): each lane copies one key row into a row padded by 16
+// bytes, and one copy brings the 32 value rows.  Scores: lane = row, all
+// lanes reading the same 16-byte chunk index (the padding puts them in
+// different banks, and the query rows are read as broadcasts); P V: lane =
+// d/32 columns.  Online softmax per warp and Eq. 15 merges as in
+// decode_kernel.
 template <int D, int GG>
 __global__ void __launch_bounds__(kThreads, 3) decode_bulk_kernel(const DecodeArgs a) {
   constexpr int NC = D / 32;
   constexpr int ROWB = D * 2;                    // bytes per row
   constexpr int CH = ROWB / 16;                  // 16-byte chunks per row
   extern __shared__ __align__(128) uint8_t dsm[];
-  uint8_t* kbuf0 = dsm;                          // [4 warps][32 rows][ROWB]
-  uint8_t* vbuf0 = dsm + kWarps * 32 * ROWB;
+  constexpr int ROWP = ROWB + 16;                 // padded key row in shared memory
+  uint8_t* kbuf0 = dsm;                          // [4 warps][32 rows][ROWP]
+  uint8_t* vbuf0 = dsm + kWarps * 32 * ROWP;      // [4 warps][32 rows][ROWB]
   __shared__ __align__(16) float qs[GG][D];
   __shared__ float wm[kWarps][GG], wl[kWarps][GG];
   __shared__ float wacc[kWarps][GG][D];
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_bulk_kernel(const DecodeAr
   const int lo = min(n, split * per), hi = min(n, lo + per);
   __syncthreads();
   volatile int* abort_flag = &abort_i;
-  uint8_t* kb = kbuf0 + warp * 32 * ROWB;
+  uint8_t* kb = kbuf0 + warp * 32 * ROWP;
   uint8_t* vb = vbuf0 + warp * 32 * ROWB;
   const uint32_t bar = smem_u32(&bars[warp]);
   const uint8_t* kg = static_cast<const uint8_t*>(a.pools.k_bf16) + static_cast<int64_t>(u) * a.capacity * ROWB;
@@ -235,12 +238,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_bulk_kernel(const DecodeAr
   uint32_t phase = 0;
   for (int base = lo + warp * 32; base < hi; base += kThreads) {
     const int nrow = min(32, hi - base);
-    if (lane == 0) {
-      fence_proxy_async_smem();                   // the buffers' last reads precede the copies
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * nrow * ROWB));
-      bulk_copy_g2s(smem_u32(kb), kg + static_cast<int64_t>(base) * ROWB, nrow * ROWB, bar);
-      bulk_copy_g2s(smem_u32(vb), vg + static_cast<int64_t>(base) * ROWB, nrow * ROWB, bar);
-    }
+    // key rows: one copy per lane into its padded row; value rows: one copy
+    fence_proxy_async_smem();                     // the buffers' last reads precede the copies
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * nrow * ROWB));
+    __syncwarp();
+    if (lane < nrow)
+      bulk_copy_g2s(smem_u32(kb + lane * ROWP), kg + (static_cast<int64_t>(base) + lane) * ROWB, ROWB, bar);
+    if (lane == 0) bulk_copy_g2s(smem_u32(vb), vg + static_cast<int64_t>(base) * ROWB, nrow * ROWB, bar);
     const bool ok = __all_sync(kFull, mbar_wait(bar, phase, abort_flag));
     if (!ok) {
       // a copy that did not land in time: wait for it (bounded) before leaving
@@ -257,10 +261,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_bulk_kernel(const DecodeAr
     float s[GG];
 #pragma unroll
     for (int h = 0; h < GG; ++h) s[h] = 0.f;
-    const uint4* krow = reinterpret_cast<const uint4*>(kb + lane * ROWB);
+    const uint4* krow = reinterpret_cast<const uint4*>(kb + lane * ROWP);
 #pragma unroll 4
     for (int v = 0; v < CH; ++v) {
-      const int cidx = (v + lane) & (CH - 1);   // rotated chunk order: different banks per lane
+      const int cidx = v;                       // the padding puts the lanes in different banks
       const uint4 w = krow[cidx];
       const uint32_t rw[4] = {w.x, w.y, w.z, w.w};
       float x[8];
@@ -391,8 +395,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const dim3 grid(a.U, a.splits);
   const bool bf = a.pool_lo == KVC_POOL_BF16;
   if (bf) {
-    // bulk-staged kernel: 2 x 4 warps x 32 rows x 2d bytes of dynamic shared memory
-    const size_t smem = static_cast<size_t>(2) * kWarps * 32 * a.d * 2;
+    // bulk-staged kernel: 4 warps x 32 rows x (padded key row + value row) of dynamic shared memory
+    const size_t smem = static_cast<size_t>(kWarps) * 32 * (a.d * 2 + 16 + a.d * 2);   // padded key rows + value rows
     const int g4 = a.G <= 1 ? 1 : a.G <= 2 ? 2 : a.G <= 4 ? 4 : 8;
     void (*k)(const DecodeArgs) = nullptr;
     if (a.d == 64) k = g4 == 1 ? decode_bulk_kernel<64, 1> : g4 == 2 ? decode_bulk_kernel<64, 2>

@@ -233,19 +233,21 @@ engine_attn_kernel(const DecodeArgs a) {
 
 // bf16 storages only (token / page mode pools, recent, current): the split's
 // rows are walked storage by storage, and each warp step's 32 rows (all in
-// one storage, so contiguous) reach the warp's shared-memory buffers by two
-// bulk copies, one for the key rows and one for the value rows.  Scores: lane
-// = row, 16-byte chunks read in a lane-rotated order (different banks per
-// lane); P V: lane = d / 32 columns.  The buffers hold the warps' partial
-// results for the final merge.
+// one storage, so contiguous) reach the warp's shared-memory buffers by bulk
+// copies: each lane copies one key row into a row padded by 16 bytes, one
+// copy brings the value rows.  Scores: lane = row, all lanes reading the same
+// 16-byte chunk index (the padding puts them in different banks, the query
+// rows are read as broadcasts); P V: lane = d / 32 columns.  The buffers hold
+// the warps' partial results for the final merge.
 template <int D, int RR>
 __global__ void __launch_bounds__(kEngThreads, RR >= 16 ? 2 : 3) engine_bulk_kernel(const DecodeArgs a) {
   constexpr int NC = D / 32;
   constexpr int ROWB = D * 2;
   constexpr int CH = ROWB / 16;
   extern __shared__ __align__(128) uint8_t esm[];
-  uint8_t* kbuf0 = esm;                          // [4 warps][32 rows][ROWB]
-  uint8_t* vbuf0 = esm + kEngWarps * 32 * ROWB;
+  constexpr int ROWP = ROWB + 16;                 // padded key row in shared memory
+  uint8_t* kbuf0 = esm;                          // [4 warps][32 rows][ROWP]
+  uint8_t* vbuf0 = esm + kEngWarps * 32 * ROWP;  // [4 warps][32 rows][ROWB]
   __shared__ __align__(16) float qs[RR][D];
   __shared__ int qp[RR];
   __shared__ float wm[kEngWarps][RR], wl[kEngWarps][RR];
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(kEngThreads, RR >= 16 ? 2 : 3) engine_bulk_ker
   const int lo = min(n, split * per), hi = min(n, lo + per);
   __syncthreads();
   volatile int* abort_flag = &abort_i;
-  uint8_t* kb = kbuf0 + warp * 32 * ROWB;
+  uint8_t* kb = kbuf0 + warp * 32 * ROWP;
   uint8_t* vb = vbuf0 + warp * 32 * ROWB;
   const uint32_t bar = smem_u32(&bars[warp]);
 
@@ -316,12 +318,13 @@ __global__ void __launch_bounds__(kEngThreads, RR >= 16 ? 2 : 3) engine_bulk_ker
 #pragma unroll 1
     for (int base = s0 + warp * 32; base < s1; base += kEngThreads) {
       const int nrow = min(32, s1 - base);
-      if (lane == 0) {
-        fence_proxy_async_smem();                 // the buffers' last reads precede the copies
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * nrow * ROWB));
-        bulk_copy_g2s(smem_u32(kb), kg + static_cast<int64_t>(base) * ROWB, nrow * ROWB, bar);
-        bulk_copy_g2s(smem_u32(vb), vg + static_cast<int64_t>(base) * ROWB, nrow * ROWB, bar);
-      }
+      // key rows: one copy per lane into its padded row; value rows: one copy
+      fence_proxy_async_smem();                     // the buffers' last reads precede the copies
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * nrow * ROWB));
+      __syncwarp();
+      if (lane < nrow)
+        bulk_copy_g2s(smem_u32(kb + lane * ROWP), kg + (static_cast<int64_t>(base) + lane) * ROWB, ROWB, bar);
+      if (lane == 0) bulk_copy_g2s(smem_u32(vb), vg + static_cast<int64_t>(base) * ROWB, nrow * ROWB, bar);
       const bool valid = lane < nrow;
       const int kp = (valid && pg) ? __ldg(pg + base + lane) : INT_MIN;
       const bool ok = __all_sync(kAll, mbar_wait(bar, phase, abort_flag));
@@ -341,10 +344,10 @@ __global__ void __launch_bounds__(kEngThreads, RR >= 16 ? 2 : 3) engine_bulk_ker
       float s[RR];
 #pragma unroll
       for (int h = 0; h < RR; ++h) s[h] = 0.f;
-      const uint4* krow = reinterpret_cast<const uint4*>(kb + lane * ROWB);
+      const uint4* krow = reinterpret_cast<const uint4*>(kb + lane * ROWP);
 #pragma unroll 4
       for (int v = 0; v < CH; ++v) {
-        const int cidx = (v + lane) & (CH - 1);
+        const int cidx = v;                     // the padding puts the lanes in different banks
         const uint4 w = krow[cidx];
         const uint32_t rw[4] = {w.x, w.y, w.z, w.w};
         float x[8];
@@ -453,8 +456,8 @@ cudaError_t launch_engine(const DecodeArgs& a, cudaStream_t stream) {
   const bool bf = !a.has_pools || a.pool_lo == KVC_POOL_BF16;
   const int rr = a.G <= 1 ? 1 : a.G <= 2 ? 2 : a.G <= 4 ? 4 : a.G <= 8 ? 8 : 16;
   if (bf) {
-    // bulk-staged kernel: 2 x 4 warps x 32 rows x 2d bytes of dynamic shared memory
-    const size_t smem = static_cast<size_t>(2) * kEngWarps * 32 * a.d * 2;
+    // bulk-staged kernel: 4 warps x 32 rows x (padded key row + value row) of dynamic shared memory
+    const size_t smem = static_cast<size_t>(kEngWarps) * 32 * (a.d * 2 + 16 + a.d * 2);   // padded key rows + value rows
     void (*k)(const DecodeArgs) = nullptr;
     if (a.d == 64)
       k = rr == 1 ? engine_bulk_kernel<64, 1> : rr == 2 ? engine_bulk_kernel<64, 2> : rr == 4 ? engine_bulk_kernel<64, 4>
