@@ -217,9 +217,16 @@ kvc_status plan_select(const kvc_shape* s, const kvc_policy* pol, SelectPlan* sp
 int decode_splits(const kvc_shape* s, const kvc_policy* pol, int sms) {
   const int64_t U = n_units(s);
   const int64_t rows = static_cast<int64_t>(pol->capacity) * (pol->budget_bytes > 0 ? 3 : 1);
-  // about eight CTAs (32 warps) per SM to keep enough row loads in flight,
-  // but no split shorter than 128 rows
-  int64_t want = (8LL * sms + U - 1) / U;
+  // byte mode (the register kernel): about eight CTAs (32 warps) per SM to
+  // keep enough row loads in flight; bf16 pools (the bulk-staged kernel,
+  // three CTAs per SM): as many splits as fit one wave of resident CTAs, so
+  // that no CTA waits for a second wave and most units need no merge; no
+  // split shorter than 128 rows
+  int64_t want = pol->budget_bytes > 0 ? (8LL * sms + U - 1) / U : std::max<int64_t>(1, 3LL * sms / U);
+  if (const char* e = getenv("KVC_DECODE_SPLITS")) {       // tuning override
+    const int v = atoi(e);
+    if (v >= 1 && v <= 32) want = v;
+  }
   const int64_t most = std::max<int64_t>(1, (rows + 127) / 128);
   want = std::min<int64_t>(std::min<int64_t>(want, most), 32);
   return static_cast<int>(std::max<int64_t>(want, 1));
@@ -254,7 +261,11 @@ kvc_status plan_engine(const kvc_shape* s, const kvc_policy* pol, int32_t n_q, b
   DevInfo info;
   if ((st = check_device(&info)) != KVC_OK) return st;
   const int64_t U = n_units(s);
-  int64_t want = (8LL * info.sms + U - 1) / U;
+  // the register kernel (int8 / int4 pools): about eight CTAs per SM; the
+  // bulk-staged kernel (bf16 storages): one wave of resident CTAs
+  const int per_sm = rows >= 16 ? 2 : 3;
+  int64_t want = p->byte_mode ? (8LL * info.sms + U - 1) / U
+                              : std::max<int64_t>(1, static_cast<int64_t>(per_sm) * info.sms / U);
   want = std::min<int64_t>(std::min<int64_t>(want, std::max<int64_t>(1, (keys + 127) / 128)), 32);
   p->splits = static_cast<int>(std::max<int64_t>(want, 1));
   p->rows = static_cast<int>(rows);

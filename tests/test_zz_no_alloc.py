@@ -66,7 +66,11 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(kvc):
     """A request whose scratch would exceed 2 MiB is refused before any launch."""
     from budgeted_kv_cache_gb300 import Policy, Pools, make_shape
     shape = make_shape(1, 75, 32, 4, 128, 4096)       # 300 units, 8 query heads per KV head
-    pol = Policy(budget_tokens=512, capacity=512)
+    # byte mode: the register decode kernel splits each unit over several
+    # CTAs (bf16-only pools run one wave and need little scratch)
+    u8 = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    pol = Policy(budget_bytes=1 << 20, capacity=4096, n_tags=1, n_layer_groups=1, tags=u8,
+                 action_table=u8)
     need = kvc.kvc_decode_workspace_bytes(shape, pol)
     if need <= (2 << 20):
         pytest.skip("this device's split count keeps the request within the scratch")
