@@ -147,20 +147,7 @@ def dist_setup():
     return world, rank, local
 
 
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+from budgeted_kv_cache_gb300.sharding import barrier, max_over_ranks  # noqa: E402
 
 
 # ---------------------------------------------------------------------------- oracle timing
