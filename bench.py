@@ -470,6 +470,36 @@ def run_gpu(args, w, world, rank, local):
         t_cref = statistics.mean(t_c)
         del rk_out, rp_out
 
+    # the same pass captured once as a CUDA graph and replayed (launch overhead check)
+    graph_ms = None
+    try:
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"],
+                  x["rope_sin"], x.get("bonus"), stream=gs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs, capture_error_mode="thread_local"):
+            p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"],
+                  x["rope_sin"], x.get("bonus"), stream=gs)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        t_g = []
+        for _ in range(10):
+            flush.fill_(1)
+            d0, d1 = ev(), ev()
+            d0.record()
+            graph.replay()
+            d1.record()
+            torch.cuda.synchronize()
+            t_g.append(d0.elapsed_time(d1))
+        graph_ms = statistics.mean(t_g)
+        del graph
+    except Exception as exc:                     # reported, not fatal: the eager pass is the metric
+        graph_ms = f"capture failed: {exc!r}"[:200]
+
     # CommitKV (Sec. 3.2-3.3), timed separately
     t_eff = None if args.no_commitkv else commitkv_stage(dev, stream, flush)
 
@@ -553,7 +583,13 @@ def run_gpu(args, w, world, rank, local):
                       "compact": statistics.mean(t_compact), "decode": t_decode,
                       "compact_reference_store": t_cref, **t_eng, **t_h2o, **t_var, **(t_eff or {})},
         "pass_roofline": {"t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_step,
-                          "algorithmic_bytes": ab["total"], "algorithmic_flops": flops},
+                          "algorithmic_bytes": ab["total"], "algorithmic_flops": flops,
+                          # informational: one exponential per window logit (U R T) at the
+                          # measured 30 ex2 results per clock per SM and the sampled SM clock
+                          "t_exp_ms": 1e3 * wr.n_units * wr.rows_per_unit * wr.n_tokens
+                                      / (30.0 * torch.cuda.get_device_properties(dev).multi_processor_count
+                                         * ((clocks or {}).get("sm_mhz") or 2070.0) * 1e6)},
+        "graph_ms_per_step": graph_ms,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": 3 * args.steps, "clocks": clocks,
     }
