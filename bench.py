@@ -36,13 +36,12 @@ import workloads as wl  # noqa: E402
 
 METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or TC util)"
 
-# DRAM bytes (read + write) of one score_kernel launch, per unit, from the ncu
-# capture summarised in profiles/score_kernel_qwen3_8b_T32768_4layers.md
-# (32 units: 274,451,968 B read + 6,573,568 B written).  Traffic grows with the
-# number of units (each unit's keys are read once), so a launch moves
-# bytes_per_unit x units.  Valid only for the kernel source with this SHA-1;
-# after any change the bench reports traffic as null until it is measured again.
-SCORE_TRAFFIC = {"sha1": "a80fb9d505362f2abb3058f0e76bf5d5e68e41c2", "bytes_per_unit": (275224064 + 7888640) / 32}
+# DRAM bytes (read + write) of one score_kernel launch, per unit: the full
+# 288-unit launch of this workload captured with ncu's DRAM byte counters (one
+# replay pass; profiles/score_kernel_traffic_qwen3_8b_T32768.md).  Valid while
+# the kernel and its launch plan (score_tc.cu, kvc_api.cu) are the captured
+# ones, else reported as null.
+SCORE_TRAFFIC = {"sha1": "73695e850d52cd7a6c2976bd32d0c23da4dc4ea7", "bytes_per_unit": (4737061888 + 26635008) / 288}
 UNIT = "tokens/s (summed over layer x KV-head units)"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -71,10 +70,12 @@ def algorithmic_bytes(w, kept_per_unit: int) -> dict:
 
 def score_traffic(n_units: int):
     import hashlib
-    src = os.path.join(ROOT, "budgeted_kv_cache_gb300", "csrc", "score_tc.cu")
-    with open(src, "rb") as f:
-        if hashlib.sha1(f.read()).hexdigest() != SCORE_TRAFFIC["sha1"]:
-            return None
+    h = hashlib.sha1()
+    for name in ("score_tc.cu", "kvc_api.cu"):
+        with open(os.path.join(ROOT, "budgeted_kv_cache_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != SCORE_TRAFFIC["sha1"]:
+        return None
     return SCORE_TRAFFIC["bytes_per_unit"] * n_units
 
 
