@@ -40,8 +40,9 @@ METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or
 # 288-unit launch of this workload captured with ncu's DRAM byte counters (one
 # replay pass; profiles/score_kernel_traffic_qwen3_8b_T32768.md).  Valid while
 # the kernel and its launch plan (score_tc.cu, kvc_api.cu) are the captured
-# ones, else reported as null.
-SCORE_TRAFFIC = {"sha1": "73695e850d52cd7a6c2976bd32d0c23da4dc4ea7", "bytes_per_unit": (4737061888 + 26635008) / 288}
+# ones (the kernel's source and the plan_score function that sizes its work
+# items), else reported as null.
+SCORE_TRAFFIC = {"sha1": "22f8a641ad5cc924d76ba3f168a23191d1e1184b", "bytes_per_unit": (4737061888 + 26635008) / 288}
 UNIT = "tokens/s (summed over layer x KV-head units)"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -70,10 +71,14 @@ def algorithmic_bytes(w, kept_per_unit: int) -> dict:
 
 def score_traffic(n_units: int):
     import hashlib
+    csrc = os.path.join(ROOT, "budgeted_kv_cache_gb300", "csrc")
     h = hashlib.sha1()
-    for name in ("score_tc.cu", "kvc_api.cu"):
-        with open(os.path.join(ROOT, "budgeted_kv_cache_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    with open(os.path.join(csrc, "score_tc.cu"), "rb") as f:
+        h.update(f.read())
+    with open(os.path.join(csrc, "kvc_api.cu")) as f:
+        api = f.read()
+    i = api.find("kvc_status plan_score(")
+    h.update(api[i:api.index("\n}\n", i) + 3].encode() if i >= 0 else b"")
     if h.hexdigest() != SCORE_TRAFFIC["sha1"]:
         return None
     return SCORE_TRAFFIC["bytes_per_unit"] * n_units

@@ -319,6 +319,10 @@ kvc_status plan_effect(const kvc_shape* s, int32_t window, EffectPlan* p) {
   // the two passes, and there are about two items per SM
   const int64_t want = (U * p->n_tiles + 2 * info.sms - 1) / (2 * info.sms);
   p->chunk = static_cast<int>(std::min<int64_t>(std::max<int64_t>(want, 2), 8));
+  if (const char* e = getenv("KVC_EFFECT_CHUNK_TILES")) {          // tuning override
+    const int v = atoi(e);
+    if (v >= 1 && v <= 1 << 20) p->chunk = v;
+  }
   p->chunk = std::min(p->chunk, p->n_tiles);
   p->splits = (p->n_tiles + p->chunk - 1) / p->chunk;
   const int64_t items = U * p->splits;
