@@ -401,6 +401,8 @@ kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_
   a.q_rows = p.q_rows;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.row_lse = row_lse;
+  a.stall_unit = -1;
+  if (const char* e = getenv("KVC_TEST_STALL_UNIT")) a.stall_unit = atoi(e);   // failure test only
   a.bonus = bonus;
   a.scores = scores;
   a.page_scores = page_size > 1 ? page_scores : nullptr;

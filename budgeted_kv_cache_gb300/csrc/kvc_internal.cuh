@@ -41,6 +41,7 @@ struct ScoreArgs {
   int32_t* unit_status;
   uint32_t* counters;          // [U] pass-1 chunks finished per unit
   float2* stats;               // [U][S][R] (max, sum) in the log2 domain
+  int32_t stall_unit;            // test hook (-1 = none): this unit's pass-1 wait never completes
   const __nv_bfloat16* k_small;  // small-window path: keys [U][T][d]
   const __nv_bfloat16* q_small;  // small-window path: window rows [U][R][d]
 };

@@ -399,13 +399,14 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     uint32_t jt = 0;           // tile counter of both passes (TMEM buffer, phase)
     uint32_t jt2 = 0;          // pass-2 tile counter (reduction slot, phase, finalizer)
     bool fail = false;
-    int cur_u = -1;
+    int cur_u = -1, cur_it = -1;
     for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
       const int u = it / S, c = it % S;
       const int t0 = c * a.chunk_tiles;
       const int nt = min(a.chunk_tiles, a.n_tiles - t0);
       const int b = u / (a.L * a.Hkv);
       cur_u = u;
+      cur_it = it;
 
       if (a.row_lse == nullptr) {
         // ---------------- pass 1: per-row online max / sum (log2 domain)
@@ -458,7 +459,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
           atom_add_release_gpu(&a.counters[u], 1u);
           uint64_t t_start = 0;
           for (uint32_t n = 0;; ++n) {
-            if (ld_acquire_gpu(&a.counters[u]) >= static_cast<uint32_t>(S)) break;
+            // (a.stall_unit: a test raises one unit's target to a count nothing reaches)
+            if (ld_acquire_gpu(&a.counters[u]) >= static_cast<uint32_t>(S + (u == a.stall_unit))) break;
             if (*abort_flag) {
               timed_out = true;
               break;
@@ -647,7 +649,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       fail = named_bar_or(1, kEpiThreads, fail);
       if (fail) break;
     }
-    if (fail && et == 0 && cur_u >= 0 && a.unit_status) a.unit_status[cur_u] = KVC_UNIT_TIMEOUT;
+    // a CTA that gave up leaves its current item and every later one
+    // unscored: all their units are marked
+    if (fail && et == 0 && cur_it >= 0 && a.unit_status)
+      for (int it = cur_it; it < a.n_items; it += gridDim.x) a.unit_status[it / S] = KVC_UNIT_TIMEOUT;
   }
 
   tc_fence_before();

@@ -1,0 +1,124 @@
+"""Failure detection and determinism on the GPU, without faulting it.
+
+Data-dependent failures are written per unit to `unit_status`; no kernel
+traps.  A device wait that cannot complete gives up after its bound (2 s):
+the test stalls one unit's cross-CTA wait through the library's test hook
+(its completion target is raised to a count nothing reaches), and checks
+that exactly that unit reports KVC_UNIT_TIMEOUT, that the other unit's
+scores are correct, and that the GPU context stays usable.  Determinism: the
+same inputs twice give identical bytes.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+import workloads as wl
+from helpers import assert_scores_close, bits, unit_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from budgeted_kv_cache_gb300 import build
+    build.build()
+    import budgeted_kv_cache_gb300 as lib
+    lib.library()
+    return lib
+
+
+def _pass(w):
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    x = wl.make_inputs(w, device="cuda")
+    return pass_for_workload(w, inputs=x), x
+
+
+def test_a_wait_that_cannot_complete_reports_timeout(kvc, monkeypatch):
+    w = wl.tiny()                                      # 2 units, window rows on the tensor cores
+    p, x = _pass(w)
+    monkeypatch.setenv("KVC_TEST_STALL_UNIT", "1")
+    p.score(x["k_cache"], x["q_window"], x.get("bonus"))
+    torch.cuda.synchronize()
+    status = p.score_status.cpu().numpy()
+    assert status[1] == kvc.UNIT_TIMEOUT and status[0] == kvc.UNIT_OK
+    ui = unit_inputs(w, x, 0)
+    ref = o.unit_scores(ui["k"], ui["q"], 1 / math.sqrt(w.head_dim), ui["bonus"])
+    assert_scores_close(p.scores[0].cpu().numpy(), ref)
+    # the context is still usable: the same call without the stall succeeds
+    monkeypatch.delenv("KVC_TEST_STALL_UNIT")
+    p.score_status.zero_()
+    p.score(x["k_cache"], x["q_window"], x.get("bonus"))
+    torch.cuda.synchronize()
+    assert int(p.score_status.abs().sum()) == 0
+
+
+def test_kept_index_out_of_range_marks_its_unit(kvc):
+    w = wl.tiny()
+    p, x = _pass(w)
+    p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"], x["rope_sin"],
+          x.get("bonus"))
+    torch.cuda.synchronize()
+    assert int(p.compact_status.abs().sum()) == 0
+    p.kept_idx[2, 0, 5] = w.n_tokens + 5               # bf16 pool of unit 0
+    p.compact(x["k_cache"], x["v_cache"], x["pos_in"], x["rope_cos"], x["rope_sin"])
+    torch.cuda.synchronize()
+    st = p.compact_status.cpu().numpy()
+    assert st[0] == o.UNIT_BAD_INDEX and st[1] == o.UNIT_OK
+
+
+def test_rope_table_shorter_than_the_positions_marks_the_units(kvc):
+    w = wl.tiny()                                      # renumbering: kept keys rotate
+    p, x = _pass(w)
+    p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"], x["rope_sin"],
+          x.get("bonus"))
+    cap = p.policy.capacity
+    # shorter than the new positions (0 .. capacity - 1): refused before any launch
+    with pytest.raises(kvc.KvcError) as e:
+        p.compact(x["k_cache"], x["v_cache"], x["pos_in"], x["rope_cos"][:cap - 1].contiguous(),
+                  x["rope_sin"][:cap - 1].contiguous())
+    assert e.value.code == 1
+    # long enough for the new positions, shorter than the old ones (up to T - 1):
+    # the kernel marks every unit whose kept keys it cannot rotate
+    p.compact_status.zero_()
+    p.compact(x["k_cache"], x["v_cache"], x["pos_in"], x["rope_cos"][:cap].contiguous(),
+              x["rope_sin"][:cap].contiguous())
+    torch.cuda.synchronize()
+    assert (p.compact_status.cpu().numpy() == o.UNIT_BAD_INDEX).all()
+
+
+def test_the_pass_and_the_deletion_effect_are_deterministic(kvc):
+    w = wl.qwen3_8b_32k().replace(name="det", n_layers=2, n_kv_heads=2, n_q_heads=8, n_tokens=3000,
+                                  budget_tokens=512, decode_pos=512)
+    p, x = _pass(w)
+    args = (x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"], x["rope_sin"],
+            x.get("bonus"))
+    p.run(*args)
+    first = [t.clone() for t in (p.scores, p.kept_idx, p.kept_count, p.pools.k_bf16, p.pools.v_bf16,
+                                 p.pools.pos_out)]
+    p.run(*args)
+    torch.cuda.synchronize()
+    again = (p.scores, p.kept_idx, p.kept_count, p.pools.k_bf16, p.pools.v_bf16, p.pools.pos_out)
+    for a, b in zip(first, again):
+        assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.uint8) if b.dtype == torch.bfloat16 else b)
+    we = wl.commitkv_effect_small()
+    xe = wl.make_effect_inputs(we, "cuda")
+    es = kvc.make_shape(we.batch, we.n_layers, we.n_q_heads, we.n_kv_heads, 128, we.n_tokens)
+    ws = torch.empty(kvc.kvc_deletion_effect_workspace_bytes(es, we.window), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for _ in range(2):
+        rec = kvc.EffectRecord(es, we.window, we.n_pages)
+        eff = torch.empty((we.batch, we.n_layers, we.n_pages), device="cuda")
+        kvc.kvc_deletion_effect(es, xe["k_cache"], xe["v_cache"], xe["q_minus"], we.window, 0.0,
+                                xe["page_start"], xe["page_len"], eff, rec, ws)
+        torch.cuda.synchronize()
+        outs.append((eff.clone(), rec.o.clone(), rec.u.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
