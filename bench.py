@@ -42,7 +42,7 @@ METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or
 # the kernel and its launch plan (score_tc.cu, kvc_api.cu) are the captured
 # ones (the kernel's source and the plan_score function that sizes its work
 # items), else reported as null.
-SCORE_TRAFFIC = {"sha1": "22f8a641ad5cc924d76ba3f168a23191d1e1184b", "bytes_per_unit": (4737061888 + 26635008) / 288}
+SCORE_TRAFFIC = {"sha1": "9ac6a9416f61340b20baa4c9ef882afefd28901b", "bytes_per_unit": (4738432768 + 26530560) / 288}
 UNIT = "tokens/s (summed over layer x KV-head units)"
 L2_FLUSH_BYTES = 256 << 20
 

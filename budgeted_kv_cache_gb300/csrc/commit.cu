@@ -340,12 +340,13 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
     uint32_t jt = 0, jp = 0;
     int li = 0;
     bool fail = false;
-    int cur_u = -1;
+    int cur_u = -1, cur_it = -1;
     for (int it = it0; it < it1; ++it, ++li) {
       const int u = it / SP, c = it % SP;
       const int t0 = c * a.chunk_tiles;
       const int nt = min(a.chunk_tiles, a.n_tiles - t0);
       cur_u = u;
+      cur_it = it;
       // ---- pass 1: online max / sum of y = z * cs over this thread's tokens
       float m = -INFINITY, l = 0.f;
       for (int t = 0; t < nt; ++t, ++jt) {
@@ -460,7 +461,10 @@ effect_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
       fail = named_bar_or(1, kEffEpiThreads, fail);
       if (fail) break;
     }
-    if (fail && et == 0 && cur_u >= 0 && a.unit_status) a.unit_status[cur_u] = KVC_UNIT_TIMEOUT;
+    // a CTA that gave up leaves its current item and the rest of its range
+    // unprocessed: all their units are marked
+    if (fail && et == 0 && cur_it >= 0 && a.unit_status)
+      for (int it = cur_it; it < it1; ++it) a.unit_status[it / SP] = KVC_UNIT_TIMEOUT;
   }
 
   tc_fence_before();
