@@ -42,7 +42,7 @@ METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or
 # the kernel and its launch plan (score_tc.cu, kvc_api.cu) are the captured
 # ones (the kernel's source and the plan_score function that sizes its work
 # items), else reported as null.
-SCORE_TRAFFIC = {"sha1": "9ac6a9416f61340b20baa4c9ef882afefd28901b", "bytes_per_unit": (4738432768 + 26530560) / 288}
+SCORE_TRAFFIC = {"sha1": "93edc597c1b1579fb3971d4087d1dc7d91123fbf", "bytes_per_unit": (4738432768 + 26530560) / 288}
 UNIT = "tokens/s (summed over layer x KV-head units)"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -69,16 +69,24 @@ def algorithmic_bytes(w, kept_per_unit: int) -> dict:
     return dict(score=score, select=select, compact=compact, total=score + select + compact)
 
 
+def _code(src: str) -> str:
+    """Source text without comments and blank lines (the key ignores comment edits)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
+
+
 def score_traffic(n_units: int):
     import hashlib
     csrc = os.path.join(ROOT, "budgeted_kv_cache_gb300", "csrc")
     h = hashlib.sha1()
-    with open(os.path.join(csrc, "score_tc.cu"), "rb") as f:
-        h.update(f.read())
+    with open(os.path.join(csrc, "score_tc.cu")) as f:
+        h.update(_code(f.read()).encode())
     with open(os.path.join(csrc, "kvc_api.cu")) as f:
         api = f.read()
     i = api.find("kvc_status plan_score(")
-    h.update(api[i:api.index("\n}\n", i) + 3].encode() if i >= 0 else b"")
+    h.update(_code(api[i:api.index("\n}\n", i) + 3]).encode() if i >= 0 else b"")
     if h.hexdigest() != SCORE_TRAFFIC["sha1"]:
         return None
     return SCORE_TRAFFIC["bytes_per_unit"] * n_units

@@ -15,11 +15,13 @@
 //           epilogue thread owns one token and sums exp(z - lse) over rows,
 //           so neither pass needs a cross-thread reduction.
 // A unit's T keys are split into work items of `chunk_tiles` 128-token
-// tiles; one persistent CTA per SM walks the items round-robin.  After pass
-// 1 of an item its row statistics are published and a per-unit counter is
-// bumped; pass 2 starts once every item of the unit has published, so the
-// log-sum-exp of each row is exact.  The items of a round cover a contiguous
-// range of units, so the keys read by pass 1 are still in L2 for pass 2.
+// tiles (the host picks the size: few, large items when there are enough
+// units, since every item carries a fixed cost); one persistent CTA per SM
+// walks the items round-robin.  After pass 1 of an item its row statistics
+// are published and a per-unit counter is bumped; pass 2 starts once every
+// item of the unit has published, so the log-sum-exp of each row is exact.
+// When the items of a round are small their keys are still in L2 for pass
+// 2; whole-unit items read them from HBM again.
 // Co-residency of all CTAs (needed by that wait) is guaranteed by launching
 // cooperatively; every wait is bounded in time.
 //
