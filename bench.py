@@ -573,9 +573,9 @@ def run_gpu(args, w, world, rank, local):
     if world == 1 and not args.no_cpu_baseline:
         ws = wr.replace(n_layers=1, n_kv_heads=1, n_q_heads=wr.group)
         xh = wl.make_inputs(ws, device="cpu")
-        done, dt, threads = oracle_sample(ws, xh, seconds=args.cpu_seconds, max_units=64)
+        done, dt, threads = oracle_sample(ws, xh, seconds=args.cpu_seconds, max_units=1024)
         cpu = {"value": done * ws.n_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{done} whole (layer, KV head) unit(s) of {wr.name} "
+               "sample": f"{done} passes over one whole (layer, KV head) unit of {wr.name} "
                          f"(score+select+compact, numpy fp64), {dt:.1f} s"}
 
     line = {
