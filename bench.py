@@ -197,6 +197,13 @@ def oracle_sample(w, x_host, seconds: float, max_units: int):
     return done, dt, threads
 
 
+def _config(w) -> dict:
+    """The workload both arms name in their JSON line."""
+    return {"workload": w.name, "units": w.n_units, "n_tokens": w.n_tokens,
+            "budget": w.budget_tokens, "window": w.window, "head_dim": w.head_dim,
+            "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "layers": w.n_layers}
+
+
 def run_reference(args, w, world, rank):
     if rank != 0:
         return
@@ -218,8 +225,7 @@ def run_reference(args, w, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "units_per_step": 1, "n_tokens": w.n_tokens,
-                   "budget": w.budget_tokens, "window": w.window, "head_dim": w.head_dim},
+        "config": _config(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"1 of {w.n_units} (layer, KV head) units per step, "
                                    f"score+select+compact, numpy fp64"},
@@ -582,10 +588,7 @@ def run_gpu(args, w, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wr.name, "units": wr.n_units, "n_tokens": wr.n_tokens,
-                   "budget": wr.budget_tokens, "window": wr.window, "head_dim": wr.head_dim,
-                   "q_heads": wr.n_q_heads, "kv_heads": wr.n_kv_heads, "layers": wr.n_layers,
-                   "parallelism": f"replicas x{world}",
+        "config": {**_config(wr), "parallelism": f"replicas x{world}",
                    "l2": "256 MiB buffer written between timed steps; K/V inputs (2.4 GB each) exceed L2"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": score_traffic(wr.n_units),
