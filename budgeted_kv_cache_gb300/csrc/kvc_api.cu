@@ -294,6 +294,23 @@ kvc_status plan_engine(const kvc_shape* s, const kvc_policy* pol, int32_t n_q, b
   return KVC_OK;
 }
 
+// The address the device reads `*p` through: device or managed memory as it
+// is, page-locked host memory through its mapping (unregistered host memory
+// is refused).
+kvc_status device_view(const void** p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, *p) != cudaSuccess) {
+    cudaGetLastError();
+    return KVC_ERR_INVALID_ARG;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return KVC_OK;
+  if (at.type == cudaMemoryTypeHost && at.devicePointer) {
+    *p = at.devicePointer;
+    return KVC_OK;
+  }
+  return KVC_ERR_INVALID_ARG;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- CommitKV plans
@@ -606,6 +623,14 @@ kvc_status kvc_compact_rerotate_quant_ref(const kvc_shape* shape, const kvc_poli
   if (rd < 16 || rd > shape->head_dim || rd % 16 != 0) return KVC_ERR_INVALID_ARG;
   DevInfo info;
   if ((st = check_device(&info)) != KVC_OK) return st;
+  // the caches and positions may sit in page-locked host memory: only the
+  // kept rows are read, in place, through the mapping
+  if ((st = device_view(&k_cache)) != KVC_OK || (st = device_view(&v_cache)) != KVC_OK) return st;
+  {
+    const void* p = pos_in;
+    if ((st = device_view(&p)) != KVC_OK) return st;
+    pos_in = static_cast<const int32_t*>(p);
+  }
   CompactArgs a = {};
   if (ref) a.ref = *ref;
   a.rope_layout = policy->rope_layout;

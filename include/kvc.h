@@ -22,7 +22,7 @@
  *
  * Conventions shared by every entry point
  *   - Every data pointer is DEVICE memory of the current CUDA device, owned
- *     by the caller.  The library keeps no pointer after a call returns and
+ *     by the caller, unless a call says otherwise.  The library keeps no pointer after a call returns and
  *     allocates no device memory; scratch space is the caller's workspace,
  *     sized by the matching *_workspace_bytes call.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
@@ -307,7 +307,13 @@ typedef struct {
  * round-half-even(x / scale) clipped to [-qmax, qmax], qmax 7 (int4) or 127
  * (int8); an all-zero group stores zero codes and scale 1.
  *
+ * k_cache, v_cache  bf16 [B][L][H_kv][T][d], as for kvc_score.
  * pos_in       int32 [U][T] physical position of each cached row.
+ *              These three may also be page-locked host memory registered
+ *              with CUDA (cudaHostAlloc, cudaHostRegister): the kept rows
+ *              are then read in place through the device mapping, so a cache
+ *              offloaded to host memory is not copied whole.  Unregistered
+ *              host memory: KVC_ERR_INVALID_ARG.
  * kept_idx, kept_count  as written by kvc_select.
  * rope_cos, rope_sin    fp32 [rope_max_pos][d/2]: cos / sin of p theta_i.
  *              Every old and new position must be < rope_max_pos; a row

@@ -191,6 +191,35 @@ def test_inactive_pass_is_bytewise_identity(kvc):
     assert torch.equal(p.pools.v_bf16.view(w.n_units, 640, -1), x["v_cache"].view(w.n_units, 640, -1))
 
 
+@pytest.mark.parametrize("idx", [2, 4], ids=["token_mode", "byte_mode"])
+def test_host_resident_cache_is_read_in_place(kvc, idx):
+    """Keys, values and positions in page-locked host memory: compaction reads
+    the kept rows through the device mapping and stores the same bytes as
+    from device memory; unregistered host memory is refused before a launch."""
+    import dataclasses
+    w = small_workloads()[idx]
+    x = wl.make_inputs(w, device="cuda")
+    p = run_pass(w, x)
+    pools = [getattr(p.pools, f.name) for f in dataclasses.fields(p.pools)]
+    pools = [t for t in pools if t is not None]
+    for t in pools:
+        t.view(torch.uint8).fill_(0x5A)
+    p.compact(x["k_cache"], x["v_cache"], x["pos_in"], x["rope_cos"], x["rope_sin"])
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in pools]
+    for t in pools:
+        t.view(torch.uint8).fill_(0x5A)
+    hk, hv, hp = (x[n].cpu().pin_memory() for n in ("k_cache", "v_cache", "pos_in"))
+    p.compact(hk, hv, hp, x["rope_cos"], x["rope_sin"])
+    torch.cuda.synchronize()
+    for a, b in zip(pools, ref):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert int(p.compact_status.abs().sum()) == 0
+    with pytest.raises(kvc.KvcError) as e:
+        p.compact(x["k_cache"], x["v_cache"].cpu(), x["pos_in"], x["rope_cos"], x["rope_sin"])
+    assert e.value.code == 1
+
+
 def test_over_budget_and_bad_flags(kvc):
     w = wl.tiny().replace(n_tokens=512, budget_tokens=16, n_sink=10, n_recent=10)
     x = wl.make_inputs(w, device="cuda")
