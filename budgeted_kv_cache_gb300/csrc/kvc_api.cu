@@ -294,16 +294,18 @@ kvc_status plan_engine(const kvc_shape* s, const kvc_policy* pol, int32_t n_q, b
   return KVC_OK;
 }
 
-// The address the device reads `*p` through: device or managed memory as it
-// is, page-locked host memory through its mapping (unregistered host memory
-// is refused).
+// The address the device reads `*p` through: memory of the current device
+// or managed memory as it is, page-locked host memory through its mapping
+// (unregistered host memory and another device's memory are refused).
 kvc_status device_view(const void** p) {
   cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, *p) != cudaSuccess) {
+  int dev = -1;
+  if (cudaPointerGetAttributes(&at, *p) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return KVC_ERR_INVALID_ARG;
   }
-  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return KVC_OK;
+  if (at.type == cudaMemoryTypeDevice) return at.device == dev ? KVC_OK : KVC_ERR_INVALID_ARG;
+  if (at.type == cudaMemoryTypeManaged) return KVC_OK;
   if (at.type == cudaMemoryTypeHost && at.devicePointer) {
     *p = at.devicePointer;
     return KVC_OK;
