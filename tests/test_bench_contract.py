@@ -60,3 +60,21 @@ def test_traffic_key_ignores_comments():
     bench = _bench()
     src = "int a; // note\n/* block\n comment */ int b;\n\n"
     assert bench._code(src) == bench._code("int a;\n int b;")
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched like the driver's N = 2 run (two ranks, gloo on a CPU host):
+    rank 0 alone runs the oracle and prints; the other rank exits cleanly."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600,
+                       env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2 and lines[0]["value"] > 0
