@@ -54,7 +54,7 @@ typedef void* kvc_stream;
 typedef enum {
   KVC_OK = 0,
   KVC_ERR_INVALID_ARG = 1,  /* a null pointer, a bad shape or size         */
-  KVC_ERR_UNSUPPORTED = 2,  /* a valid request this build does not handle */
+  KVC_ERR_UNSUPPORTED = 2,  /* a valid request the library does not handle */
   KVC_ERR_WORKSPACE = 3,    /* workspace missing or too small             */
   KVC_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed        */
   KVC_ERR_NO_DEVICE = 5     /* no usable sm_103 device                    */

@@ -63,12 +63,12 @@ def _compact(kvc, T, cap, k, v, pos, kept, cnt, cos, sin, ref_k, ref_pos):
     return pools, rk[2], rp[2], fails
 
 
-def test_reference_store_two_rounds_bit_exact(kvc):
+def test_reference_store_two_renumbers_bit_exact(kvc):
     rng = np.random.default_rng(11)
     T1, n1, n2 = 1000, 300, 150
     cos, sin = wl.rope_tables(1024, D, 1e4, device="cuda")
     cos_h, sin_h = cos.cpu().numpy(), sin.cpu().numpy()
-    # round 0: keys rotated at positions 0..T1-1
+    # before any renumber: keys rotated at positions 0..T1-1
     k1 = (torch.randn(U, T1, D, generator=torch.Generator().manual_seed(3)) * 2).to(torch.bfloat16).cuda()
     v1 = torch.randn(U, T1, D, generator=torch.Generator().manual_seed(4)).to(torch.bfloat16).cuda()
     pos1 = torch.arange(T1, dtype=torch.int32).repeat(U, 1).contiguous().cuda()
@@ -76,7 +76,7 @@ def test_reference_store_two_rounds_bit_exact(kvc):
     ref_p1 = torch.full((U, T1), -1, dtype=torch.int32, device="cuda")
     prm = o.PassParams(budget_tokens=n1, budget_bytes=0, n_sink=0, n_recent=0, page_size=1,
                        renumber=True, quant_mode=0, n_layer_groups=1)
-    # round 1: first renumber creates the references
+    # renumber 1: creates the references
     idx1, kept1, cnt1 = _kept(T1, n1, rng)
     pools1, rk1, rp1, f1 = _compact(kvc, T1, n1, k1, v1, pos1, kept1, cnt1, cos, sin, ref_k1, ref_p1)
     k2, v2 = pools1.k_bf16, pools1.v_bf16
@@ -86,11 +86,11 @@ def test_reference_store_two_rounds_bit_exact(kvc):
     stale_row = int(np.nonzero(rp1[1].cpu().numpy() >= 0)[0][-1])   # >= n2: its rank changes
     ref_k2_in = ref_k2.clone()
     ref_k2_in[1, stale_row, 0] = -ref_k2_in[1, stale_row, 0] if float(ref_k2_in[1, stale_row, 0]) != 0 else 1.0
-    # round 2: renumber again, from the references (the stale row is kept)
+    # renumber 2: from the references (the stale row is kept)
     idx2, kept2, cnt2 = _kept(n1, n2, rng, must={1: stale_row})
     pools2, rk2, rp2, f2 = _compact(kvc, n1, n2, k2, v2, pos2, kept2, cnt2, cos, sin, ref_k2_in, ref_p2)
     for u in range(U):
-        # oracle, round 1
+        # oracle, renumber 1
         act1 = np.zeros(T1, np.int64)
         act1[idx1[u]] = o.ACT_BF16
         ref1 = o.compact_unit(bits(k1[u]), bits(v1[u]), pos1[u].cpu().numpy(), act1, prm, cos_h, sin_h,
@@ -102,7 +102,7 @@ def test_reference_store_two_rounds_bit_exact(kvc):
         assert np.array_equal(bits(rk1[u]), p1.k_ref)
         assert np.array_equal(rp1[u].cpu().numpy(), p1.p_ref)
         assert int(f1[u]) == 0
-        # oracle, round 2 (from the round-1 outputs as the GPU saw them)
+        # oracle, renumber 2 (from the renumber-1 outputs as the GPU saw them)
         act2 = np.zeros(n1, np.int64)
         act2[idx2[u]] = o.ACT_BF16
         ref2 = o.compact_unit(bits(k2[u]), bits(v2[u]), pos2[u].cpu().numpy(), act2, prm, cos_h, sin_h,
