@@ -527,13 +527,14 @@ def run_gpu(args, w, world, rank, local):
     # scoring reads whole (keys, window queries, bonus) and the rotary tables
     # are copied in from pinned host memory; values and positions stay in
     # pinned host memory and compaction reads their kept rows in place; the
-    # compacted cache comes back.  The layers go in four groups: the keys of
-    # group g + 1 are copied (side stream) while group g is compacted and its
-    # results copied out, so only the last group's pass is not hidden.
+    # compacted cache comes back.  The layers go in groups (nine by default):
+    # the keys of group g + 1 are copied (side stream) while group g is
+    # compacted and its results copied out, so only the last group's pass is
+    # not hidden.
     e2e = None
     if not args.no_e2e:
         from budgeted_kv_cache_gb300.passes import pass_for_workload
-        n_groups = 4 if wr.batch == 1 and wr.n_layers % 4 == 0 else 1
+        n_groups = args.e2e_groups if wr.batch == 1 and wr.n_layers % max(args.e2e_groups, 1) == 0 else 1
         wg = wr.replace(n_layers=wr.n_layers // n_groups)
         gpasses = [p] if n_groups == 1 else [pass_for_workload(wg, inputs=x, device=dev)
                                               for _ in range(n_groups)]
@@ -667,6 +668,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=9,
+                    help="layer groups of the end-to-end leg (copies of one overlap the pass of another)")
     ap.add_argument("--no-commitkv", action="store_true",
                     help="skip the CommitKV deletion-effect and commit stages")
     ap.add_argument("--commitkv-only", action="store_true",
