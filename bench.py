@@ -38,7 +38,7 @@ METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or
 
 # DRAM bytes (read + write) of one score_kernel launch, per unit: the full
 # 288-unit launch of this workload captured with ncu's DRAM byte counters (one
-# replay pass; profiles/score_kernel_traffic_qwen3_8b_T32768.md).  Valid while
+# replay pass, the summary kept with the other profiles).  Valid while
 # the kernel and its launch plan (score_tc.cu, kvc_api.cu) are the captured
 # ones (the kernel's source and the plan_score function that sizes its work
 # items), else reported as null.

@@ -76,6 +76,12 @@ class kvc_effect_record(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("o", "lse", "s", "u")]
 
 
+class kvc_overrides(ctypes.Structure):
+    """Launch-plan overrides of kvc_set_overrides (tuning and failure tests)."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("score_chunk_tiles", "decode_splits",
+                                              "effect_chunk_tiles", "score_stall_unit")]
+
+
 class kvc_commit_thresholds(ctypes.Structure):
     """CommitKV Sec. 4.1 thresholds."""
     _fields_ = [(n, ctypes.c_float) for n in ("tau_use", "tau_dead", "rho_use", "rho_dead", "tau_joint")]
@@ -117,6 +123,7 @@ def _load():
                                                      P]),
             "kvc_protect_pending": (ctypes.c_int, [SH, I32, I32, P, P, P, I32, I32, P, P]),
             "kvc_commit_flags": (ctypes.c_int, [I32, I64, I32, P, P, P, P, P, P]),
+            "kvc_set_overrides": (ctypes.c_int, [ctypes.POINTER(kvc_overrides)]),
             "kvc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -225,6 +232,16 @@ class Pools:
 
 
 # ----------------------------------------------------------------------------- entry points
+
+def kvc_set_overrides(score_chunk_tiles: int = 0, decode_splits: int = 0,
+                      effect_chunk_tiles: int = 0, score_stall_unit: int = -1, reset: bool = False):
+    """Process-wide launch-plan overrides (tuning sweeps, failure tests); reset=True restores defaults."""
+    if reset:
+        _check("kvc_set_overrides", library().kvc_set_overrides(None))
+        return
+    o = kvc_overrides(score_chunk_tiles, decode_splits, effect_chunk_tiles, score_stall_unit)
+    _check("kvc_set_overrides", library().kvc_set_overrides(ctypes.byref(o)))
+
 
 def kvc_status_string(code: int) -> str:
     return _load().kvc_status_string(code).decode()

@@ -303,7 +303,12 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   const int u = blockIdx.y;
   const int U = a.U;
   const int cap = a.capacity;
-  const int cnt = __ldg(a.kept_count + pool * U + u);
+  // a count outside [0, capacity] is clamped (rows past the capacity would
+  // belong to the next unit) and reported as a bad index
+  const int cnt_raw = __ldg(a.kept_count + pool * U + u);
+  const int cnt = clamp_count(cnt_raw, cap);
+  if (cnt != cnt_raw && blockIdx.x == 0 && threadIdx.x == 0 && a.unit_status)
+    a.unit_status[u] = KVC_UNIT_BAD_INDEX;
   const int64_t i_base =
       (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kRows * rows_per_warp + sub;
   if (__all_sync(kFull, i_base >= cnt)) return;
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
         int rank = static_cast<int>(i_base + n * rows_per_warp);
         for (int q = 0; q < KVC_N_POOLS; ++q) {
           if (q == pool) continue;
-          const int cq = __ldg(a.kept_count + q * U + u);
+          const int cq = clamp_count(__ldg(a.kept_count + q * U + u), cap);
           if (cq > 0)
             rank += lower_bound_i32(a.kept_idx + (static_cast<int64_t>(q) * U + u) * cap, cq, t[n]);
         }

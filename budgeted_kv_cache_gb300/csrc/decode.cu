@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(kThreads, 6) decode_kernel(const DecodeArgs a)
   int n = 0;
 #pragma unroll
   for (int p = 0; p < KVC_N_POOLS; ++p) {
-    cnt[p] = (p >= a.pool_lo && p < a.pool_hi) ? a.kept_count[p * a.U + u] : 0;
+    // a count outside [0, capacity] is clamped, so no row past the pool is read
+    cnt[p] = (p >= a.pool_lo && p < a.pool_hi) ? clamp_count(a.kept_count[p * a.U + u], a.capacity) : 0;
     n += cnt[p];
   }
   const int per = (n + a.splits - 1) / a.splits;
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_bulk_kernel(const DecodeAr
       qs[idx / D][idx % D] = idx / D < G ? __bfloat162float(q[idx]) * cs : 0.f;
   }
   fence_barrier_init();
-  const int n = a.kept_count[KVC_POOL_BF16 * a.U + u];
+  const int n = clamp_count(a.kept_count[KVC_POOL_BF16 * a.U + u], a.capacity);
   const int per = (n + a.splits - 1) / a.splits;
   const int lo = min(n, split * per), hi = min(n, lo + per);
   __syncthreads();

@@ -92,9 +92,11 @@ engine_attn_kernel(const DecodeArgs a) {
 #pragma unroll
   for (int c = 0; c < kClasses; ++c) {
     int v = 0;
-    if (c < KVC_N_POOLS) v = (a.has_pools && c >= a.pool_lo && c < a.pool_hi) ? a.kept_count[c * a.U + u] : 0;
-    else if (c == KVC_N_POOLS) v = a.rec_count ? a.rec_count[u] : 0;
-    else v = a.cur_count ? a.cur_count[u] : 0;
+    // counts outside [0, capacity] are clamped, so no row past a storage is read
+    if (c < KVC_N_POOLS)
+      v = (a.has_pools && c >= a.pool_lo && c < a.pool_hi) ? clamp_count(a.kept_count[c * a.U + u], a.capacity) : 0;
+    else if (c == KVC_N_POOLS) v = a.rec_count ? clamp_count(a.rec_count[u], a.rec_cap) : 0;
+    else v = a.cur_count ? clamp_count(a.cur_count[u], a.cur_cap) : 0;
     cnt[c] = v;
     n += v;
   }
@@ -269,9 +271,10 @@ __global__ void __launch_bounds__(kEngThreads, RR >= 16 ? 2 : 3) engine_bulk_ker
   }
   fence_barrier_init();
   int cnt[3];
-  cnt[0] = a.has_pools ? a.kept_count[KVC_POOL_BF16 * a.U + u] : 0;
-  cnt[1] = a.rec_count ? a.rec_count[u] : 0;
-  cnt[2] = a.cur_count ? a.cur_count[u] : 0;
+  // counts outside [0, capacity] are clamped, so no row past a storage is read
+  cnt[0] = a.has_pools ? clamp_count(a.kept_count[KVC_POOL_BF16 * a.U + u], a.capacity) : 0;
+  cnt[1] = a.rec_count ? clamp_count(a.rec_count[u], a.rec_cap) : 0;
+  cnt[2] = a.cur_count ? clamp_count(a.cur_count[u], a.cur_cap) : 0;
   const int n = cnt[0] + cnt[1] + cnt[2];
   const int per = (n + a.splits - 1) / a.splits;
   const int lo = min(n, split * per), hi = min(n, lo + per);

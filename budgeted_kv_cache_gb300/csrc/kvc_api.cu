@@ -5,6 +5,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "kvc_internal.cuh"
@@ -12,6 +13,13 @@
 using namespace kvc;
 
 namespace {
+
+// Process-wide launch-plan overrides set through kvc_set_overrides (tuning
+// sweeps, failure tests); 0 / -1 = the library's own choice.
+std::atomic<int32_t> g_score_chunk_tiles{0};
+std::atomic<int32_t> g_decode_splits{0};
+std::atomic<int32_t> g_effect_chunk_tiles{0};
+std::atomic<int32_t> g_score_stall_unit{-1};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -137,10 +145,8 @@ kvc_status plan_score(const kvc_shape* s, int32_t window, ScorePlan* p) {
       chunk = c;
     }
   }
-  if (const char* e = getenv("KVC_SCORE_CHUNK_TILES")) {          // tuning override
-    const int v = atoi(e);
-    if (v >= 1 && v <= 1 << 20) chunk = v;
-  }
+  if (const int v = g_score_chunk_tiles.load(std::memory_order_relaxed); v >= 1)   // override
+    chunk = v;
   chunk = std::max(chunk, (p->n_tiles + p->grid - 1) / p->grid);   // S <= grid (co-resident unit)
   p->chunk_tiles = std::min(chunk, p->n_tiles);
   p->S = (p->n_tiles + p->chunk_tiles - 1) / p->chunk_tiles;
@@ -241,10 +247,7 @@ int decode_splits(const kvc_shape* s, const kvc_policy* pol, int sms) {
   // that no CTA waits for a second wave and most units need no merge; no
   // split shorter than 128 rows
   int64_t want = pol->budget_bytes > 0 ? (8LL * sms + U - 1) / U : std::max<int64_t>(1, 3LL * sms / U);
-  if (const char* e = getenv("KVC_DECODE_SPLITS")) {       // tuning override
-    const int v = atoi(e);
-    if (v >= 1 && v <= 32) want = v;
-  }
+  if (const int v = g_decode_splits.load(std::memory_order_relaxed); v >= 1) want = v;   // override
   const int64_t most = std::max<int64_t>(1, (rows + 127) / 128);
   want = std::min<int64_t>(std::min<int64_t>(want, most), 32);
   return static_cast<int>(std::max<int64_t>(want, 1));
@@ -338,10 +341,8 @@ kvc_status plan_effect(const kvc_shape* s, int32_t window, EffectPlan* p) {
   // the two passes, and there are about two items per SM
   const int64_t want = (U * p->n_tiles + 2 * info.sms - 1) / (2 * info.sms);
   p->chunk = static_cast<int>(std::min<int64_t>(std::max<int64_t>(want, 2), 8));
-  if (const char* e = getenv("KVC_EFFECT_CHUNK_TILES")) {          // tuning override
-    const int v = atoi(e);
-    if (v >= 1 && v <= 1 << 20) p->chunk = v;
-  }
+  if (const int v = g_effect_chunk_tiles.load(std::memory_order_relaxed); v >= 1)   // override
+    p->chunk = v;
   p->chunk = std::min(p->chunk, p->n_tiles);
   p->splits = (p->n_tiles + p->chunk - 1) / p->chunk;
   const int64_t items = U * p->splits;
@@ -364,6 +365,18 @@ kvc_status plan_effect(const kvc_shape* s, int32_t window, EffectPlan* p) {
 }
 
 extern "C" {
+
+kvc_status kvc_set_overrides(const kvc_overrides* o) {
+  if (o && (o->score_chunk_tiles < 0 || o->score_chunk_tiles > (1 << 20) || o->decode_splits < 0 ||
+            o->decode_splits > 32 || o->effect_chunk_tiles < 0 || o->effect_chunk_tiles > (1 << 20) ||
+            o->score_stall_unit < -1))
+    return KVC_ERR_INVALID_ARG;
+  g_score_chunk_tiles.store(o ? o->score_chunk_tiles : 0);
+  g_decode_splits.store(o ? o->decode_splits : 0);
+  g_effect_chunk_tiles.store(o ? o->effect_chunk_tiles : 0);
+  g_score_stall_unit.store(o ? o->score_stall_unit : -1);
+  return KVC_OK;
+}
 
 const char* kvc_status_string(kvc_status status) {
   switch (status) {
@@ -420,8 +433,7 @@ kvc_status kvc_score(const kvc_shape* shape, const void* k_cache, const void* q_
   a.q_rows = p.q_rows;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.row_lse = row_lse;
-  a.stall_unit = -1;
-  if (const char* e = getenv("KVC_TEST_STALL_UNIT")) a.stall_unit = atoi(e);   // failure test only
+  a.stall_unit = g_score_stall_unit.load(std::memory_order_relaxed);   // failure test hook (-1: none)
   a.bonus = bonus;
   a.scores = scores;
   a.page_scores = page_size > 1 ? page_scores : nullptr;
@@ -985,19 +997,44 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;    // 2 MiB per device
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the symbol is only a host-side stand-in, so the address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and cached.
+// cudaGetSymbolAddress (with that device current) and cached per device,
+// together with the context it belongs to: after cudaDeviceReset the device
+// gets a new context and module, and the address is looked up again.
 kvc_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVC_ERR_NO_DEVICE;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (!get_ctx) return KVC_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return KVC_ERR_CUDA;     // NULL before the first runtime call
   static void* addr[64] = {};
+  static CUcontext owner[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || !ctx || owner[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVC_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return KVC_ERR_CUDA;
     addr[dev] = p;
+    owner[dev] = ctx;
   }
   *out = addr[dev];
   return KVC_OK;

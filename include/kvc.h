@@ -405,8 +405,10 @@ kvc_status kvc_decode_attn(const kvc_shape* shape, const kvc_policy* policy, con
  *   - Returns KVC_ERR_WORKSPACE if kvc_decode_workspace_bytes(shape, policy)
  *     exceeds 2 MiB (nothing is launched).
  *   - Calls no cudaMalloc / cudaFree.  The first call on a device looks up
- *     the array's device address (cudaGetSymbolAddress) and caches it; make
- *     that first call before any stream capture.
+ *     the array's device address (cudaGetSymbolAddress) and caches it with
+ *     the device's current context; make that first call before any stream
+ *     capture.  After cudaDeviceReset the device has a new context, and the
+ *     next call looks the address up again (again outside any capture).
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents; nothing in it needs to start at zero (every partition
  *     slot the merge reads is written earlier in the same call).  Calls that
@@ -586,6 +588,30 @@ kvc_status kvc_commit_flags(int32_t batch, int64_t n_tokens, int32_t n_pages,
                             const int32_t* page_start, const int32_t* page_len,
                             const uint8_t* retire, const uint8_t* protect, uint8_t* flags,
                             kvc_stream stream);
+
+/* ------------------------------------------------------------------------
+ * kvc_set_overrides -- process-wide overrides of the launch plans, for
+ * tuning sweeps and for failure-detection tests.  Not a step of the pages'
+ * methods; a production caller never needs it.  0 in a field keeps the
+ * library's own choice:
+ *   score_chunk_tiles   key tiles (of 128 rows) per kvc_score work item
+ *   decode_splits       split partitions per unit of kvc_decode_attn (<= 32)
+ *   effect_chunk_tiles  key tiles per kvc_deletion_effect work item
+ *   score_stall_unit    -1 = off.  Test hook: in kvc_score the pass-1 wait
+ *                       of this unit never completes, so after the bounded
+ *                       wait (2 s) that unit and every unit its CTA leaves
+ *                       unscored report KVC_UNIT_TIMEOUT.
+ * NULL restores every default.  Values out of range return
+ * KVC_ERR_INVALID_ARG and change nothing.  A call affects calls issued
+ * after it from any host thread; it does not synchronise with them.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t score_chunk_tiles;
+  int32_t decode_splits;
+  int32_t effect_chunk_tiles;
+  int32_t score_stall_unit;
+} kvc_overrides;
+kvc_status kvc_set_overrides(const kvc_overrides* overrides);
 
 /* Static text for a status code. */
 const char* kvc_status_string(kvc_status status);

@@ -39,19 +39,21 @@ def _pass(w):
     return pass_for_workload(w, inputs=x), x
 
 
-def test_a_wait_that_cannot_complete_reports_timeout(kvc, monkeypatch):
+def test_a_wait_that_cannot_complete_reports_timeout(kvc):
     w = wl.tiny()                                      # 2 units, window rows on the tensor cores
     p, x = _pass(w)
-    monkeypatch.setenv("KVC_TEST_STALL_UNIT", "1")
-    p.score(x["k_cache"], x["q_window"], x.get("bonus"))
-    torch.cuda.synchronize()
+    kvc.kvc_set_overrides(score_stall_unit=1)
+    try:
+        p.score(x["k_cache"], x["q_window"], x.get("bonus"))
+        torch.cuda.synchronize()
+    finally:
+        kvc.kvc_set_overrides(reset=True)
     status = p.score_status.cpu().numpy()
     assert status[1] == kvc.UNIT_TIMEOUT and status[0] == kvc.UNIT_OK
     ui = unit_inputs(w, x, 0)
     ref = o.unit_scores(ui["k"], ui["q"], 1 / math.sqrt(w.head_dim), ui["bonus"])
     assert_scores_close(p.scores[0].cpu().numpy(), ref)
     # the context is still usable: the same call without the stall succeeds
-    monkeypatch.delenv("KVC_TEST_STALL_UNIT")
     p.score_status.zero_()
     p.score(x["k_cache"], x["q_window"], x.get("bonus"))
     torch.cuda.synchronize()
@@ -70,6 +72,45 @@ def test_kept_index_out_of_range_marks_its_unit(kvc):
     torch.cuda.synchronize()
     st = p.compact_status.cpu().numpy()
     assert st[0] == o.UNIT_BAD_INDEX and st[1] == o.UNIT_OK
+
+
+def test_kept_count_beyond_capacity_is_clamped_and_marked(kvc):
+    """A kept count past the capacity (or negative) in caller memory: compaction
+    marks the unit, writes no row past its capacity, and the decode and engine
+    kernels read no row past the pools."""
+    w = wl.tiny().replace(n_layers=2)                   # 4 units
+    p, x = _pass(w)
+    p.run(x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"], x["rope_sin"],
+          x.get("bonus"))
+    torch.cuda.synchronize()
+    cap = p.policy.capacity
+    good_k = p.pools.k_bf16.clone()
+    ref_out = p.decode(x["q_decode"]).clone()
+    kc = p.kept_count.clone()
+    p.kept_count[kvc.POOL_BF16, 1] = cap + 1
+    p.kept_count[kvc.POOL_BF16, 2] = -3
+    p.compact_status.zero_()
+    p.pools.k_bf16.fill_(0)
+    p.compact(x["k_cache"], x["v_cache"], x["pos_in"], x["rope_cos"], x["rope_sin"])
+    torch.cuda.synchronize()
+    st = p.compact_status.cpu().numpy()
+    assert st[1] == o.UNIT_BAD_INDEX and st[2] == o.UNIT_BAD_INDEX
+    assert st[0] == o.UNIT_OK and st[3] == o.UNIT_OK
+    # units 0 and 3 are compacted as before; unit 2 writes nothing; unit 1
+    # writes at most its capacity (its own slots only)
+    for u in (0, 3):
+        assert torch.equal(p.pools.k_bf16[u].view(torch.int16), good_k[u].view(torch.int16))
+    assert int(p.pools.k_bf16[2].view(torch.int16).abs().sum()) == 0
+    # decode over the clamped counts: units with valid counts are unchanged
+    p.pools.k_bf16.copy_(good_k)
+    out = p.decode(x["q_decode"]).clone()
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    G = w.group
+    for u in (0, 3):
+        assert torch.equal(out[u * G:(u + 1) * G], ref_out[u * G:(u + 1) * G])
+    assert int(out[2 * G:3 * G].float().abs().sum()) == 0     # no rows: zeros
+    p.kept_count.copy_(kc)
 
 
 def test_rope_table_shorter_than_the_positions_marks_the_units(kvc):
