@@ -57,16 +57,51 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def algorithmic_bytes(w, kept_per_unit: int) -> dict:
-    """Bytes the method must move once per pass (counted per stage)."""
-    U, T, d, R = w.n_units, w.n_tokens, w.head_dim, w.rows_per_unit
-    score = U * T * 2 * d + U * R * 2 * d + U * T * 4 + (w.batch * T * 4 if w.bonus_spans else 0)
-    select = U * T * 4 + 3 * U * kept_per_unit * 4
-    row_io = 2 * 2 * d                                  # K and V row, bf16
-    compact = U * kept_per_unit * (row_io + row_io + 4 + 4 + 4 + 4)
+POOL_INT4, POOL_INT8, POOL_BF16 = 0, 1, 2
+
+
+def kv_row_bytes(w, pool: int) -> int:
+    """Stored bytes of one kept row's key and value in a pool (codes + scales)."""
+    d = w.head_dim
+    if pool == POOL_BF16:
+        return 2 * 2 * d
+    scales = 2 * (d // 32) if w.quant_mode == wl.QUANT_G32_BF16 else 2
+    return 2 * ((d if pool == POOL_INT8 else d // 2) + scales)
+
+
+def algorithmic_bytes(w, kept_rows=None) -> dict:
+    """Bytes the method must move once per pass, per stage.
+
+    kept_rows: {pool: kept rows summed over all units} (the run's kept
+    counts); default: the token budget of every unit, in the bf16 pool.
+      score   keys once, window queries, scores written (and page scores),
+              the per-sequence bonus
+      select  scores (or page scores) read, tags / flags read, kept indices
+              written
+      compact per kept row: its index and old position read, its bf16 key and
+              value read, its pool bytes and its new / original position
+              written; the rotary table rows touched (renumbering)
+    """
+    U, T, d, R, B = w.n_units, w.n_tokens, w.head_dim, w.rows_per_unit, w.batch
+    P = w.page_size
+    if kept_rows is None:
+        kept_rows = {POOL_BF16: U * w.budget_tokens}
+    n_kept = sum(kept_rows.values())
+    n_items = T // P
+    score = U * T * 2 * d + U * R * 2 * d + U * T * 4 + (U * n_items * 4 if P > 1 else 0) + \
+        (B * T * 4 if w.bonus_spans else 0)
+    select = U * n_items * 4 + (B * T if w.tag_probs is not None else 0) + \
+        (B * n_items if (w.protect_pages or w.retire_pages) else 0) + n_kept * 4
+    compact = n_kept * (4 + 4 + 2 * 2 * d + 4 + 4) + sum(n * kv_row_bytes(w, p) for p, n in kept_rows.items())
     if w.renumber:
         compact += min(w.max_pos, T) * d * 4            # cos + sin rows touched (fp32, d/2 each)
     return dict(score=score, select=select, compact=compact, total=score + select + compact)
+
+
+def kept_rows_of(kept_count) -> dict:
+    """{pool: rows summed over units} from a [3][U] kept-count tensor."""
+    c = kept_count.sum(dim=1).tolist()
+    return {POOL_INT4: int(c[0]), POOL_INT8: int(c[1]), POOL_BF16: int(c[2])}
 
 
 def _code(src: str) -> str:
@@ -280,6 +315,128 @@ def commitkv_stage(dev, stream, flush, repeats: int = 10) -> dict:
     kv_bytes = 2 * we.n_units * we.n_tokens * 128 * 2
     out["commitkv_effect_gbs"] = kv_bytes / (out["commitkv_effect"] * 1e-3) / 1e9
     out["commitkv_retired_pages"] = int(rt_.sum().item())
+    return out
+
+
+# ---------------------------------------------------------------------------- the other workloads
+
+def _timed(fn, stream, flush, repeats):
+    """Mean ms of `repeats` calls of fn (CUDA events on `stream`, L2 flushed before each)."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    t = []
+    for _ in range(repeats):
+        flush.fill_(1)
+        a, b = ev(), ev()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b))
+    return statistics.mean(t)
+
+
+def _roofline(w, ab_total, flops, t_ms, hbm, tc):
+    t_roof = max(ab_total / (hbm * 1e9), flops / (tc * 1e12)) * 1e3
+    return {"t_roof_ms": t_roof, "frac": t_roof / t_ms,
+            "bound": "hbm" if ab_total / hbm >= flops / (tc * 1e3) else "tensor",
+            "algorithmic_bytes": ab_total, "algorithmic_flops": flops,
+            "gbs": ab_total / (t_ms * 1e-3) / 1e9}
+
+
+def time_workload(w, dev, stream, flush, steps, warmup, hbm, tc) -> dict:
+    """One compaction pass of workload w (score -> select -> compact) on
+    device-resident inputs: mean of `steps` passes after `warmup`, L2 flushed
+    before each; per-stage times, rows/s, GB/s on the algorithmic bytes and
+    the fraction of the pass roofline.  A paged workload also times one
+    decode step over its compacted cache."""
+    from budgeted_kv_cache_gb300.passes import pass_for_workload
+    x = wl.make_inputs(w, device=dev)
+    p = pass_for_workload(w, inputs=x, device=dev)
+    args = (x["k_cache"], x["v_cache"], x["q_window"], x["pos_in"], x["rope_cos"], x["rope_sin"], x.get("bonus"))
+    for _ in range(warmup):
+        p.run(*args, stream=stream)
+    torch.cuda.synchronize()
+    assert int(p.score_status.abs().sum()) == 0 and int(p.compact_status.abs().sum()) == 0
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    st = {"score": [], "select": [], "compact": []}
+    for _ in range(steps):
+        flush.fill_(1)
+        m = [ev() for _ in range(4)]
+        m[0].record(stream)
+        p.score(x["k_cache"], x["q_window"], x.get("bonus"), stream=stream)
+        m[1].record(stream)
+        p.select(stream=stream)
+        m[2].record(stream)
+        p.compact(x["k_cache"], x["v_cache"], x["pos_in"], x["rope_cos"], x["rope_sin"], stream=stream)
+        m[3].record(stream)
+        torch.cuda.synchronize()
+        for i, k in enumerate(st):
+            st[k].append(m[i].elapsed_time(m[i + 1]))
+    stages = {k: statistics.mean(v) for k, v in st.items()}
+    t = sum(stages.values())
+    kept = kept_rows_of(p.kept_count)
+    ab = algorithmic_bytes(w, kept)
+    out = {"workload": w.name, "units": w.n_units, "n_tokens": w.n_tokens, "ms_per_step": t,
+           "value": w.n_units * w.n_tokens / (t * 1e-3), "unit": UNIT, "stages_ms": stages,
+           "kept_rows": kept, "roofline": _roofline(w, ab["total"], algorithmic_flops(w), t, hbm, tc),
+           "steps": steps, "warmup": warmup}
+    if w.page_size > 1:
+        out["decode_ms"] = _timed(lambda: p.decode(x["q_decode"], stream=stream), stream, flush, steps)
+    del x, p
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_session(w, dev, stream, hbm, tc, warmup=3) -> dict:
+    """The million-token session in cycles: each cycle appends a chunk
+    (the engine's KV write, timed apart) and compacts the cache back to the
+    budget; sustained rows/s = rows appended over the summed pass time."""
+    from budgeted_kv_cache_gb300.session import BoundedSession
+    s0 = wl.session_start(w, dev)
+    sess = BoundedSession(w.batch, w.n_layers, w.n_q_heads, w.n_kv_heads, w.head_dim, w.budget_tokens,
+                          w.chunk, w.window, w.limit, w.n_sink, w.n_recent, device=dev)
+    sess.start(s0["k0"], s0["v0"])
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    marks = []
+    for c in range(-warmup, w.cycles):
+        ch = wl.session_chunk(w, c, dev)              # drawn outside the timed events
+        m = [ev() for _ in range(3)]
+        m[0].record(stream)
+        sess.append(ch["k"], ch["v"], stream=stream)
+        m[1].record(stream)
+        sess.compact(ch["q_window"], s0["rope_cos"], s0["rope_sin"], stream=stream)
+        m[2].record(stream)
+        if c >= 0:
+            marks.append(m)
+    torch.cuda.synchronize()
+    p = sess.last_pass
+    assert int(p.unit_status.abs().sum()) == 0 and int(p.compact_status.abs().sum()) == 0
+    t_app = sum(m[0].elapsed_time(m[1]) for m in marks)
+    t_pass = sum(m[1].elapsed_time(m[2]) for m in marks)
+    rows = w.n_units * w.chunk * w.cycles
+    ab = algorithmic_bytes(w)                          # one cycle: a pass over budget + chunk rows
+    flops = algorithmic_flops(w)
+    roof = _roofline(w, ab["total"] * w.cycles, flops * w.cycles, t_pass, hbm, tc)
+    out = {"workload": w.name, "units": w.n_units, "cycles": w.cycles, "chunk": w.chunk,
+           "cache_rows": w.n_tokens, "budget": w.budget_tokens, "limit": w.limit,
+           "value": rows / (t_pass * 1e-3), "unit": "appended rows/s (summed over layer x KV-head units)",
+           "ms_per_cycle": t_pass / w.cycles, "append_ms_per_cycle": t_app / w.cycles,
+           "value_with_append": rows / ((t_pass + t_app) * 1e-3),
+           "renumbered_cycles": int(sum(sess.renumbered[warmup:])), "roofline": roof,
+           "l2": "not flushed between cycles: each cycle's chunk is written just before its compaction"}
+    del sess, s0
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_configs(dev, stream, flush, hbm, tc, steps) -> dict:
+    """Every other workload of the pages, one pass each (C2 is the headline)."""
+    out = {}
+    for key, mk in (("C1", wl.tiny), ("C3", wl.pask_batch16), ("C4", wl.commitkv_pages_128k),
+                    ("C5A", wl.million_token_8l)):
+        out[key] = time_workload(mk(), dev, stream, flush, steps=steps, warmup=3, hbm=hbm, tc=tc)
+    out["C1"]["us_per_step"] = 1e3 * out["C1"]["ms_per_step"]
+    out["C5B"] = time_session(wl.million_token_sustained(), dev, stream, hbm, tc)
     return out
 
 
@@ -551,7 +708,7 @@ def run_gpu(args, w, world, rank, local):
 
         host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs_of(q)]
                     for q in gpasses]
-        kept_rows = wr.n_units * wr.budget_tokens
+        kept_rows = sum(kept_rows_of(p.kept_count).values())
         h2d = sum(host[n].numel() * host[n].element_size() for n in copied) + \
             kept_rows * (wr.head_dim * 2 + 4)               # kept value rows and positions, read in place
         d2h = sum(t.numel() * t.element_size() for ts in host_out for t in ts)
@@ -608,11 +765,13 @@ def run_gpu(args, w, world, rank, local):
                "matches_device_resident_pass": same}
         del host, dev_in, host_out, gpasses
 
+    hbm, tc, src = _peaks()
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = run_configs(dev, stream, flush, hbm, tc, steps=max(3, min(args.steps, 5)))
     if rank != 0:
         return
-    hbm, tc, src = _peaks()
-    kept = wr.budget_tokens
-    ab = algorithmic_bytes(wr, kept)
+    ab = algorithmic_bytes(wr, kept_rows_of(p.kept_count))
     flops = algorithmic_flops(wr)
     ms_step = total_ms / args.steps
     score_ms = statistics.mean(t_score)
@@ -652,6 +811,7 @@ def run_gpu(args, w, world, rank, local):
                                       / (30.0 * torch.cuda.get_device_properties(dev).multi_processor_count
                                          * ((clocks or {}).get("sm_mhz") or 2070.0) * 1e6)},
         "graph_ms_per_step": graph_ms,
+        "configs": configs,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": 3 * args.steps, "clocks": clocks,
     }
@@ -668,6 +828,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the passes over the pages' other workloads (C1, C3, C4, C5 A and B)")
     ap.add_argument("--e2e-groups", type=int, default=9,
                     help="layer groups of the end-to-end leg (copies of one overlap the pass of another)")
     ap.add_argument("--no-commitkv", action="store_true",

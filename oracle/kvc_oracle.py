@@ -805,6 +805,32 @@ def run_unit(k_bits, v_bits, q_bits, pos_in, params: PassParams, cos_tab, sin_ta
     return res
 
 
+def session_cycle(res_k, res_v, res_pos, new_k, new_v, q_bits, params: PassParams, limit: int,
+                  cos_tab, sin_tab, scores=None):
+    """One cycle of a bounded-position session of one unit (PACE Sec. 3.2,
+    "Bounded positions" and "Choosing L"; Sec. 5.7 runs such sessions).
+
+    The chunk's H rows are appended after the resident rows at the next
+    physical positions (one past the resident rows' largest position).  The
+    cache is scored by the window queries (its last W rows), selected and
+    compacted back to the budget.  The compaction renumbers iff the position
+    one past the cache's last row is within H of the limit L, i.e. the next
+    chunk would otherwise reach L.  `scores` may be given (stage-wise
+    parity).  Returns (k_bits, v_bits, pos) of the new resident rows (the
+    bf16 pool) and the cycle's UnitResult.
+    """
+    res_pos = np.asarray(res_pos, np.int64)
+    H = np.asarray(new_k).shape[0]
+    start = int(res_pos.max()) + 1 if res_pos.size else 0
+    pos_in = np.concatenate([res_pos, np.arange(start, start + H, dtype=np.int64)])
+    k = np.concatenate([np.asarray(res_k, np.uint16), np.asarray(new_k, np.uint16)])
+    v = np.concatenate([np.asarray(res_v, np.uint16), np.asarray(new_v, np.uint16)])
+    prm = PassParams(**{**params.__dict__, "renumber": renumber_due(start + H, limit, H)})
+    r = run_unit(k, v, q_bits, pos_in, prm, cos_tab, sin_tab, scores=scores)
+    pool = r.pools[ACT_BF16]
+    return pool.k, pool.v, pool.pos, r
+
+
 def cache_bytes(n_tokens: int, n_layers: int, n_kv_heads: int, head_dim: int,
                 action: int = ACT_BF16, quant_mode: int = QUANT_G32_BF16) -> int:
     """Bytes of K and V payload for n_tokens tokens across all layers and KV heads."""

@@ -49,11 +49,34 @@ def test_algorithmic_work_of_the_qwen3_8b_workload():
     assert (w.n_units, w.n_tokens, w.head_dim, w.rows_per_unit) == (288, 32768, 128, 256)
     flops = bench.algorithmic_flops(w)
     assert flops == 618_475_290_624                       # 2 x 288 units x 256 rows x 32768 keys x 128
-    ab = bench.algorithmic_bytes(w, w.budget_tokens)
+    ab = bench.algorithmic_bytes(w)
     keys = 288 * 32768 * 128 * 2                          # K read once: 2.416 GB
     assert ab["score"] == keys + 288 * 256 * 128 * 2 + 288 * 32768 * 4 + 32768 * 4
     assert ab["total"] == pytest.approx(3.14e9, rel=0.01)
     assert ab["score"] / ab["total"] == pytest.approx(0.786, abs=0.005)   # K dominates the pass
+
+
+def test_algorithmic_bytes_of_a_byte_mode_pass():
+    """PASK batch 16 (byte budget): every pool's rows are costed at their own
+    width -- int4 / int8 codes plus one bf16 scale per 32 elements (PASK
+    App. B.5), bf16 rows in full -- and no rotary rows are touched (no
+    renumbering); tags are read by the selection."""
+    bench = _bench()
+    w = bench.wl.pask_batch16()
+    U, T, d = 4096, 8192, 128
+    assert (w.n_units, w.n_tokens, w.head_dim) == (U, T, d)
+    kept = {bench.POOL_INT4: 3000 * U, bench.POOL_INT8: 2000 * U, bench.POOL_BF16: 1000 * U}
+    ab = bench.algorithmic_bytes(w, kept)
+    n = 6000 * U
+    # per row K + V: int4 2 x (64 + 8) = 144, int8 2 x (128 + 8) = 272, bf16 512
+    pools = U * (3000 * 144 + 2000 * 272 + 1000 * 512)
+    assert ab["compact"] == n * (4 + 4 + 512 + 8) + pools
+    assert ab["select"] == U * T * 4 + 16 * T + n * 4
+    assert ab["score"] == U * T * 256 + U * 256 * 256 + U * T * 4
+    # row mode (one fp16 scale per row): int4 2 x (64 + 2) = 132
+    wr = w.replace(quant_mode=bench.wl.QUANT_ROW_FP16)
+    assert bench.kv_row_bytes(wr, bench.POOL_INT4) == 132
+    assert bench.kv_row_bytes(wr, bench.POOL_INT8) == 2 * (128 + 2)
 
 
 def test_traffic_key_ignores_comments():

@@ -65,6 +65,9 @@ class Workload:
     retire_pages: int = 0           # page mode: retired (excluded) pages
     first_pos: int = 0              # physical position of token 0
     decode_pos: int = 0             # physical position of the decode query
+    chunk: int = 0                  # session: rows appended per cycle (n_tokens = budget + chunk)
+    cycles: int = 0                 # session: compaction cycles
+    limit: int = 0                  # session: position limit L
 
     @property
     def group(self) -> int:
@@ -86,7 +89,7 @@ class Workload:
     def max_pos(self) -> int:
         """Rows of the rotary table: every old and new position must index it."""
         return max(self.first_pos + self.n_tokens, self.decode_pos + 1,
-                   self.budget_tokens + 1)
+                   self.budget_tokens + 1, self.limit)
 
     def capacity(self) -> int:
         """Rows per pool per unit that always suffice for this policy."""
@@ -160,6 +163,15 @@ def million_token_8l() -> Workload:
                     n_kv_heads=8, head_dim=128, n_tokens=1 << 20, window=64, rope_theta=1e6,
                     seed=BASE_SEED + 4, budget_tokens=2048, n_sink=4, n_recent=128,
                     renumber=True, decode_pos=2048)
+
+
+def million_token_sustained() -> Workload:
+    """The million-token session in cycles (PACE Sec. 3.2 "Choosing L", Sec. 5.7):
+    2,048 resident rows; each cycle appends a chunk of 4,096 rows and compacts
+    the 6,144-row cache back to 2,048 rows, renumbering below L = 8,192;
+    256 cycles append 1,048,576 rows."""
+    return million_token_8l().replace(name="qwen3_8b_8L_sustained_4096x256", n_tokens=2048 + 4096,
+                                      chunk=4096, cycles=256, limit=8192)
 
 
 ALL = {w().name: w for w in (tiny, qwen3_8b_32k, pask_batch16, commitkv_pages_128k,
@@ -267,6 +279,31 @@ def make_inputs(w: Workload, device="cpu", with_tables: bool = True) -> dict:
         cos, sin = rope_tables(w.max_pos, d, w.rope_theta, dev)
         out["rope_cos"], out["rope_sin"] = cos, sin
     return out
+
+
+def session_start(w: Workload, device="cpu") -> dict:
+    """Resident rows before a session's first cycle: keys and values
+    [B][L][H_kv][budget][d] bf16 at positions 0..budget-1, and the rotary
+    tables (positions below the limit L)."""
+    dev = torch.device(device)
+    g = _gen(w.seed, dev)
+    B, L, Hkv, d = w.batch, w.n_layers, w.n_kv_heads, w.head_dim
+    k0 = _randn_bf16((B, L, Hkv, w.budget_tokens, d), g, dev)
+    v0 = _randn_bf16((B, L, Hkv, w.budget_tokens, d), g, dev)
+    cos, sin = rope_tables(w.max_pos, d, w.rope_theta, dev)
+    return dict(k0=k0, v0=v0, rope_cos=cos, rope_sin=sin)
+
+
+def session_chunk(w: Workload, c: int, device="cpu") -> dict:
+    """Chunk c of a session (its own seed): keys and values
+    [B][L][H_kv][chunk][d] bf16, treated as rotated at the positions the session
+    assigns them, and the window queries [B][L][H_q][W][d] of its last W rows."""
+    dev = torch.device(device)
+    g = _gen(w.seed * 4099 + 17 * c + 1, dev)
+    B, L, Hq, Hkv, d, W = w.batch, w.n_layers, w.n_q_heads, w.n_kv_heads, w.head_dim, w.window
+    return dict(k=_randn_bf16((B, L, Hkv, w.chunk, d), g, dev),
+                v=_randn_bf16((B, L, Hkv, w.chunk, d), g, dev),
+                q_window=_randn_bf16((B, L, Hq, W, d), g, dev))
 
 
 def unit_index(w: Workload, b: int, l: int, g: int) -> int:
