@@ -90,6 +90,12 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n
   return s;
 }
 
+// First tile of slice c of a unit: the n_tiles tiles are split into S
+// slices whose sizes differ by at most one.
+__device__ __forceinline__ int slice_begin(const ScoreArgs& a, int c) {
+  return static_cast<int>((static_cast<int64_t>(c) * a.n_tiles) / a.items_per_unit);
+}
+
 // Wait that ignores the abort flag (used to drain work already in flight).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -269,8 +275,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       int q_loads = 0;
       for (int it = blockIdx.x; it < a.n_items; it += gridDim.x, ++li) {
         const int u = it / S, c = it % S;
-        const int t0 = c * a.chunk_tiles;
-        const int nt = min(a.chunk_tiles, a.n_tiles - t0);
+        const int t0 = slice_begin(a, c);
+        const int nt = slice_begin(a, c + 1) - t0;
         if (li > 0 && !mbar_wait_backoff(smem_u32(s.qempty), (li - 1) & 1, abort_flag, kProducerSleepNs))
           break;
         mbar_arrive_expect_tx(smem_u32(s.qfull), static_cast<uint32_t>(n_kc * a.R * 128));
@@ -290,7 +296,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             mbar_arrive_expect_tx(smem_u32(&s.full[st]), stage_bytes);
             for (int kc = 0; kc < n_kc; ++kc)
               tma_load_3d(smem_u32(s.k + st * stage_bytes + kc * kChunkBytes), &tmap_k,
-                          smem_u32(&s.full[st]), kc * 64, (t0 + t) * kTileTokens, u,
+                          smem_u32(&s.full[st]), kc * 64,
+                          (t0 + (pass == 0 ? t : nt - 1 - t)) * kTileTokens, u,
                           pass == 0 ? keep : stream);
           }
         }
@@ -320,8 +327,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       int li = 0;
       for (int it = blockIdx.x; it < a.n_items; it += gridDim.x, ++li) {
         const int c = it % S;
-        const int t0 = c * a.chunk_tiles;
-        const int nt = min(a.chunk_tiles, a.n_tiles - t0);
+        const int nt = slice_begin(a, c + 1) - slice_begin(a, c);
         if (!mbar_wait_backoff(smem_u32(s.qfull), li & 1, abort_flag, kMmaSleepNs)) break;
         tc_fence_after();
         bool ok = true;
@@ -404,8 +410,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     int cur_u = -1, cur_it = -1;
     for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
       const int u = it / S, c = it % S;
-      const int t0 = c * a.chunk_tiles;
-      const int nt = min(a.chunk_tiles, a.n_tiles - t0);
+      const int t0 = slice_begin(a, c);
+      const int nt = slice_begin(a, c + 1) - t0;
       const int b = u / (a.L * a.Hkv);
       cur_u = u;
       cur_it = it;
@@ -574,7 +580,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       for (int t = 0; t < nt; ++t, ++jt, ++jt2) {
         const uint32_t tb = jt & 1, tph = (jt >> 1) & 1;
         const int fg = static_cast<int>(jt2 & 3);
-        const int64_t tile0 = static_cast<int64_t>(t0 + t) * kTileTokens;
+        // pass 2 walks the item's tiles last to first: the tiles pass 1 read
+        // most recently are the likeliest to still be in L2
+        const int64_t tile0 = static_cast<int64_t>(t0 + nt - 1 - t) * kTileTokens;
         const int64_t j = tile0 + lrow;
         const bool masked = (tile0 + kTileTokens - 1) > Tq;
         float bon = 0.f, old = 0.f;
