@@ -16,6 +16,8 @@
 // comes over one shuffle; the two partners split the cos/sin work.  All float operations use explicit round-to-
 // nearest intrinsics (no contraction into FMA), so the stored bits are a
 // fixed function of the inputs.
+#include <algorithm>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -283,22 +285,32 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
   }
 }
 
-// Each lane group moves kRows rows.  The loads of every stage (kept index;
-// row and position; rotation tables) are issued for all of them through
-// the read-only path before any is consumed, and the one status word a bad
-// index sets is written after the last load, so the loads of the rows are
-// not ordered behind a store.
+// A block works on one (unit, pool, K-or-V) stream, in batches of up to
+// kBatch kept rows.  For a batch it first stages every row's kept index, old
+// position, new position and status in shared memory (one thread per row,
+// all loads of the batch in flight together), so the dependent chain kept
+// index -> position -> rotary rows is walked once per batch instead of once
+// per row.  Then each lane group moves kRows rows at a time: the row loads
+// and the rotary-table loads of all of them are issued before any is used.
+// The grid has up to kBatch-row batches of every stream side by side; a
+// block takes the batches blockIdx.x, blockIdx.x + gridDim.x, ... that lie
+// below the stream's kept count.
 constexpr int kRows = 2;
+constexpr int kBatch = 512;
+constexpr uint8_t kValid = 1, kRotate = 2, kChange = 4;
 
 template <bool kStore, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs a) {
+  __shared__ int32_t s_t[kBatch], s_p[kBatch], s_p2[kBatch], s_pr[kStore ? kBatch : 1];
+  __shared__ uint8_t s_f[kBatch];
+  __shared__ int s_bad;
   const int d = a.d;
   const int lpr = d / 8;                        // lanes per row (16 B = 8 bf16 per lane)
   const int rows_per_warp = 32 / lpr;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / lpr;
   const int hl = lane % lpr;
-  const int is_v = blockIdx.z & 1;              // K rows and V rows go to separate warps
+  const int is_v = blockIdx.z & 1;              // K rows and V rows go to separate blocks
   const int pool = a.pool_lo + (blockIdx.z >> 1);
   const int u = blockIdx.y;
   const int U = a.U;
@@ -309,175 +321,195 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   const int cnt = clamp_count(cnt_raw, cap);
   if (cnt != cnt_raw && blockIdx.x == 0 && threadIdx.x == 0 && a.unit_status)
     a.unit_status[u] = KVC_UNIT_BAD_INDEX;
-  const int64_t i_base =
-      (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kRows * rows_per_warp + sub;
-  if (__all_sync(kFull, i_base >= cnt)) return;
+  if (static_cast<int64_t>(blockIdx.x) * kBatch >= cnt) return;    // block-uniform
+  if (threadIdx.x == 0) s_bad = 0;
 
   const int64_t slot0 = (static_cast<int64_t>(pool) * U + u) * cap;
-  bool valid[kRows];
-  int32_t t[kRows];
-#pragma unroll
-  for (int n = 0; n < kRows; ++n) {
-    const int64_t i = i_base + n * rows_per_warp;
-    valid[n] = i < cnt;
-    t[n] = valid[n] ? __ldg(a.kept_idx + slot0 + i) : 0;
-  }
-  bool bad = false;
-  uint4 w[kRows];
-  int32_t p[kRows];
-  const __nv_bfloat16* src = is_v ? a.v : a.k;
-#pragma unroll
-  for (int n = 0; n < kRows; ++n) {
-    if (valid[n] && (t[n] < 0 || t[n] >= a.T)) {
-      valid[n] = false;
-      bad = true;
-    }
-    w[n] = valid[n] ? __ldg(reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(u) * a.T + t[n]) * d) + hl)
-                    : make_uint4(0, 0, 0, 0);
-    p[n] = (valid[n] && !is_v) ? __ldg(a.pos_in + static_cast<int64_t>(u) * a.T + t[n]) : 0;
-  }
-  // reference store (keys only): p_ref and the reference bits of each row
   const bool use_store = kStore && !is_v;                       // block-uniform
-  int32_t pr[kRows];
-  uint4 wr[kRows];
-#pragma unroll
-  for (int n = 0; n < kRows; ++n) {
-    pr[n] = -1;
-    wr[n] = make_uint4(0, 0, 0, 0);
-    if (use_store && valid[n]) {
-      pr[n] = __ldg(a.ref.ref_pos + static_cast<int64_t>(u) * a.T + t[n]);
-      if (pr[n] >= a.rope_max_pos) {
-        valid[n] = false;
-        bad = true;
-      } else if (pr[n] >= 0) {
-        wr[n] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.ref.ref_k) +
-                                                     (static_cast<int64_t>(u) * a.T + t[n]) * d) + hl);
-      }
-    }
-  }
-  int32_t p2[kRows];
-  bool rotate[kRows];
-#pragma unroll
-  for (int n = 0; n < kRows; ++n) {
-    p2[n] = p[n];
-    rotate[n] = false;
-    if (valid[n] && !is_v) {
-      if (a.renumber) {
-        // rank among the kept rows of every pool (pools are disjoint, ascending)
-        int rank = static_cast<int>(i_base + n * rows_per_warp);
-        for (int q = 0; q < KVC_N_POOLS; ++q) {
-          if (q == pool) continue;
-          const int cq = clamp_count(__ldg(a.kept_count + q * U + u), cap);
-          if (cq > 0)
-            rank += lower_bound_i32(a.kept_idx + (static_cast<int64_t>(q) * U + u) * cap, cq, t[n]);
-        }
-        p2[n] = rank;
-      }
-      rotate[n] = p2[n] != p[n];
-      if (rotate[n] && (p[n] < 0 || p[n] >= a.rope_max_pos || p2[n] < 0 || p2[n] >= a.rope_max_pos)) {
-        valid[n] = false;
-        rotate[n] = false;
-        bad = true;
-      }
-    }
-  }
-  // with the store, rows rotate in their own branch below (no hoisted tables)
-  bool chg[kRows];
-#pragma unroll
-  for (int n = 0; n < kRows; ++n) {
-    chg[n] = use_store && rotate[n];
-    if (use_store) rotate[n] = false;
-  }
-  // rotation tables: cos / sin of the old and new position for the four
-  // (C, S) pairs this lane forms
+  const __nv_bfloat16* src = is_v ? a.v : a.k;
   const LaneRot lr = kGeneral ? lane_rot(a.rope_layout, a.rotary_dim, lane, hl, lpr)
                               : lane_rot(KVC_ROPE_SPLIT_HALF, d, lane, hl, lpr);
   const int j0 = lr.j0;
   const int half = lr.half;
-  float4 tab[kRows][4];
+
+  for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * kBatch; b0 < cnt;
+       b0 += static_cast<int64_t>(gridDim.x) * kBatch) {
+    const int nb = static_cast<int>(min(static_cast<int64_t>(kBatch), cnt - b0));
+    // ---------------- stage the batch's rows (one thread per row)
+    __syncthreads();                            // the previous batch is done with the arrays
+    bool bad = false;
+    for (int q = threadIdx.x; q < nb; q += kThreads) {
+      const int64_t i = b0 + q;
+      const int32_t t = __ldg(a.kept_idx + slot0 + i);
+      uint8_t f = 0;
+      int32_t p = 0, p2 = 0, pr = -1;
+      if (t < 0 || t >= a.T) {
+        bad = true;
+      } else {
+        f = kValid;
+        if (!is_v) {
+          p = __ldg(a.pos_in + static_cast<int64_t>(u) * a.T + t);
+          p2 = p;
+          if (a.renumber) {
+            // rank among the kept rows of every pool (pools are disjoint, ascending)
+            int rank = static_cast<int>(i);
+            for (int qq = 0; qq < KVC_N_POOLS; ++qq) {
+              if (qq == pool) continue;
+              const int cq = clamp_count(__ldg(a.kept_count + qq * U + u), cap);
+              if (cq > 0)
+                rank += lower_bound_i32(a.kept_idx + (static_cast<int64_t>(qq) * U + u) * cap, cq, t);
+            }
+            p2 = rank;
+          }
+          if (p2 != p) {
+            if (p < 0 || p >= a.rope_max_pos || p2 < 0 || p2 >= a.rope_max_pos) {
+              f = 0;
+              bad = true;
+            } else {
+              f |= kRotate;
+            }
+          }
+          if (use_store && (f & kValid)) {
+            pr = __ldg(a.ref.ref_pos + static_cast<int64_t>(u) * a.T + t);
+            if (pr >= a.rope_max_pos) {
+              f = 0;
+              bad = true;
+            }
+          }
+        }
+      }
+      s_t[q] = t;
+      s_p[q] = p;
+      s_p2[q] = p2;
+      if (kStore) s_pr[q] = pr;
+      s_f[q] = f;
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+
+    // ---------------- move the rows: lane group `sub` of each warp takes rows
+    // q = q0 + n * rows_per_warp + sub, n < kRows
+    const int step = (kThreads / 32) * rows_per_warp * kRows;
+    for (int q0 = warp * rows_per_warp * kRows; q0 < nb; q0 += step) {
+      bool valid[kRows], rotate[kRows], chg[kRows];
+      int32_t t[kRows], p[kRows], p2[kRows], pr[kRows];
+      uint4 w[kRows], wr[kRows];
 #pragma unroll
-  for (int n = 0; n < kRows; ++n) {
-    if (rotate[n] && lr.active) {
-      tab[n][0] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p[n]) * half + j0));
-      tab[n][1] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p[n]) * half + j0));
-      tab[n][2] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p2[n]) * half + j0));
-      tab[n][3] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p2[n]) * half + j0));
-    } else {
+      for (int n = 0; n < kRows; ++n) {
+        const int q = q0 + n * rows_per_warp + sub;
+        const uint8_t f = q < nb ? s_f[q] : 0;
+        valid[n] = f & kValid;
+        t[n] = valid[n] ? s_t[q] : 0;
+        p[n] = valid[n] ? s_p[q] : 0;
+        p2[n] = valid[n] ? s_p2[q] : 0;
+        pr[n] = (kStore && valid[n]) ? s_pr[q] : -1;
+        rotate[n] = (f & kRotate) != 0;
+        w[n] = valid[n] ? __ldg(reinterpret_cast<const uint4*>(src + (static_cast<int64_t>(u) * a.T + t[n]) * d) + hl)
+                        : make_uint4(0, 0, 0, 0);
+        wr[n] = make_uint4(0, 0, 0, 0);
+        if (use_store && valid[n] && pr[n] >= 0)
+          wr[n] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.ref.ref_k) +
+                                                       (static_cast<int64_t>(u) * a.T + t[n]) * d) + hl);
+      }
+      // with the store, rows rotate in their own branch below (no hoisted tables)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tab[n][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int n = 0; n < kRows; ++n) {
+        chg[n] = use_store && rotate[n];
+        if (use_store) rotate[n] = false;
+      }
+      // rotation tables: cos / sin of the old and new position for the four
+      // (C, S) pairs this lane forms
+      float4 tab[kRows][4];
+#pragma unroll
+      for (int n = 0; n < kRows; ++n) {
+        if (rotate[n] && lr.active) {
+          tab[n][0] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p[n]) * half + j0));
+          tab[n][1] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p[n]) * half + j0));
+          tab[n][2] = __ldg(reinterpret_cast<const float4*>(a.cos + static_cast<int64_t>(p2[n]) * half + j0));
+          tab[n][3] = __ldg(reinterpret_cast<const float4*>(a.sin + static_cast<int64_t>(p2[n]) * half + j0));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tab[n][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < kRows; ++n) {
+        float x[8];
+        unpack8(w[n], x);
+        // the branch is warp-uniform: key rows only, and only if a row rotates
+        if (!is_v && __any_sync(kFull, rotate[n])) {
+          if (kGeneral) rerotate_lane_general(lr, rotate[n], tab[n], x, w[n]);
+          else rerotate_lane(lpr, hl, rotate[n], tab[n], x, w[n]);
+        }
+        const int64_t i = b0 + q0 + n * rows_per_warp + sub;
+        const int64_t row = static_cast<int64_t>(u) * cap + i;
+        if (use_store) {
+          // PACE reference store: check the copy (re-rotated p_ref -> p, it must
+          // reproduce the stored key in every lane of the row), then derive the
+          // new key from it, or from the stored key if there is no valid copy
+          const bool has_ref = valid[n] && pr[n] >= 0;
+          uint4 chk = wr[n];
+          float xc[8];
+          unpack8(chk, xc);
+          rotate_row<kGeneral>(a, lr, lpr, hl, chg[n] && has_ref && pr[n] != p[n], pr[n], p[n], chk, xc);
+          const bool lane_ok = chk.x == w[n].x && chk.y == w[n].y && chk.z == w[n].z && chk.w == w[n].w;
+          const unsigned gmask = (lpr == 32 ? kFull : ((1u << lpr) - 1u)) << (sub * lpr);
+          const bool ok = (__ballot_sync(kFull, lane_ok) & gmask) == gmask;
+          const bool use_ref = chg[n] && has_ref && ok;
+          const bool failed = chg[n] && has_ref && !ok;
+          uint4 nw = use_ref ? wr[n] : w[n];
+          const int32_t from = use_ref ? pr[n] : p[n];
+          float xs[8];
+          unpack8(nw, xs);
+          rotate_row<kGeneral>(a, lr, lpr, hl, chg[n] && from != p2[n], from, p2[n], nw, xs);
+          uint4 rw = has_ref ? wr[n] : make_uint4(0, 0, 0, 0);
+          int32_t rp = has_ref ? pr[n] : -1;
+          if (chg[n] && !use_ref) {            // first renumber, or a failed copy: the stored key
+            rw = w[n];
+            rp = p[n];
+          }
+          if (chg[n]) {
+            w[n] = nw;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = xs[k];
+          }
+          if (valid[n]) {
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ref.ref_k_out) + (slot0 + i) * d + hl * 8) = rw;
+            if (hl == 0) a.ref.ref_pos_out[slot0 + i] = rp;
+          }
+          if (failed && hl == 0 && a.ref.failures) atomicAdd(a.ref.failures + u, 1);
+        }
+        if (pool == KVC_POOL_BF16) {
+          if (valid[n]) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.pools.v_bf16 : a.pools.k_bf16);
+            *reinterpret_cast<uint4*>(dst + row * d + hl * 8) = w[n];
+          }
+        } else {
+          store_quantised(a, pool, is_v, lpr, hl, valid[n], row, x);
+        }
+        if (valid[n] && hl == 0 && !is_v) {
+          a.pools.pos_out[slot0 + i] = p2[n];
+          if (a.pools.orig_pos_out) a.pools.orig_pos_out[slot0 + i] = p[n];
+        }
+      }
     }
   }
-#pragma unroll
-  for (int n = 0; n < kRows; ++n) {
-    float x[8];
-    unpack8(w[n], x);
-    // the branch is warp-uniform: key warps only, and only if a row rotates
-    if (!is_v && __any_sync(kFull, rotate[n])) {
-      if (kGeneral) rerotate_lane_general(lr, rotate[n], tab[n], x, w[n]);
-      else rerotate_lane(lpr, hl, rotate[n], tab[n], x, w[n]);
-    }
-    const int64_t i = i_base + n * rows_per_warp;
-    const int64_t row = static_cast<int64_t>(u) * cap + i;
-    if (use_store) {
-      // PACE reference store: check the copy (re-rotated p_ref -> p, it must
-      // reproduce the stored key in every lane of the row), then derive the
-      // new key from it, or from the stored key if there is no valid copy
-      const bool has_ref = valid[n] && pr[n] >= 0;
-      uint4 chk = wr[n];
-      float xc[8];
-      unpack8(chk, xc);
-      rotate_row<kGeneral>(a, lr, lpr, hl, chg[n] && has_ref && pr[n] != p[n], pr[n], p[n], chk, xc);
-      const bool lane_ok = chk.x == w[n].x && chk.y == w[n].y && chk.z == w[n].z && chk.w == w[n].w;
-      const unsigned gmask = (lpr == 32 ? kFull : ((1u << lpr) - 1u)) << (sub * lpr);
-      const bool ok = (__ballot_sync(kFull, lane_ok) & gmask) == gmask;
-      const bool use_ref = chg[n] && has_ref && ok;
-      const bool failed = chg[n] && has_ref && !ok;
-      uint4 nw = use_ref ? wr[n] : w[n];
-      const int32_t from = use_ref ? pr[n] : p[n];
-      float xs[8];
-      unpack8(nw, xs);
-      rotate_row<kGeneral>(a, lr, lpr, hl, chg[n] && from != p2[n], from, p2[n], nw, xs);
-      uint4 rw = has_ref ? wr[n] : make_uint4(0, 0, 0, 0);
-      int32_t rp = has_ref ? pr[n] : -1;
-      if (chg[n] && !use_ref) {            // first renumber, or a failed copy: the stored key
-        rw = w[n];
-        rp = p[n];
-      }
-      if (chg[n]) {
-        w[n] = nw;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = xs[k];
-      }
-      if (valid[n]) {
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ref.ref_k_out) + (slot0 + i) * d + hl * 8) = rw;
-        if (hl == 0) a.ref.ref_pos_out[slot0 + i] = rp;
-      }
-      if (failed && hl == 0 && a.ref.failures) atomicAdd(a.ref.failures + u, 1);
-    }
-    if (pool == KVC_POOL_BF16) {
-      if (valid[n]) {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.pools.v_bf16 : a.pools.k_bf16);
-        *reinterpret_cast<uint4*>(dst + row * d + hl * 8) = w[n];
-      }
-    } else {
-      store_quantised(a, pool, is_v, lpr, hl, valid[n], row, x);
-    }
-    if (valid[n] && hl == 0 && !is_v) {
-      a.pools.pos_out[slot0 + i] = p2[n];
-      if (a.pools.orig_pos_out) a.pools.orig_pos_out[slot0 + i] = p[n];
-    }
-  }
-  if (bad && hl == 0 && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
+  __syncthreads();
+  if (threadIdx.x == 0 && s_bad && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
 }
 
 }  // namespace
 
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
-  const int rows_per_block = (kThreads / 32) * (32 / (a.d / 8)) * kRows;
-  const int bx = (a.capacity + rows_per_block - 1) / rows_per_block;
   const int n_pools = a.pool_hi - a.pool_lo;
-  if (bx == 0 || n_pools <= 0) return cudaSuccess;
-  dim3 grid(bx, a.U, 2 * n_pools);            // z: (pool, K or V)
+  if (a.capacity < 1 || n_pools <= 0) return cudaSuccess;
+  // batches of a stream side by side: as many as the capacity needs, but
+  // no more than keep about 4,096 blocks in the grid (a block whose batches
+  // all lie past the stream's kept count exits at once)
+  const int64_t streams = static_cast<int64_t>(a.U) * 2 * n_pools;
+  const int64_t per_cap = (a.capacity + kBatch - 1) / kBatch;
+  const int64_t bx = std::max<int64_t>(1, std::min<int64_t>(per_cap, (4096 + streams - 1) / streams));
+  dim3 grid(static_cast<unsigned>(bx), a.U, 2 * n_pools);            // z: (pool, K or V)
   const bool general = a.rope_layout != KVC_ROPE_SPLIT_HALF || a.rotary_dim != a.d;
   if (a.ref.ref_pos != nullptr) {
     if (general) compact_kernel<true, true><<<grid, kThreads, 0, stream>>>(a);
