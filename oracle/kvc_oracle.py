@@ -486,14 +486,17 @@ def reference_rerotate(k_bits, p: int, p_new: int, ref_bits, p_ref: int, cos_tab
     return rerotate_bits(k_bits, p, p_new, cos_tab, sin_tab), k_bits.copy(), p, failed
 
 
-def renumber_drift(x, positions, cos_tab, sin_tab, use_store: bool) -> float:
+def renumber_drift(x, positions, cos_tab, sin_tab, use_store: bool, norm: str = "max") -> float:
     """Relative error of a key renumbered along `positions` (PACE App. D).
 
     x: exact pre-rotation key [d] (fp64).  The stored key starts as the bf16
     rounding of x rotated (in fp64) to positions[0]; every later entry is a
     renumber, done by re-rotating the stored key (use_store False) or through
-    the reference store.  Returns ||stored - exact|| / ||exact|| at the last
-    position, the exact key being x rotated in fp64 to it.
+    the reference store.  Returns the relative error of the stored key at
+    the last position against x rotated there in fp64: by default in the
+    maximum norm, max_i |stored_i - exact_i| / max_i |exact_i| (the page's
+    "relative key error"; its printed means after 23 / 71 / 240 renumbers
+    are reproduced in this norm), or in the Euclidean norm (norm="l2").
     """
     x = np.asarray(x, dtype=np.float64)
     d = x.size
@@ -512,7 +515,10 @@ def renumber_drift(x, positions, cos_tab, sin_tab, use_store: bool) -> float:
         else:
             k = rerotate_bits(k, int(p), int(p_new), cos_tab, sin_tab)
     e = exact(positions[-1])
-    return float(np.linalg.norm(bf16_bits_to_f32(k).astype(np.float64) - e) / np.linalg.norm(e))
+    diff = bf16_bits_to_f32(k).astype(np.float64) - e
+    if norm == "l2":
+        return float(np.linalg.norm(diff) / np.linalg.norm(e))
+    return float(np.abs(diff).max() / np.abs(e).max())
 
 
 def new_positions(kept_sorted, pos_in, renumber: bool) -> np.ndarray:

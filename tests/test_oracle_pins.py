@@ -512,7 +512,7 @@ def test_tiny_workload_end_to_end_invariants():
 
 # --------------------------------------------------------------------------- reference store
 
-def _drift(n, use_store, keys=32, seed=5):
+def _drift(n, use_store, keys=64, seed=5):
     cos, sin = wl.rope_tables(8192, 128, 1e6)          # Qwen3-8B rotary frequencies, L = 8,192
     cos, sin = cos.numpy(), sin.numpy()
     rng = np.random.default_rng(seed)
@@ -526,26 +526,34 @@ def _drift(n, use_store, keys=32, seed=5):
 
 def test_reference_store_drift_against_printed_figures():
     """PACE App. D figures (tests/golden/pace_drift.txt).  Re-rotating the
-    stored key compounds one bf16 rounding per renumber: the mean error grows
-    as sqrt(n) with the printed ratios, at a level within a factor 1.6 of the
-    printed values (the pages do not state their key distribution or error
-    norm).  Through the reference store the error stays at the printed
-    0.003 level after 60 and after 240 renumbers."""
+    stored key compounds one bf16 rounding per renumber.  The relative key
+    error is read in the maximum norm (largest element error over the key's
+    largest element): the simulated mean errors after 23 / 71 / 240 renumbers
+    then match the printed 0.011 / 0.019 / 0.037 within 20%, and the largest
+    error after 60 renumbers the printed 0.031 within 20% (64 keys; the
+    Euclidean norm would sit near 0.71 of every printed value).  Through the
+    reference store the error stays near two roundings (the printed 0.003)
+    after 60 and after 240 renumbers."""
     rows = _rows("pace_drift.txt")
     printed = {(r[0], r[1], int(r[2])): float(r[3]) for r in rows}
     naive = {n: _drift(n, False) for n in (23, 60, 71, 240)}
     store = {n: _drift(n, True) for n in (60, 240)}
     for n in (23, 71, 240):
         ratio = naive[n].mean() / printed[("naive", "mean", n)]
-        assert 1 / 1.6 < ratio < 1.6, (n, ratio)
+        assert 1 / 1.2 < ratio < 1.2, (n, ratio)
+    ratio = naive[60].max() / printed[("naive", "max", 60)]
+    assert 1 / 1.2 < ratio < 1.2, ratio
     # growth with the number of renumbers: the printed ratio 0.037 / 0.011
     g_ours = naive[240].mean() / naive[23].mean()
     g_page = printed[("naive", "mean", 240)] / printed[("naive", "mean", 23)]
     assert abs(g_ours / g_page - 1) < 0.15
     assert abs(g_ours / math.sqrt(240 / 23) - 1) < 0.15
-    # the store: about two roundings, whatever the number of renumbers
-    assert store[60].max() <= printed[("store", "max", 60)] * 1.35
-    assert store[240].max() <= printed[("store", "max", 60)] * 1.35
+    # the store: about two roundings (two bf16 half-ulps, 2^-8, relative to
+    # the largest element), whatever the number of renumbers
+    for n in (60, 240):
+        assert store[n].mean() <= printed[("store", "max", 60)] * 1.5
+        assert store[n].max() <= 2 * 2.0 ** -8
+    assert store[240].mean() <= 1.2 * store[60].mean()
     assert naive[60].max() > 4 * store[60].max()
 
 
