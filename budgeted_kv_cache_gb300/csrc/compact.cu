@@ -252,10 +252,15 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
     }
     s_bits = __half_as_ushort(__float2half_rn(sc));
   }
+  // one reciprocal per group, then a correctly rounded quotient per element
+  // (the same bits as x / sc with IEEE division)
+  const bool fast = recip_div_ok(sc);
+  const float y = __fdiv_rn(1.f, sc);
   int qv[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    int q = amax > 0.f ? __float2int_rn(__fdiv_rn(x[k], sc)) : 0;
+    const float qf = fast ? div_by_recip(x[k], sc, y) : __fdiv_rn(x[k], sc);
+    int q = amax > 0.f ? __float2int_rn(qf) : 0;
     q = q > static_cast<int>(qmax) ? static_cast<int>(qmax) : q;
     q = q < -static_cast<int>(qmax) ? -static_cast<int>(qmax) : q;
     qv[k] = q;
@@ -292,9 +297,9 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
 // index -> position -> rotary rows is walked once per batch instead of once
 // per row.  Then each lane group moves kRows rows at a time: the row loads
 // and the rotary-table loads of all of them are issued before any is used.
-// The grid has up to kBatch-row batches of every stream side by side; a
-// block takes the batches blockIdx.x, blockIdx.x + gridDim.x, ... that lie
-// below the stream's kept count.
+// The grid has up to kBatch-row batches of every stream side by side; the
+// block of batch lane x takes the batches x, x + lanes, ... that lie below
+// the stream's kept count.
 constexpr int kRows = 2;
 constexpr int kBatch = 512;
 constexpr uint8_t kValid = 1, kRotate = 2, kChange = 4;
@@ -310,8 +315,13 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / lpr;
   const int hl = lane % lpr;
-  const int is_v = blockIdx.z & 1;              // K rows and V rows go to separate blocks
-  const int pool = a.pool_lo + (blockIdx.z >> 1);
+  // blockIdx.x = (batch lane, pool, K or V) with K / V fastest, so key blocks
+  // (re-rotation arithmetic) and value blocks (plain copies) run side by side
+  const int n_pools = a.pool_hi - a.pool_lo;
+  const int is_v = blockIdx.x & 1;              // K rows and V rows go to separate blocks
+  const int pool = a.pool_lo + static_cast<int>((blockIdx.x >> 1) % n_pools);
+  const int bxi = static_cast<int>((blockIdx.x >> 1) / n_pools);   // batch lane of the stream
+  const int bxn = static_cast<int>(gridDim.x / (2 * n_pools));     // batch lanes per stream
   const int u = blockIdx.y;
   const int U = a.U;
   const int cap = a.capacity;
@@ -319,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   // belong to the next unit) and reported as a bad index
   const int cnt_raw = __ldg(a.kept_count + pool * U + u);
   const int cnt = clamp_count(cnt_raw, cap);
-  if (cnt != cnt_raw && blockIdx.x == 0 && threadIdx.x == 0 && a.unit_status)
+  if (cnt != cnt_raw && bxi == 0 && threadIdx.x == 0 && a.unit_status)
     a.unit_status[u] = KVC_UNIT_BAD_INDEX;
-  if (static_cast<int64_t>(blockIdx.x) * kBatch >= cnt) return;    // block-uniform
+  if (static_cast<int64_t>(bxi) * kBatch >= cnt) return;    // block-uniform
   if (threadIdx.x == 0) s_bad = 0;
 
   const int64_t slot0 = (static_cast<int64_t>(pool) * U + u) * cap;
@@ -332,8 +342,7 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   const int j0 = lr.j0;
   const int half = lr.half;
 
-  for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * kBatch; b0 < cnt;
-       b0 += static_cast<int64_t>(gridDim.x) * kBatch) {
+  for (int64_t b0 = static_cast<int64_t>(bxi) * kBatch; b0 < cnt; b0 += static_cast<int64_t>(bxn) * kBatch) {
     const int nb = static_cast<int>(min(static_cast<int64_t>(kBatch), cnt - b0));
     // ---------------- stage the batch's rows (one thread per row)
     __syncthreads();                            // the previous batch is done with the arrays
@@ -509,7 +518,7 @@ cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
   const int64_t streams = static_cast<int64_t>(a.U) * 2 * n_pools;
   const int64_t per_cap = (a.capacity + kBatch - 1) / kBatch;
   const int64_t bx = std::max<int64_t>(1, std::min<int64_t>(per_cap, (4096 + streams - 1) / streams));
-  dim3 grid(static_cast<unsigned>(bx), a.U, 2 * n_pools);            // z: (pool, K or V)
+  dim3 grid(static_cast<unsigned>(bx * 2 * n_pools), a.U);            // x: (batch lane, pool, K or V)
   const bool general = a.rope_layout != KVC_ROPE_SPLIT_HALF || a.rotary_dim != a.d;
   if (a.ref.ref_pos != nullptr) {
     if (general) compact_kernel<true, true><<<grid, kThreads, 0, stream>>>(a);

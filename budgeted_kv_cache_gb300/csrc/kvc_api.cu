@@ -542,17 +542,16 @@ kvc_status kvc_broadcast_kept(const kvc_shape* shape, const kvc_policy* policy,
 }
 
 size_t kvc_select_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy) {
-  (void)shape;
-  (void)policy;
-  return 0;
+  SelectPlan sp;
+  if (plan_select(shape, policy, &sp) != KVC_OK) return 0;
+  if (sp.byte_mode || sp.n_items <= 32768) return 0;
+  return select_long_ws_bytes(n_units(shape), sp.n_items);
 }
 
 kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const float* scores,
                       int32_t* kept_idx, int32_t* kept_count, int32_t* unit_status,
                       int64_t* floor_excess, void* workspace, size_t workspace_bytes,
                       kvc_stream stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   SelectPlan sp;
   kvc_status st = plan_select(shape, policy, &sp);
   if (st != KVC_OK) return st;
@@ -585,6 +584,15 @@ kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const fl
   a.kept_count = kept_count;
   a.unit_status = unit_status;
   a.floor_excess = floor_excess;
+  // token / page mode with long units: the multi-CTA selection when the
+  // caller gave its workspace (else the one-CTA-per-unit kernel, same result)
+  const size_t long_bytes = kvc_select_workspace_bytes(shape, policy);
+  if (long_bytes > 0 && workspace && workspace_bytes >= long_bytes) {
+    if (!aligned(workspace, 256)) return KVC_ERR_WORKSPACE;
+    a.long_ws = workspace;
+    if (launch_select_long(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+  }
   const size_t cache_bytes = static_cast<size_t>(sp.n_items) * 5;
   a.cache_items = cache_bytes <= 190 * 1024 ? 1 : 0;   // + 34 KB static shared memory
   const size_t smem = a.cache_items ? (cache_bytes + 15) / 16 * 16 : 0;

@@ -68,7 +68,11 @@ struct SelectArgs {
   int32_t* unit_status;
   int64_t* floor_excess;
   int32_t cache_items;         // 1: item keys staged in shared memory
+  void* long_ws;               // multi-CTA selection of long units (token / page mode), or null
 };
+
+// Workspace of the multi-CTA selection of long units (token / page mode).
+size_t select_long_ws_bytes(int64_t U, int64_t n_items);
 
 struct CompactArgs {
   int32_t U, d;
@@ -211,6 +215,7 @@ size_t score_small_smem_bytes(int d);
 cudaError_t launch_score_small(const ScoreArgs& a, int splits, float* logits, float2* split_stats,
                                float* lse2, cudaStream_t stream);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes);
+cudaError_t launch_select_long(const SelectArgs& a, cudaStream_t stream);
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
@@ -499,6 +504,25 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 // A row count read from caller memory, limited to [0, cap] (rows past a
 // pool's capacity would belong to the next unit or lie outside the pool).
 __device__ __forceinline__ int clamp_count(int n, int cap) { return n < 0 ? 0 : (n > cap ? cap : n); }
+
+// a / b from y = RN(1 / b), the reciprocal rounded to nearest: q0 = RN(a y),
+// r = a - b q0 (one fused multiply-add), q = RN(q0 + r y) -- the correction
+// step of Markstein's division (IA-64).  The quotient is within one ulp of
+// IEEE division, not always equal to it, so it only serves where a rounded
+// integer code is formed from it: the quantiser, whose codes rint(a / b)
+// equal those of IEEE division for every bf16 dividend with every bf16 and
+// every fp16 divisor in [2^-126, 2^125] with |a| <= 256 b (checked
+// exhaustively on the GPU; a group's quotients stay below about qmax).  A
+// zero quotient may come out with the other sign.
+__device__ __forceinline__ float div_by_recip(float a, float b, float y) {
+  const float q0 = __fmul_rn(a, y);
+  const float r = __fmaf_rn(-q0, b, a);
+  return __fmaf_rn(r, y, q0);
+}
+
+__device__ __forceinline__ bool recip_div_ok(float b) {
+  return b >= 0x1p-126f && b <= 0x1p125f;
+}
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

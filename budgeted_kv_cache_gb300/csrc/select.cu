@@ -693,3 +693,426 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_
 }
 
 }  // namespace kvc
+
+// ----------------------------------------------------------------------------
+// Token / page mode for units of more than 32,768 items: the same selection
+// (forced items, then the top k candidates by (score descending, index
+// ascending)) spread over many CTAs per unit.  Three histogram levels find
+// the k-th largest candidate key tau digit by digit (11, 11 and 10 bits,
+// most significant first): each level is one pass of all CTAs over the
+// unit's items (per-CTA shared-memory histograms added into the unit's
+// global one) followed by one CTA per unit that picks the digit.  Then a
+// counting pass, one CTA per unit for the per-chunk output offsets, and a
+// writing pass that emits the kept items of each chunk in index order.
+namespace kvc {
+namespace {
+
+constexpr int kLongThreads = 256;
+constexpr int kLongChunk = 8192;          // items per CTA (32 per thread)
+constexpr int kLongBins = 2048;
+
+// Per-unit state of the multi-CTA selection.
+struct LongState {
+  uint32_t n_forced, n_cand, err;
+  uint32_t phase;          // 0 searching, 1 no candidate taken, 2 all taken, 3 nothing kept (status set)
+  uint32_t prefix;         // key digits fixed so far
+  uint32_t rank;           // 0-based rank of the k-th candidate inside the prefix
+  uint32_t take_ties;      // candidates equal to tau taken, in index order
+  uint32_t pad;
+};
+
+struct LongWs {
+  LongState* st;           // [U]
+  uint32_t* hist;          // [U][kLongBins]
+  uint32_t* fixed;         // [U][chunks] forced + candidates above tau per chunk
+  uint32_t* ties;          // [U][chunks] candidates equal to tau per chunk
+  int64_t chunks;
+};
+
+__host__ __device__ inline LongWs long_ws(void* base, int64_t U, int64_t n_items) {
+  LongWs w;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  w.chunks = (n_items + kLongChunk - 1) / kLongChunk;
+  w.st = reinterpret_cast<LongState*>(p);
+  p += (U * sizeof(LongState) + 255) / 256 * 256;
+  w.hist = reinterpret_cast<uint32_t*>(p);
+  p += (U * kLongBins * 4 + 255) / 256 * 256;
+  w.fixed = reinterpret_cast<uint32_t*>(p);
+  p += (U * w.chunks * 4 + 255) / 256 * 256;
+  w.ties = reinterpret_cast<uint32_t*>(p);
+  return w;
+}
+
+// Class of item i: 0 = neither kept nor a candidate, 1 = forced, 2 = candidate
+// (with its order key), from its already loaded score and flags.
+__device__ __forceinline__ int long_class(const SelectArgs& a, int64_t i, float s, uint8_t f, uint32_t& key,
+                                          int& err) {
+  const bool window = i < a.sink_items || i >= a.n_items - a.recent_items;
+  const bool protect = f & KVC_FLAG_PROTECT;
+  const bool exclude = f & KVC_FLAG_EXCLUDE;
+  if (protect && exclude) err = 1;
+  if (window || protect) return 1;
+  if (exclude) return 0;
+  key = order_key(s);
+  return 2;
+}
+
+// The scores (and flags) of kLongIlp items per thread, all loads issued
+// before any is used: items i0 + q * kLongThreads + threadIdx.x.
+constexpr int kLongIlp = 8;
+__device__ __forceinline__ void long_load(const float* sc, const uint8_t* fl, int64_t i0, int64_t i1,
+                                          float (&s)[kLongIlp], uint8_t (&f)[kLongIlp]) {
+#pragma unroll
+  for (int q = 0; q < kLongIlp; ++q) {
+    const int64_t i = i0 + q * kLongThreads + threadIdx.x;
+    s[q] = i < i1 ? __ldg(sc + i) : 0.f;
+    f[q] = (fl && i < i1) ? __ldg(fl + i) : 0;
+  }
+}
+
+// Digit `level` of a key and whether the key matches the digits fixed so far.
+__device__ __forceinline__ bool long_digit(uint32_t key, int level, uint32_t prefix, uint32_t& digit) {
+  if (level == 0) {
+    digit = key >> 21;
+    return true;
+  }
+  if (level == 1) {
+    digit = (key >> 10) & 2047u;
+    return (key >> 21) == prefix;
+  }
+  digit = key & 1023u;
+  return (key >> 10) == prefix;
+}
+
+// One histogram level over chunk blockIdx.x of unit blockIdx.y (level 0 also
+// counts forced items and candidates and checks the flags).
+__global__ void __launch_bounds__(kLongThreads) select_long_hist(const __grid_constant__ SelectArgs a, int level) {
+  __shared__ uint32_t h[kLongBins];
+  __shared__ uint32_t s_forced, s_cand, s_err;
+  const int u = blockIdx.y;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  LongState* st = w.st + u;
+  if (level > 0 && st->phase != 0) return;                    // block-uniform
+  const uint32_t prefix = level > 0 ? st->prefix : 0u;
+  for (int i = threadIdx.x; i < kLongBins; i += kLongThreads) h[i] = 0;
+  if (threadIdx.x == 0) s_forced = s_cand = s_err = 0;
+  __syncthreads();
+  const int b = u / (a.L * a.Hkv);
+  const float* sc = a.scores + static_cast<int64_t>(u) * a.n_items;
+  const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * a.n_items : nullptr;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLongChunk;
+  const int64_t i1 = min(a.n_items, i0 + kLongChunk);
+  uint32_t n_forced = 0, n_cand = 0;
+  int err = 0;
+  for (int64_t ib = i0; ib < i1; ib += kLongIlp * kLongThreads) {
+    float sv[kLongIlp];
+    uint8_t fv[kLongIlp];
+    long_load(sc, fl, ib, i1, sv, fv);
+#pragma unroll
+    for (int q = 0; q < kLongIlp; ++q) {
+      const int64_t i = ib + q * kLongThreads + threadIdx.x;
+      uint32_t key = 0, dg = 0;
+      const int cls = i < i1 ? long_class(a, i, sv[q], fv[q], key, err) : 0;
+      n_forced += cls == 1;
+      n_cand += cls == 2;
+      if (cls == 2 && long_digit(key, level, prefix, dg)) atomicAdd(&h[dg], 1u);
+    }
+  }
+  if (level == 0) {
+    for (int o = 16; o > 0; o >>= 1) {
+      n_forced += __shfl_xor_sync(kFull, n_forced, o);
+      n_cand += __shfl_xor_sync(kFull, n_cand, o);
+      err |= __shfl_xor_sync(kFull, err, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      atomicAdd(&s_forced, n_forced);
+      atomicAdd(&s_cand, n_cand);
+      atomicOr(&s_err, static_cast<uint32_t>(err));
+    }
+  }
+  __syncthreads();
+  uint32_t* gh = w.hist + static_cast<int64_t>(u) * kLongBins;
+  for (int i = threadIdx.x; i < kLongBins; i += kLongThreads)
+    if (h[i]) atomicAdd(gh + i, h[i]);
+  if (level == 0 && threadIdx.x == 0) {
+    if (s_forced) atomicAdd(&st->n_forced, s_forced);
+    if (s_cand) atomicAdd(&st->n_cand, s_cand);
+    if (s_err) atomicOr(&st->err, s_err);
+  }
+}
+
+// Pick the digit of `level` for every unit (one CTA per unit): the bin where
+// the descending running count of candidates passes the target rank; the
+// histogram is cleared for the next level.
+__global__ void __launch_bounds__(kLongThreads) select_long_pick(const __grid_constant__ SelectArgs a, int level) {
+  __shared__ unsigned long long wtot[32];
+  __shared__ int s_bin;
+  __shared__ uint32_t s_above;
+  const int u = blockIdx.x;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  LongState* st = w.st + u;
+  uint32_t* gh = w.hist + static_cast<int64_t>(u) * kLongBins;
+  if (level == 0 && threadIdx.x == 0) {
+    // the unit's totals decide whether a search is needed at all
+    const uint32_t n_forced = st->n_forced, n_cand = st->n_cand;
+    uint32_t phase = 0;
+    if (st->err) {
+      phase = 3;
+      a.unit_status[u] = KVC_UNIT_BAD_FLAGS;
+    } else if (n_forced > static_cast<uint32_t>(a.budget_items)) {
+      phase = 3;
+      a.unit_status[u] = KVC_UNIT_OVER_BUDGET;
+    } else {
+      const uint32_t k = min(static_cast<uint32_t>(a.budget_items) - n_forced, n_cand);
+      if (k == 0) phase = 1;
+      else if (k == n_cand) phase = 2;
+      else st->rank = k - 1;
+    }
+    st->phase = phase;
+    st->prefix = 0;
+  }
+  __syncthreads();
+  if (st->phase != 0) {
+    for (int i = threadIdx.x; i < kLongBins; i += kLongThreads) gh[i] = 0;
+    return;
+  }
+  const int nb = level == 2 ? 1024 : kLongBins;
+  const uint32_t t = st->rank;
+  if (threadIdx.x == 0) s_bin = -1;
+  // each thread owns nb / 256 consecutive bins in descending order
+  const int per = nb / kLongThreads;
+  unsigned long long local = 0;
+  uint32_t c[8];
+  for (int k = 0; k < per; ++k) {
+    c[k] = gh[nb - 1 - (threadIdx.x * per + k)];
+    local += c[k];
+  }
+  // block exclusive scan of `local`
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  unsigned long long base = 0;
+  for (int i = 0; i < warp; ++i) base += wtot[i];
+  unsigned long long run = base + incl - local;
+  for (int k = 0; k < per; ++k) {
+    if (run <= t && t < run + c[k]) {
+      s_bin = nb - 1 - (threadIdx.x * per + k);
+      s_above = static_cast<uint32_t>(run);
+    }
+    run += c[k];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kLongBins; i += kLongThreads) gh[i] = 0;
+  if (threadIdx.x == 0) {
+    const int bn = s_bin;                          // always found: t < candidates in the prefix
+    st->prefix = (st->prefix << (level == 2 ? 10 : 11)) | static_cast<uint32_t>(bn < 0 ? 0 : bn);
+    st->rank = t - s_above;
+    if (level == 2) st->take_ties = st->rank + 1;
+  }
+}
+
+// Whether item (class cls, key) is kept given the unit's state; ties (key ==
+// tau) are reported separately.
+__device__ __forceinline__ void long_decide(const LongState& s, int cls, uint32_t key, bool& fixed, bool& tie) {
+  fixed = cls == 1 || (cls == 2 && (s.phase == 2 || (s.phase == 0 && key > s.prefix)));
+  tie = cls == 2 && s.phase == 0 && key == s.prefix;
+}
+
+__global__ void __launch_bounds__(kLongThreads) select_long_count(const __grid_constant__ SelectArgs a) {
+  __shared__ uint32_t s_f, s_t;
+  const int u = blockIdx.y;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  const LongState st = w.st[u];
+  if (st.phase == 3) return;
+  if (threadIdx.x == 0) s_f = s_t = 0;
+  __syncthreads();
+  const int b = u / (a.L * a.Hkv);
+  const float* sc = a.scores + static_cast<int64_t>(u) * a.n_items;
+  const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * a.n_items : nullptr;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLongChunk;
+  const int64_t i1 = min(a.n_items, i0 + kLongChunk);
+  uint32_t nf = 0, nt = 0;
+  int err = 0;
+  for (int64_t ib = i0; ib < i1; ib += kLongIlp * kLongThreads) {
+    float sv[kLongIlp];
+    uint8_t fv[kLongIlp];
+    long_load(sc, fl, ib, i1, sv, fv);
+#pragma unroll
+    for (int q = 0; q < kLongIlp; ++q) {
+      const int64_t i = ib + q * kLongThreads + threadIdx.x;
+      if (i >= i1) continue;
+      uint32_t key = 0;
+      const int cls = long_class(a, i, sv[q], fv[q], key, err);
+      bool fixed, tie;
+      long_decide(st, cls, key, fixed, tie);
+      nf += fixed;
+      nt += tie;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    nf += __shfl_xor_sync(kFull, nf, o);
+    nt += __shfl_xor_sync(kFull, nt, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&s_f, nf);
+    atomicAdd(&s_t, nt);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    w.fixed[static_cast<int64_t>(u) * w.chunks + blockIdx.x] = s_f;
+    w.ties[static_cast<int64_t>(u) * w.chunks + blockIdx.x] = s_t;
+  }
+}
+
+// Per unit: output offset of every chunk (kept items in index order), the
+// number of ties each chunk keeps, the kept count and the unit status.
+__global__ void __launch_bounds__(32) select_long_offsets(const __grid_constant__ SelectArgs a) {
+  const int u = blockIdx.x, lane = threadIdx.x;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  const LongState st = w.st[u];
+  int32_t* cnt = a.kept_count;
+  if (st.phase == 3) {
+    if (lane < KVC_N_POOLS) cnt[lane * a.U + u] = 0;
+    if (lane == 0 && a.floor_excess) a.floor_excess[u] = 0;
+    return;
+  }
+  uint32_t* fx = w.fixed + static_cast<int64_t>(u) * w.chunks;
+  uint32_t* ti = w.ties + static_cast<int64_t>(u) * w.chunks;
+  uint32_t out_run = 0, tie_run = 0;
+  for (int64_t c0 = 0; c0 < w.chunks; c0 += 32) {
+    const int64_t c = c0 + lane;
+    const uint32_t f = c < w.chunks ? fx[c] : 0u, t = c < w.chunks ? ti[c] : 0u;
+    // ties kept by this chunk: the part of [tie_off, tie_off + t) below take_ties
+    uint32_t ti_incl = t;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, ti_incl, o);
+      if (lane >= o) ti_incl += y;
+    }
+    const uint32_t tie_off = tie_run + ti_incl - t;
+    const uint32_t take = st.phase == 0 ? st.take_ties : 0u;
+    const uint32_t kt = tie_off >= take ? 0u : min(t, take - tie_off);
+    const uint32_t kept = f + kt;
+    uint32_t k_incl = kept;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, k_incl, o);
+      if (lane >= o) k_incl += y;
+    }
+    if (c < w.chunks) {
+      fx[c] = out_run + k_incl - kept;     // output offset of the chunk
+      ti[c] = kt;                          // ties the chunk keeps
+    }
+    out_run += __shfl_sync(kFull, k_incl, 31);
+    tie_run += __shfl_sync(kFull, ti_incl, 31);
+  }
+  if (lane < KVC_N_POOLS) cnt[lane * a.U + u] = lane == KVC_POOL_BF16 ? static_cast<int32_t>(out_run) * a.page_size : 0;
+  if (lane == 0) {
+    a.unit_status[u] = KVC_UNIT_OK;
+    if (a.floor_excess) a.floor_excess[u] = 0;
+  }
+}
+
+// Write the kept items of chunk blockIdx.x of unit blockIdx.y in index order
+// (256 items per round: a block scan of the keep flags gives each its slot).
+__global__ void __launch_bounds__(kLongThreads) select_long_write(const __grid_constant__ SelectArgs a) {
+  __shared__ uint32_t wsum[kLongThreads / 32];
+  const int u = blockIdx.y;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  const LongState st = w.st[u];
+  if (st.phase == 3) return;
+  const int b = u / (a.L * a.Hkv);
+  const float* sc = a.scores + static_cast<int64_t>(u) * a.n_items;
+  const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * a.n_items : nullptr;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLongChunk;
+  const int64_t i1 = min(a.n_items, i0 + kLongChunk);
+  uint32_t out = w.fixed[static_cast<int64_t>(u) * w.chunks + blockIdx.x];
+  const uint32_t ties_kept = w.ties[static_cast<int64_t>(u) * w.chunks + blockIdx.x];
+  uint32_t tie_run = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int P = a.page_size;
+  int32_t* dst = a.kept_idx + (static_cast<int64_t>(KVC_POOL_BF16) * a.U + u) * a.capacity;
+  int err = 0;
+  float sv[kLongIlp];
+  uint8_t fv[kLongIlp];
+  for (int64_t base = i0, r = 0; base < i1; base += kLongThreads, ++r) {
+    const int q = static_cast<int>(r % kLongIlp);
+    if (q == 0) long_load(sc, fl, base, i1, sv, fv);    // the next kLongIlp rounds' items
+    const int64_t i = base + threadIdx.x;
+    bool fixed = false, tie = false;
+    if (i < i1) {
+      uint32_t key = 0;
+      float s_q = sv[0];
+      uint8_t f_q = fv[0];
+#pragma unroll
+      for (int k = 1; k < kLongIlp; ++k)
+        if (q == k) {
+          s_q = sv[k];
+          f_q = fv[k];
+        }
+      const int cls = long_class(a, i, s_q, f_q, key, err);
+      long_decide(st, cls, key, fixed, tie);
+    }
+    // rank of this tie among the chunk's ties (index order)
+    const unsigned tm = __ballot_sync(kFull, tie);
+    if (lane == 0) wsum[warp] = __popc(tm);
+    __syncthreads();
+    uint32_t tie_before = tie_run + __popc(tm & ((1u << lane) - 1u)), tie_total = 0;
+    for (int k = 0; k < kLongThreads / 32; ++k) {
+      if (k < warp) tie_before += wsum[k];
+      tie_total += wsum[k];
+    }
+    __syncthreads();
+    const bool keep = fixed || (tie && tie_before < ties_kept);
+    const unsigned km = __ballot_sync(kFull, keep);
+    if (lane == 0) wsum[warp] = __popc(km);
+    __syncthreads();
+    uint32_t pos = out + __popc(km & ((1u << lane) - 1u)), total = 0;
+    for (int k = 0; k < kLongThreads / 32; ++k) {
+      if (k < warp) pos += wsum[k];
+      total += wsum[k];
+    }
+    __syncthreads();
+    if (keep) {
+      if (P == 1) {
+        dst[pos] = static_cast<int32_t>(i);
+      } else {
+        for (int j = 0; j < P; ++j) dst[static_cast<int64_t>(pos) * P + j] = static_cast<int32_t>(i * P + j);
+      }
+    }
+    out += total;
+    tie_run += tie_total;
+  }
+}
+
+}  // namespace
+
+size_t select_long_ws_bytes(int64_t U, int64_t n_items) {
+  const int64_t chunks = (n_items + kLongChunk - 1) / kLongChunk;
+  return static_cast<size_t>((U * sizeof(LongState) + 255) / 256 * 256 + (U * kLongBins * 4 + 255) / 256 * 256 +
+                             2 * ((U * chunks * 4 + 255) / 256 * 256));
+}
+
+cudaError_t launch_select_long(const SelectArgs& a, cudaStream_t stream) {
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  // state and level-0 histogram start at zero; every later level's
+  // histogram is cleared by the pick of the level before
+  cudaError_t err = cudaMemsetAsync(a.long_ws, 0,
+                                    (a.U * sizeof(LongState) + 255) / 256 * 256 + (a.U * kLongBins * 4 + 255) / 256 * 256,
+                                    stream);
+  if (err != cudaSuccess) return err;
+  const dim3 grid(static_cast<unsigned>(w.chunks), static_cast<unsigned>(a.U));
+  for (int level = 0; level < 3; ++level) {
+    select_long_hist<<<grid, kLongThreads, 0, stream>>>(a, level);
+    select_long_pick<<<a.U, kLongThreads, 0, stream>>>(a, level);
+  }
+  select_long_count<<<grid, kLongThreads, 0, stream>>>(a);
+  select_long_offsets<<<a.U, 32, 0, stream>>>(a);
+  select_long_write<<<grid, kLongThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

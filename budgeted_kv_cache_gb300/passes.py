@@ -12,7 +12,7 @@ import torch
 
 from . import (Policy, Pools, kvc_compact_rerotate_quant, kvc_decode_attn,
                kvc_decode_workspace_bytes, kvc_score, kvc_score_workspace_bytes, kvc_select,
-               make_shape, N_POOLS, SCORE_ACCUMULATE)
+               kvc_select_workspace_bytes, make_shape, N_POOLS, SCORE_ACCUMULATE)
 
 
 class CompactionPass:
@@ -38,6 +38,8 @@ class CompactionPass:
         self.unit_status = e(U, dt=torch.int32)
         self.compact_status = torch.zeros(U, dtype=torch.int32, device=dev)
         self.floor_excess = e(U, dt=torch.int64)
+        sb = kvc_select_workspace_bytes(self.shape, policy)
+        self.select_ws = e(sb, dt=torch.uint8) if sb > 0 else None
         self.pools = Pools.allocate(self.shape, policy, dev)
         db = kvc_decode_workspace_bytes(self.shape, policy)
         self.decode_ws = e(db, dt=torch.uint8) if db > 0 else None
@@ -54,7 +56,8 @@ class CompactionPass:
         src = scores if scores is not None else (
             self.page_scores if self.policy.page_size > 1 else self.scores)
         kvc_select(self.shape, self.policy, src, self.kept_idx, self.kept_count, self.unit_status,
-                   self.floor_excess, stream=stream)
+                   self.floor_excess, self.select_ws,
+                   self.select_ws.numel() if self.select_ws is not None else 0, stream=stream)
 
     def compact(self, k_cache, v_cache, pos_in, rope_cos, rope_sin, stream=None):
         kvc_compact_rerotate_quant(self.shape, self.policy, k_cache, v_cache, pos_in,

@@ -228,7 +228,12 @@ typedef struct {
  * kept_count   int32 [KVC_N_POOLS][U].
  * unit_status  int32 [U], always written (KVC_UNIT_OK or an error code).
  * floor_excess optional int64 [U] (byte mode; 0 otherwise).
- * The workspace is unused today: pass NULL and 0.
+ * workspace    optional: in token and page mode with more than 32,768 items
+ *              per unit, a workspace of kvc_select_workspace_bytes (256-byte
+ *              aligned; contents need not be initialised) lets the selection
+ *              of every unit run over many CTAs; without it each unit is
+ *              selected by one CTA (same result, slower).  Otherwise the
+ *              size is 0 and NULL is accepted.
  * ---------------------------------------------------------------------- */
 size_t kvc_select_workspace_bytes(const kvc_shape* shape, const kvc_policy* policy);
 kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const float* scores,

@@ -127,3 +127,27 @@ def kth_threshold(scores, kept_ref, forced_mask):
     if sel.size == 0:
         return math.inf
     return float(np.min(scores[sel]))
+
+
+# ------------------------------------------------------------------ oracle compaction in a process pool
+
+_POOL_TABLES = {}
+
+
+def _pool_init(cos, sin):
+    _POOL_TABLES["cos"], _POOL_TABLES["sin"] = cos, sin
+
+
+def _pool_compact(job):
+    k, v, pos, act, prm = job
+    return o.compact_unit(k, v, pos, act, prm, _POOL_TABLES["cos"], _POOL_TABLES["sin"])
+
+
+def oracle_compact_many(jobs, cos, sin, processes=None):
+    """oracle.compact_unit over many units in a pool of spawned processes
+    (spawned, not forked: the parent has an initialised CUDA context)."""
+    import multiprocessing as mp
+    import os
+    n = processes or max(1, min(16, os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(n, initializer=_pool_init, initargs=(cos, sin)) as pool:
+        return pool.map(_pool_compact, jobs, chunksize=max(1, len(jobs) // (4 * n)))

@@ -19,7 +19,7 @@ import torch
 
 import oracle as o
 import workloads as wl
-from helpers import (DECODE_ATOL, assert_pools_equal, assert_scores_close,
+from helpers import (bits, DECODE_ATOL, assert_pools_equal, assert_scores_close,
                      assert_selection_consistent, bits, kept_lists, params_of, unit_inputs,
                      unit_pools_from_gpu)
 
@@ -273,15 +273,71 @@ def _sample_units(w, n=3):
     return sorted({0, U // 2, U - 1} if n >= 3 else {0, U - 1})
 
 
+def _round_units(U, grid=152, extra=2):
+    """One unit of every round of the scoring kernel's work items (whole units
+    run round-robin over the CTAs), plus the last unit and a few more."""
+    us = set(range(0, U, grid)) | {U - 1}
+    us |= {min(U - 1, r * grid + grid // 2) for r in range(extra)}
+    return sorted(us)
+
+
 @pytest.mark.parametrize("make", [wl.qwen3_8b_32k, wl.pask_batch16, wl.commitkv_pages_128k],
                          ids=lambda f: f.__name__)
-def test_parity_full_size_sampled_units(kvc, make):
+def test_parity_full_size_all_units(kvc, make):
+    """Full-size workloads.  Every unit: the selection from the GPU's scores
+    (bit-exact against the oracle's selection of the same scores).  Every
+    unit (token and page mode) or 64 spread units (byte mode, 4,096 units):
+    the compaction of that kept set (bit-exact).  One unit per round of the
+    scoring kernel: scores within tolerance, decode, end-to-end consistency."""
+    from helpers import oracle_compact_many
     w = make()
     x = wl.make_inputs(w, device="cuda")
     p = run_pass(w, x)
     assert int(p.score_status.abs().sum()) == 0
     assert int(p.compact_status.abs().sum()) == 0
-    for u in _sample_units(w):
+    U, T, d = w.n_units, w.n_tokens, w.head_dim
+    prm = params_of(w)
+    table = x["action_table"].cpu().numpy() if "action_table" in x else None
+    scores = p.scores.cpu().numpy()
+    pscores = p.page_scores.cpu().numpy() if w.page_size > 1 else None
+    status = p.unit_status.cpu().numpy()
+    excess = p.floor_excess.cpu().numpy()
+    cnt = p.kept_count.cpu().numpy()
+    kept = p.kept_idx.cpu().numpy()
+    flags = x["flags"].cpu().numpy() if "flags" in x else None
+    tags = x["tags"].cpu().numpy() if "tags" in x else None
+    acts = {}
+    for u in range(U):
+        b, l, g = wl.unit_coords(w, u)
+        grp = o.layer_group(l, w.n_layers, w.n_layer_groups) if w.byte_mode else 0
+        act, exc, st = o.select_unit(scores[u], pscores[u] if pscores is not None else None, T, d, prm,
+                                     flags[b] if flags is not None else None,
+                                     tags[b] if tags is not None else None, table, grp)
+        assert int(status[u]) == st, f"unit {u}"
+        if w.byte_mode:
+            assert int(excess[u]) == exc, f"unit {u}"
+        for a in (o.ACT_INT4, o.ACT_INT8, o.ACT_BF16):
+            n = int(cnt[a - 1, u])
+            assert np.array_equal(kept[a - 1, u, :n], np.nonzero(act == a)[0]), f"unit {u} pool {a}"
+        acts[u] = act
+    # compaction: the kept rows only (the oracle's positions are ranks among
+    # the kept rows or their old positions, so a gathered sub-problem gives
+    # the same pools up to the indices, which the selection check covered)
+    cu = list(range(U)) if not w.byte_mode else list(range(0, U, U // 64))
+    jobs = []
+    for u in cu:
+        b, l, g = wl.unit_coords(w, u)
+        keep = np.nonzero(acts[u] != o.ACT_RELEASE)[0]
+        kt = torch.from_numpy(keep).to("cuda")
+        jobs.append((bits(x["k_cache"][b, l, g].index_select(0, kt)), bits(x["v_cache"][b, l, g].index_select(0, kt)),
+                     x["pos_in"][u].index_select(0, kt).cpu().numpy(), acts[u][keep], prm))
+    refs = oracle_compact_many(jobs, x["rope_cos"].cpu().numpy(), x["rope_sin"].cpu().numpy())
+    for u, ref_pools in zip(cu, refs):
+        got = unit_pools_from_gpu(p, u, w)
+        for a, rp in ref_pools.items():
+            rp.idx = got[a].idx if got[a].idx.size == rp.idx.size else rp.idx
+        assert_pools_equal(got, ref_pools)
+    for u in _round_units(U):
         check_unit(w, x, p, u)
     del p, x
     torch.cuda.empty_cache()
