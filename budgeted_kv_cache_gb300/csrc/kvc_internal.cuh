@@ -542,6 +542,19 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of a K-major bf16 operand of 16 columns
+// stored with the 32-byte swizzle: rows of 16 elements (32 B), 8-row atoms
+// of 256 B.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(1) << 16;                     // leading byte offset (unused)
+  d |= static_cast<uint64_t>(256 >> 4) << 32;              // stride byte offset: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                     // descriptor version
+  d |= static_cast<uint64_t>(6) << 61;                     // 32-byte swizzle
+  return d;
+}
+
 // Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
 __host__ __device__ constexpr uint32_t mma_idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |

@@ -52,6 +52,8 @@ constexpr uint32_t kMmaSleepNs = 32;
 struct Smem {
   uint8_t* q;           // n_kc chunks of q_rows x 128 B
   uint8_t* k;           // n_stages stages of n_kc chunks of 128 x 128 B
+  uint8_t* ones;        // 128 x 16 bf16 ones, 32-byte swizzled rows (pass-2 extra K step)
+  uint8_t* aug;         // q_rows x 16 bf16: -lse / scale as three parts per window row
   uint64_t* full;
   uint64_t* empty;
   uint64_t* tfull;      // [2]
@@ -60,6 +62,7 @@ struct Smem {
   uint64_t* qempty;
   uint64_t* mmadone;
   uint64_t* redfull;    // [4 slots][4 TMEM lane quarters]
+  uint64_t* augfull;    // the item's aug rows are written
   uint32_t* tmem_slot;
   int* abort_flag;
   float* lam;           // [256] negated log-sum-exp of each window row
@@ -72,7 +75,9 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n
   Smem s;
   s.q = base;
   s.k = base + n_kc * q_rows * 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.k + n_stages * n_kc * kChunkBytes);
+  s.ones = s.k + n_stages * n_kc * kChunkBytes;
+  s.aug = s.ones + 128 * 32;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.aug + q_rows * 32);
   s.full = bars;
   s.empty = bars + n_stages;
   s.tfull = bars + 2 * n_stages;
@@ -81,7 +86,8 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int n_kc, int q_rows, int n
   s.qempty = bars + 2 * n_stages + 5;
   s.mmadone = bars + 2 * n_stages + 6;
   s.redfull = bars + 2 * n_stages + 8;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * n_stages + 24);
+  s.augfull = bars + 2 * n_stages + 24;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * n_stages + 26);
   s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
   s.lam = reinterpret_cast<float*>(s.tmem_slot + 4);
   s.red = s.lam + 256;
@@ -173,19 +179,16 @@ __device__ __forceinline__ float exp_sum(const uint32_t (&r)[N], float cs, float
   return u2.x + u2.y;
 }
 
-// Pass 2: add exp2(z * cs - lse_r) of N rows r to the token's mass (four
-// packed pairs of running sums).  nlam holds -lse of those N rows.
+// Pass 2: add exp2(y) of N rows to the token's mass (four packed pairs of
+// running sums), y = D * cs where the accumulator D = z - lse_r / cs
+// already holds the row's log-sum-exp (the extra K step of the MMA).
 template <int N>
-__device__ __forceinline__ void mass_accum(const uint32_t (&r)[N], const float* nlam, float cs,
-                                           float2 (&acc)[4]) {
+__device__ __forceinline__ void mass_accum(const uint32_t (&r)[N], float cs, float2 (&acc)[4]) {
   const float2 cs2 = make_float2(cs, cs);
 #pragma unroll
   for (int i = 0; i < N; i += 4) {
-    const float4 nl = *reinterpret_cast<const float4*>(nlam + i);
-    const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), cs2,
-                                make_float2(nl.x, nl.y));
-    const float2 y = __ffma2_rn(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])),
-                                cs2, make_float2(nl.z, nl.w));
+    const float2 x = __fmul2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), cs2);
+    const float2 y = __fmul2_rn(make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), cs2);
     const int k = (i >> 2) & 1;
     acc[2 * k] = __fadd2_rn(acc[2 * k], make_float2(ex2_approx(x.x), ex2_approx(x.y)));
     acc[2 * k + 1] = __fadd2_rn(acc[2 * k + 1], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
@@ -195,14 +198,13 @@ __device__ __forceinline__ void mass_accum(const uint32_t (&r)[N], const float* 
 // Same with the causal mask of the last tiles: row r0 + i sees token j iff
 // j <= Tq + (r0 + i) mod W.
 template <int N>
-__device__ __forceinline__ void mass_accum_masked(const uint32_t (&r)[N], const float* nlam,
-                                                  float cs, int r0, int64_t j, int64_t Tq, int W,
-                                                  float2 (&acc)[4]) {
+__device__ __forceinline__ void mass_accum_masked(const uint32_t (&r)[N], float cs, int r0, int64_t j,
+                                                  int64_t Tq, int W, float2 (&acc)[4]) {
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
     const bool v0 = j <= Tq + ((r0 + i) % W), v1 = j <= Tq + ((r0 + i + 1) % W);
-    const float e0 = v0 ? ex2_approx(fmaf(__uint_as_float(r[i]), cs, nlam[i])) : 0.f;
-    const float e1 = v1 ? ex2_approx(fmaf(__uint_as_float(r[i + 1]), cs, nlam[i + 1])) : 0.f;
+    const float e0 = v0 ? ex2_approx(__uint_as_float(r[i]) * cs) : 0.f;
+    const float e1 = v1 ? ex2_approx(__uint_as_float(r[i + 1]) * cs) : 0.f;
     acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], make_float2(e0, e1));
   }
 }
@@ -238,6 +240,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     mbar_init(smem_u32(s.qfull), 1);
     mbar_init(smem_u32(s.qempty), 1);
     mbar_init(smem_u32(s.mmadone), 1);
+    mbar_init(smem_u32(s.augfull), 1);
     for (int i = 0; i < 16; ++i) mbar_init(smem_u32(&s.redfull[i]), 96);   // 3 groups x 32 threads
     *s.abort_flag = 0;
     fence_barrier_init();
@@ -247,6 +250,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
     uint4* q4 = reinterpret_cast<uint4*>(s.q);
     const int n16 = n_kc * q_chunk_bytes / 16;
     for (int i = threadIdx.x; i < n16; i += kThreads) q4[i] = make_uint4(0, 0, 0, 0);
+    // the all-ones operand of pass 2's extra K step (bf16 1.0 = 0x3f80)
+    uint4* o4 = reinterpret_cast<uint4*>(s.ones);
+    for (int i = threadIdx.x; i < 128 * 32 / 16; i += kThreads) o4[i] = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
   }
   fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
@@ -322,6 +328,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
       constexpr int KS = D / 16;
       const uint64_t qdesc0 = sw128_desc(smem_u32(s.q));
       const uint64_t kdesc0 = sw128_desc(smem_u32(s.k));
+      const uint64_t onesdesc = sw32_desc(smem_u32(s.ones));
+      const uint64_t augdesc = sw32_desc(smem_u32(s.aug));
       const uint32_t qchunk16 = q_chunk_bytes >> 4;
       uint32_t jt = 0;
       int li = 0;
@@ -332,6 +340,11 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         tc_fence_after();
         bool ok = true;
         for (int pass = a.row_lse ? 1 : 0; pass < 2 && ok; ++pass) {
+          // pass 2 adds -lse / scale through one more K step: wait for the rows
+          if (pass == 1 && !mbar_wait_backoff(smem_u32(s.augfull), li & 1, abort_flag, kMmaSleepNs)) {
+            ok = false;
+            break;
+          }
           for (int t = 0; t < nt; ++t, ++jt) {
             const uint32_t st = jt % a.n_stages;
             const uint32_t ph = (jt / a.n_stages) & 1;
@@ -363,6 +376,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
                 const uint64_t bd = qdesc0 + ((ks >> 2) * qchunk16 + (ks & 3) * 2);
                 tc_mma_bf16(d_tmem, ad, bd, idesc2, ks > 0);
               }
+              tc_mma_bf16(d_tmem, onesdesc, augdesc, idesc2, 1);
             }
             tc_commit(smem_u32(&s.empty[st]));
             tc_commit(smem_u32(&s.tfull[tb]));
@@ -533,6 +547,33 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
         for (int r = a.R + et; r < a.Rp; r += kEpiThreads) s.lam[r] = -INFINITY;
         named_bar_sync(1, kEpiThreads);
       }
+      // Pass 2's extra K step: row r of `aug` holds -lse_r / scale as the sum
+      // of three bf16 parts (all 24 bits of the fp32 value; the rest of the
+      // row zero), and every row of `ones` is all ones, so the MMA adds that
+      // sum to z = q . k and the epilogue forms z * scale - lse_r with one
+      // multiply.  A padding row gets a large negative finite value (its
+      // exponentials vanish).  The previous item's pass-2 MMAs, the last
+      // readers of `aug`, have completed: this epilogue consumed all of their
+      // accumulators before it reached this point.
+      for (int r = et; r < a.Rp; r += kEpiThreads) {
+        const float lm = s.lam[r];
+        float hi = -0x1p120f, mid = 0.f, lo = 0.f;
+        if (lm != -INFINITY) {
+          const float av = lm / cs;
+          hi = __bfloat162float(__float2bfloat16_rn(av));
+          const float r1 = av - hi;
+          mid = __bfloat162float(__float2bfloat16_rn(r1));
+          lo = __bfloat162float(__float2bfloat16_rn(r1 - mid));
+        }
+        uint4* row = reinterpret_cast<uint4*>(s.aug + (r >> 3) * 256 + (r & 7) * 32);
+        const uint32_t w0 = static_cast<uint32_t>(float_to_bf16_bits(hi)) |
+                            (static_cast<uint32_t>(float_to_bf16_bits(mid)) << 16);
+        row[0] = make_uint4(w0, float_to_bf16_bits(lo), 0, 0);
+        row[1] = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, kEpiThreads);
+      if (et == 0) mbar_arrive(smem_u32(s.augfull));
 
       // ---------------- pass 2: per-token sum of exp2(z cs - lse) over rows
       // The four groups' partial sums of pass-2 tile jt2 meet in slot jt2 % 4
@@ -602,8 +643,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
-            if (!masked) mass_accum<64>(r, s.lam + p2_r0, cs, acc);
-            else mass_accum_masked<64>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
+            if (!masked) mass_accum<64>(r, cs, acc);
+            else mass_accum_masked<64>(r, cs, p2_r0, j, Tq, a.W, acc);
           } else if (p2_n == 32 || (kAnyR && p2_n == 48)) {
             uint32_t r[32];
             tmem_ld32_issue(taddr, r);
@@ -613,11 +654,11 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
-            if (!masked) mass_accum<32>(r, s.lam + p2_r0, cs, acc);
-            else mass_accum_masked<32>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
+            if (!masked) mass_accum<32>(r, cs, acc);
+            else mass_accum_masked<32>(r, cs, p2_r0, j, Tq, a.W, acc);
             if (kAnyR && p2_n == 48) {
-              if (!masked) mass_accum<16>(r16, s.lam + p2_r0 + 32, cs, acc);
-              else mass_accum_masked<16>(r16, s.lam + p2_r0 + 32, cs, p2_r0 + 32, j, Tq, a.W, acc);
+              if (!masked) mass_accum<16>(r16, cs, acc);
+              else mass_accum_masked<16>(r16, cs, p2_r0 + 32, j, Tq, a.W, acc);
             }
           } else if (kAnyR && p2_n == 16) {
             uint32_t r[16];
@@ -625,8 +666,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[tb]));
-            if (!masked) mass_accum<16>(r, s.lam + p2_r0, cs, acc);
-            else mass_accum_masked<16>(r, s.lam + p2_r0, cs, p2_r0, j, Tq, a.W, acc);
+            if (!masked) mass_accum<16>(r, cs, acc);
+            else mass_accum_masked<16>(r, cs, p2_r0, j, Tq, a.W, acc);
           } else {
             tc_fence_before();
             __syncwarp();
@@ -680,7 +721,8 @@ size_t score_smem_bytes(int d, int q_rows, int n_stages) {
   size_t bytes = 1024;                                   // alignment slack
   bytes += static_cast<size_t>(n_kc) * q_rows * 128;     // Q
   bytes += static_cast<size_t>(n_stages) * n_kc * kChunkBytes;
-  bytes += (2 * n_stages + 24) * 8;                      // barriers
+  bytes += 128 * 32 + static_cast<size_t>(q_rows) * 32;  // ones, aug
+  bytes += (2 * n_stages + 26) * 8;                      // barriers
   bytes += 16;                                           // tmem slot, abort flag
   bytes += (256 + 2048 + 2 * 1024) * 4;                 // lam, red, hm, hl
   return bytes;
