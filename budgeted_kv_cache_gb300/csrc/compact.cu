@@ -290,6 +290,69 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
   }
 }
 
+constexpr int kBatch = 512;
+constexpr uint8_t kValid = 1, kRotate = 2, kChange = 4;
+
+// Stages the kept index, old and new position and flags of rows b0 .. b0 +
+// nb - 1 of one (unit, pool) stream in shared memory, one thread per row
+// (all the loads of the batch in flight together).  Value streams (is_v)
+// need no positions.  Returns whether this thread met a bad row.
+template <bool kStore>
+__device__ __forceinline__ bool stage_batch(const CompactArgs& a, int pool, int is_v, int u, int64_t slot0,
+                                            int64_t b0, int nb, bool use_store, int32_t* s_t, int32_t* s_p,
+                                            int32_t* s_p2, int32_t* s_pr, uint8_t* s_f) {
+  const int U = a.U;
+  const int cap = a.capacity;
+  bool bad = false;
+  for (int q = threadIdx.x; q < nb; q += kThreads) {
+    const int64_t i = b0 + q;
+    const int32_t t = __ldg(a.kept_idx + slot0 + i);
+    uint8_t f = 0;
+    int32_t p = 0, p2 = 0, pr = -1;
+    if (t < 0 || t >= a.T) {
+      bad = true;
+    } else {
+      f = kValid;
+      if (!is_v) {
+        p = __ldg(a.pos_in + static_cast<int64_t>(u) * a.T + t);
+        p2 = p;
+        if (a.renumber) {
+          // rank among the kept rows of every pool (pools are disjoint, ascending)
+          int rank = static_cast<int>(i);
+          for (int qq = 0; qq < KVC_N_POOLS; ++qq) {
+            if (qq == pool) continue;
+            const int cq = clamp_count(__ldg(a.kept_count + qq * U + u), cap);
+            if (cq > 0)
+              rank += lower_bound_i32(a.kept_idx + (static_cast<int64_t>(qq) * U + u) * cap, cq, t);
+          }
+          p2 = rank;
+        }
+        if (p2 != p) {
+          if (p < 0 || p >= a.rope_max_pos || p2 < 0 || p2 >= a.rope_max_pos) {
+            f = 0;
+            bad = true;
+          } else {
+            f |= kRotate;
+          }
+        }
+        if (use_store && (f & kValid)) {
+          pr = __ldg(a.ref.ref_pos + static_cast<int64_t>(u) * a.T + t);
+          if (pr >= a.rope_max_pos) {
+            f = 0;
+            bad = true;
+          }
+        }
+      }
+    }
+    s_t[q] = t;
+    s_p[q] = p;
+    s_p2[q] = p2;
+    if (kStore) s_pr[q] = pr;
+    s_f[q] = f;
+  }
+  return bad;
+}
+
 // A block works on one (unit, pool, K-or-V) stream, in batches of up to
 // kBatch kept rows.  For a batch it first stages every row's kept index, old
 // position, new position and status in shared memory (one thread per row,
@@ -301,8 +364,6 @@ __device__ __forceinline__ void store_quantised(const CompactArgs& a, int pool, 
 // block of batch lane x takes the batches x, x + lanes, ... that lie below
 // the stream's kept count.
 constexpr int kRows = 2;
-constexpr int kBatch = 512;
-constexpr uint8_t kValid = 1, kRotate = 2, kChange = 4;
 
 template <bool kStore, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs a) {
@@ -346,53 +407,7 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
     const int nb = static_cast<int>(min(static_cast<int64_t>(kBatch), cnt - b0));
     // ---------------- stage the batch's rows (one thread per row)
     __syncthreads();                            // the previous batch is done with the arrays
-    bool bad = false;
-    for (int q = threadIdx.x; q < nb; q += kThreads) {
-      const int64_t i = b0 + q;
-      const int32_t t = __ldg(a.kept_idx + slot0 + i);
-      uint8_t f = 0;
-      int32_t p = 0, p2 = 0, pr = -1;
-      if (t < 0 || t >= a.T) {
-        bad = true;
-      } else {
-        f = kValid;
-        if (!is_v) {
-          p = __ldg(a.pos_in + static_cast<int64_t>(u) * a.T + t);
-          p2 = p;
-          if (a.renumber) {
-            // rank among the kept rows of every pool (pools are disjoint, ascending)
-            int rank = static_cast<int>(i);
-            for (int qq = 0; qq < KVC_N_POOLS; ++qq) {
-              if (qq == pool) continue;
-              const int cq = clamp_count(__ldg(a.kept_count + qq * U + u), cap);
-              if (cq > 0)
-                rank += lower_bound_i32(a.kept_idx + (static_cast<int64_t>(qq) * U + u) * cap, cq, t);
-            }
-            p2 = rank;
-          }
-          if (p2 != p) {
-            if (p < 0 || p >= a.rope_max_pos || p2 < 0 || p2 >= a.rope_max_pos) {
-              f = 0;
-              bad = true;
-            } else {
-              f |= kRotate;
-            }
-          }
-          if (use_store && (f & kValid)) {
-            pr = __ldg(a.ref.ref_pos + static_cast<int64_t>(u) * a.T + t);
-            if (pr >= a.rope_max_pos) {
-              f = 0;
-              bad = true;
-            }
-          }
-        }
-      }
-      s_t[q] = t;
-      s_p[q] = p;
-      s_p2[q] = p2;
-      if (kStore) s_pr[q] = pr;
-      s_f[q] = f;
-    }
+    const bool bad = stage_batch<kStore>(a, pool, is_v, u, slot0, b0, nb, use_store, s_t, s_p, s_p2, s_pr, s_f);
     if (bad) s_bad = 1;
     __syncthreads();
 
@@ -507,11 +522,175 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
   if (threadIdx.x == 0 && s_bad && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
 }
 
+// ----------------------------------------------------------------------------
+// bf16 pool with every element in split-half rotation and no reference
+// store (the common case): keys and values of the same rows move together.
+// A block takes batches of one unit's kept rows (kCopyBatch at a time, staged
+// as above).  Each lane copies its 16-byte pieces of a row -- key, value and,
+// for a key that changes position, the four rotary-table pieces it needs --
+// into shared memory with asynchronous copies, kCopyStages - 1 steps ahead
+// of the step it is working on; no registers are held by the copies in flight,
+// so a block keeps several rows per lane group in flight.  A lane reads back
+// only the pieces it copied itself, so no block-wide barrier separates the
+// copy and the use.
+constexpr int kCopyStages = 4;
+constexpr int kCopyRows = 1;          // rows per lane group and step
+constexpr int kCopyBatch = 256;       // rows staged per block and batch
+constexpr int kPieces = 6;            // key, value, cos(p), sin(p), cos(p'), sin(p')
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(saddr), "l"(src), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_hint(void* dst, const uint4& w, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(w.x), "r"(w.y),
+               "r"(w.z), "r"(w.w), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+size_t compact_copy_smem_bytes() {
+  return static_cast<size_t>(kCopyStages) * kCopyRows * kPieces * kThreads * 16;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) compact_copy_kernel(const CompactArgs a) {
+  extern __shared__ uint4 s_pieces[];   // [stage][row n][piece][thread]
+  __shared__ int32_t s_t[kCopyBatch], s_p[kCopyBatch], s_p2[kCopyBatch];
+  __shared__ uint8_t s_f[kCopyBatch];
+  __shared__ int s_bad;
+  const int d = a.d;
+  const int lpr = d / 8;                        // lanes per row (16 B = 8 bf16 per lane)
+  const int rows_per_warp = 32 / lpr;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / lpr;
+  const int hl = lane % lpr;
+  const int groups = (kThreads / 32) * rows_per_warp;   // lane groups of the block
+  const int grp = warp * rows_per_warp + sub;
+  const int per_step = groups * kCopyRows;
+  const int pool = KVC_POOL_BF16;
+  const int u = blockIdx.y;
+  const int U = a.U;
+  const int cap = a.capacity;
+  const int cnt_raw = __ldg(a.kept_count + pool * U + u);
+  const int cnt = clamp_count(cnt_raw, cap);
+  if (cnt != cnt_raw && blockIdx.x == 0 && threadIdx.x == 0 && a.unit_status)
+    a.unit_status[u] = KVC_UNIT_BAD_INDEX;
+  if (static_cast<int64_t>(blockIdx.x) * kCopyBatch >= cnt) return;    // block-uniform
+  if (threadIdx.x == 0) s_bad = 0;
+  const int64_t slot0 = (static_cast<int64_t>(pool) * U + u) * cap;
+  const LaneRot lr = lane_rot(KVC_ROPE_SPLIT_HALF, d, lane, hl, lpr);
+  const int j0 = lr.j0;
+  const int half = lr.half;
+  const uint32_t piece0 = smem_u32(s_pieces) + threadIdx.x * 16;
+  auto piece = [&](int stage, int n, int c) {
+    return piece0 + static_cast<uint32_t>(((stage * kCopyRows + n) * kPieces + c) * kThreads * 16);
+  };
+  const int64_t row0 = static_cast<int64_t>(u) * a.T;
+  // the rotary tables are read by every unit: keep them in L2 while the
+  // rows stream through it once
+  const uint64_t keep = l2_policy_evict_last();
+  const uint64_t stream = l2_policy_evict_first();
+
+  for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * kCopyBatch; b0 < cnt;
+       b0 += static_cast<int64_t>(gridDim.x) * kCopyBatch) {
+    const int nb = static_cast<int>(min(static_cast<int64_t>(kCopyBatch), cnt - b0));
+    __syncthreads();                            // the previous batch is done with the arrays
+    const bool bad = stage_batch<false>(a, pool, 0, u, slot0, b0, nb, false, s_t, s_p, s_p2, nullptr, s_f);
+    if (bad) s_bad = 1;
+    __syncthreads();
+
+    // step k: lane group g takes rows q = k * per_step + n * groups + g
+    const int n_steps = (nb + per_step - 1) / per_step;
+    auto issue = [&](int k) {
+      const int stage = k % kCopyStages;
+#pragma unroll
+      for (int n = 0; n < kCopyRows; ++n) {
+        const int q = k * per_step + n * groups + grp;
+        const uint8_t f = (k < n_steps && q < nb) ? s_f[q] : 0;
+        if (f & kValid) {
+          const int64_t r = row0 + s_t[q];
+          cp_async16(piece(stage, n, 0), reinterpret_cast<const uint4*>(a.k + r * d) + hl, stream);
+          cp_async16(piece(stage, n, 1), reinterpret_cast<const uint4*>(a.v + r * d) + hl, stream);
+          if ((f & kRotate) && lr.active) {
+            const int64_t p = s_p[q], p2 = s_p2[q];
+            cp_async16(piece(stage, n, 2), a.cos + p * half + j0, keep);
+            cp_async16(piece(stage, n, 3), a.sin + p * half + j0, keep);
+            cp_async16(piece(stage, n, 4), a.cos + p2 * half + j0, keep);
+            cp_async16(piece(stage, n, 5), a.sin + p2 * half + j0, keep);
+          }
+        }
+      }
+      cp_async_commit();                        // one group per step, empty or not
+    };
+#pragma unroll
+    for (int k = 0; k < kCopyStages - 1; ++k) issue(k);
+    for (int k = 0; k < n_steps; ++k) {
+      issue(k + kCopyStages - 1);
+      cp_async_wait<kCopyStages - 1>();         // this thread's pieces of step k have landed
+      const int stage = k % kCopyStages;
+#pragma unroll
+      for (int n = 0; n < kCopyRows; ++n) {
+        const int q = k * per_step + n * groups + grp;
+        const uint8_t f = q < nb ? s_f[q] : 0;
+        const bool valid = f & kValid;
+        const bool rot = (f & kRotate) != 0;
+        uint4 w = make_uint4(0, 0, 0, 0), wv = w;
+        float4 tab[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tab[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(piece(stage, n, 0)));
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(wv.x), "=r"(wv.y), "=r"(wv.z), "=r"(wv.w) : "r"(piece(stage, n, 1)));
+        }
+        if (rot && lr.active) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(tab[c].x), "=f"(tab[c].y), "=f"(tab[c].z), "=f"(tab[c].w)
+                         : "r"(piece(stage, n, 2 + c)));
+        }
+        // whole warps: the rotation exchanges halves between partner lanes
+        if (__any_sync(kFull, rot)) {
+          float x[8];
+          unpack8(w, x);
+          rerotate_lane(lpr, hl, rot, tab, x, w);
+        }
+        if (valid) {
+          const int64_t i = b0 + q;
+          const int64_t row = static_cast<int64_t>(u) * cap + i;
+          st_global_hint(static_cast<__nv_bfloat16*>(a.pools.k_bf16) + row * d + hl * 8, w, stream);
+          st_global_hint(static_cast<__nv_bfloat16*>(a.pools.v_bf16) + row * d + hl * 8, wv, stream);
+          if (hl == 0) {
+            a.pools.pos_out[slot0 + i] = s_p2[q];
+            if (a.pools.orig_pos_out) a.pools.orig_pos_out[slot0 + i] = s_p[q];
+          }
+        }
+      }
+    }
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && s_bad && a.unit_status) a.unit_status[u] = KVC_UNIT_BAD_INDEX;
+}
+
 }  // namespace
 
 cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
   const int n_pools = a.pool_hi - a.pool_lo;
   if (a.capacity < 1 || n_pools <= 0) return cudaSuccess;
+  const bool general = a.rope_layout != KVC_ROPE_SPLIT_HALF || a.rotary_dim != a.d;
+  if (a.ref.ref_pos == nullptr && !general && n_pools == 1 && a.pool_lo == KVC_POOL_BF16) {
+    // keys and values together, every batch of a unit in its own block
+    const int64_t bx = (a.capacity + kCopyBatch - 1) / kCopyBatch;
+    const size_t smem = compact_copy_smem_bytes();
+    cudaError_t err = cudaFuncSetAttribute(compact_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    compact_copy_kernel<<<dim3(static_cast<unsigned>(bx), a.U), kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
   // batches of a stream side by side: as many as the capacity needs, but
   // no more than keep about 4,096 blocks in the grid (a block whose batches
   // all lie past the stream's kept count exits at once)
@@ -519,7 +698,6 @@ cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
   const int64_t per_cap = (a.capacity + kBatch - 1) / kBatch;
   const int64_t bx = std::max<int64_t>(1, std::min<int64_t>(per_cap, (4096 + streams - 1) / streams));
   dim3 grid(static_cast<unsigned>(bx * 2 * n_pools), a.U);            // x: (batch lane, pool, K or V)
-  const bool general = a.rope_layout != KVC_ROPE_SPLIT_HALF || a.rotary_dim != a.d;
   if (a.ref.ref_pos != nullptr) {
     if (general) compact_kernel<true, true><<<grid, kThreads, 0, stream>>>(a);
     else compact_kernel<true, false><<<grid, kThreads, 0, stream>>>(a);
