@@ -42,7 +42,7 @@ METRIC = "KV tokens compacted/sec per layer·head and % of roofline (HBM GB/s or
 # the kernel and its launch plan (score_tc.cu, kvc_api.cu) are the captured
 # ones (the kernel's source and the plan_score function that sizes its work
 # items), else reported as null.
-SCORE_TRAFFIC = {"sha1": "88294ac7e5db5615cd6f7352e65a28bb57f551e1", "bytes_per_unit": (4661378048 + 27917312) / 288}
+SCORE_TRAFFIC = {"sha1": "841fba020628687e94b8620e0130905146bcd4ba", "bytes_per_unit": (4666309632 + 27208192) / 288}
 UNIT = "tokens/s (summed over layer x KV-head units)"
 L2_FLUSH_BYTES = 256 << 20
 
