@@ -523,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
 }
 
 // ----------------------------------------------------------------------------
-// bf16 pool with every element in split-half rotation and no reference
-// store (the common case): keys and values of the same rows move together.
+// Split-half rotation over every element and no reference store (the common
+// case; any pool, blockIdx.z): keys and values of the same rows move together.
 // A block takes batches of one unit's kept rows (kCopyBatch at a time, staged
 // as above).  Each lane copies its 16-byte pieces of a row -- key, value and,
 // for a key that changes position, the four rotary-table pieces it needs --
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 2) compact_copy_kernel(const Compact
   const int groups = (kThreads / 32) * rows_per_warp;   // lane groups of the block
   const int grp = warp * rows_per_warp + sub;
   const int per_step = groups * kCopyRows;
-  const int pool = KVC_POOL_BF16;
+  const int pool = a.pool_lo + static_cast<int>(blockIdx.z);
   const int u = blockIdx.y;
   const int U = a.U;
   const int cap = a.capacity;
@@ -652,16 +652,23 @@ __global__ void __launch_bounds__(kThreads, 2) compact_copy_kernel(const Compact
                          : "r"(piece(stage, n, 2 + c)));
         }
         // whole warps: the rotation exchanges halves between partner lanes
-        if (__any_sync(kFull, rot)) {
-          float x[8];
-          unpack8(w, x);
-          rerotate_lane(lpr, hl, rot, tab, x, w);
+        float x[8];
+        unpack8(w, x);
+        if (__any_sync(kFull, rot)) rerotate_lane(lpr, hl, rot, tab, x, w);
+        const int64_t i = b0 + q;
+        const int64_t row = static_cast<int64_t>(u) * cap + i;
+        if (pool == KVC_POOL_BF16) {
+          if (valid) {
+            st_global_hint(static_cast<__nv_bfloat16*>(a.pools.k_bf16) + row * d + hl * 8, w, stream);
+            st_global_hint(static_cast<__nv_bfloat16*>(a.pools.v_bf16) + row * d + hl * 8, wv, stream);
+          }
+        } else {                                  // whole warps (group maxima over lanes)
+          float xv[8];
+          unpack8(wv, xv);
+          store_quantised(a, pool, 0, lpr, hl, valid, row, x);
+          store_quantised(a, pool, 1, lpr, hl, valid, row, xv);
         }
         if (valid) {
-          const int64_t i = b0 + q;
-          const int64_t row = static_cast<int64_t>(u) * cap + i;
-          st_global_hint(static_cast<__nv_bfloat16*>(a.pools.k_bf16) + row * d + hl * 8, w, stream);
-          st_global_hint(static_cast<__nv_bfloat16*>(a.pools.v_bf16) + row * d + hl * 8, wv, stream);
           if (hl == 0) {
             a.pools.pos_out[slot0 + i] = s_p2[q];
             if (a.pools.orig_pos_out) a.pools.orig_pos_out[slot0 + i] = s_p[q];
@@ -681,14 +688,18 @@ cudaError_t launch_compact(const CompactArgs& a, cudaStream_t stream) {
   const int n_pools = a.pool_hi - a.pool_lo;
   if (a.capacity < 1 || n_pools <= 0) return cudaSuccess;
   const bool general = a.rope_layout != KVC_ROPE_SPLIT_HALF || a.rotary_dim != a.d;
-  if (a.ref.ref_pos == nullptr && !general && n_pools == 1 && a.pool_lo == KVC_POOL_BF16) {
-    // keys and values together, every batch of a unit in its own block
-    const int64_t bx = (a.capacity + kCopyBatch - 1) / kCopyBatch;
+  if (a.ref.ref_pos == nullptr && !general) {
+    // keys and values together; batch lanes of a (unit, pool) stream side by
+    // side, as many as the capacity needs but no more than keep the grid near
+    // 2,048 blocks (in byte mode the capacity is T and most of it unused)
+    const int64_t streams = static_cast<int64_t>(a.U) * n_pools;
+    const int64_t per_cap = (a.capacity + kCopyBatch - 1) / kCopyBatch;
+    const int64_t bx = std::max<int64_t>(1, std::min<int64_t>(per_cap, (2048 + streams - 1) / streams));
     const size_t smem = compact_copy_smem_bytes();
     cudaError_t err = cudaFuncSetAttribute(compact_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    compact_copy_kernel<<<dim3(static_cast<unsigned>(bx), a.U), kThreads, smem, stream>>>(a);
+    compact_copy_kernel<<<dim3(static_cast<unsigned>(bx), a.U, n_pools), kThreads, smem, stream>>>(a);
     return cudaGetLastError();
   }
   // batches of a stream side by side: as many as the capacity needs, but
