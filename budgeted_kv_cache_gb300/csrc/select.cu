@@ -1056,6 +1056,9 @@ __global__ void __launch_bounds__(kLongThreads) select_long_write(const __grid_c
       const int cls = long_class(a, i, s_q, f_q, key, err);
       long_decide(st, cls, key, fixed, tie);
     }
+    // a round with nothing to keep and no tie needs no ranks (the common case:
+    // a chunk keeps a few of its items)
+    if (!__syncthreads_or(fixed || tie)) continue;
     // rank of this tie among the chunk's ties (index order)
     const unsigned tm = __ballot_sync(kFull, tie);
     if (lane == 0) wsum[warp] = __popc(tm);
