@@ -1091,6 +1091,239 @@ __global__ void __launch_bounds__(kLongThreads) select_long_write(const __grid_c
   }
 }
 
+// ---- Four items per load.  The same passes for units whose item count is a
+// multiple of 4, with 16-byte aligned scores and 4-byte aligned flags: thread
+// t takes items i0 + 4 (q kLongThreads + t) + e (q < kLongIlp, e < 4), so in
+// index order a chunk is kLongIlp slabs of 1,024 items, thread by thread,
+// four items each.  A chunk that holds no sink or recent item, with no
+// flags, classifies every item as a candidate without the per-item tests.
+__device__ __forceinline__ void long_load4(const float* sc, const uint8_t* fl, int64_t i0, int64_t i1,
+                                           float4 (&s)[kLongIlp], uint32_t (&f)[kLongIlp]) {
+#pragma unroll
+  for (int q = 0; q < kLongIlp; ++q) {
+    const int64_t i = i0 + 4 * (q * kLongThreads + threadIdx.x);
+    s[q] = i < i1 ? __ldg(reinterpret_cast<const float4*>(sc + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    f[q] = (fl && i < i1) ? __ldg(reinterpret_cast<const uint32_t*>(fl + i)) : 0u;
+  }
+}
+
+__device__ __forceinline__ float quad_at(const float4& v, int e) {
+  return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ int long_class4(const SelectArgs& a, bool plain, int64_t i, float s, uint32_t f4, int e,
+                                           uint32_t& key, int& err) {
+  if (plain) {
+    key = order_key(s);
+    return 2;
+  }
+  return long_class(a, i, s, static_cast<uint8_t>(f4 >> (8 * e)), key, err);
+}
+
+__device__ __forceinline__ bool long_plain(const SelectArgs& a, const uint8_t* fl, int64_t i0, int64_t i1) {
+  return fl == nullptr && i0 >= a.sink_items && i1 <= a.n_items - a.recent_items;
+}
+
+__global__ void __launch_bounds__(kLongThreads) select_long_hist4(const __grid_constant__ SelectArgs a, int level) {
+  __shared__ uint32_t h[kLongBins];
+  __shared__ uint32_t s_forced, s_cand, s_err;
+  const int u = blockIdx.y;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  LongState* st = w.st + u;
+  if (level > 0 && st->phase != 0) return;                    // block-uniform
+  const uint32_t prefix = level > 0 ? st->prefix : 0u;
+  for (int i = threadIdx.x; i < kLongBins; i += kLongThreads) h[i] = 0;
+  if (threadIdx.x == 0) s_forced = s_cand = s_err = 0;
+  __syncthreads();
+  const int b = u / (a.L * a.Hkv);
+  const float* sc = a.scores + static_cast<int64_t>(u) * a.n_items;
+  const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * a.n_items : nullptr;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLongChunk;
+  const int64_t i1 = min(a.n_items, i0 + kLongChunk);
+  const bool plain = long_plain(a, fl, i0, i1);
+  uint32_t n_forced = 0, n_cand = 0;
+  int err = 0;
+  float4 sv[kLongIlp];
+  uint32_t fv[kLongIlp];
+  long_load4(sc, fl, i0, i1, sv, fv);
+#pragma unroll
+  for (int q = 0; q < kLongIlp; ++q) {
+    const int64_t ib = i0 + 4 * (q * kLongThreads + threadIdx.x);
+    if (ib >= i1) continue;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t key = 0, dg = 0;
+      const int cls = long_class4(a, plain, ib + e, quad_at(sv[q], e), fv[q], e, key, err);
+      n_forced += cls == 1;
+      n_cand += cls == 2;
+      if (cls == 2 && long_digit(key, level, prefix, dg)) atomicAdd(&h[dg], 1u);
+    }
+  }
+  if (level == 0) {
+    for (int o = 16; o > 0; o >>= 1) {
+      n_forced += __shfl_xor_sync(kFull, n_forced, o);
+      n_cand += __shfl_xor_sync(kFull, n_cand, o);
+      err |= __shfl_xor_sync(kFull, err, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      atomicAdd(&s_forced, n_forced);
+      atomicAdd(&s_cand, n_cand);
+      atomicOr(&s_err, static_cast<uint32_t>(err));
+    }
+  }
+  __syncthreads();
+  uint32_t* gh = w.hist + static_cast<int64_t>(u) * kLongBins;
+  for (int i = threadIdx.x; i < kLongBins; i += kLongThreads)
+    if (h[i]) atomicAdd(gh + i, h[i]);
+  if (level == 0 && threadIdx.x == 0) {
+    if (s_forced) atomicAdd(&st->n_forced, s_forced);
+    if (s_cand) atomicAdd(&st->n_cand, s_cand);
+    if (s_err) atomicOr(&st->err, s_err);
+  }
+}
+
+__global__ void __launch_bounds__(kLongThreads) select_long_count4(const __grid_constant__ SelectArgs a) {
+  __shared__ uint32_t s_f, s_t;
+  const int u = blockIdx.y;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  const LongState st = w.st[u];
+  if (st.phase == 3) return;
+  if (threadIdx.x == 0) s_f = s_t = 0;
+  __syncthreads();
+  const int b = u / (a.L * a.Hkv);
+  const float* sc = a.scores + static_cast<int64_t>(u) * a.n_items;
+  const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * a.n_items : nullptr;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLongChunk;
+  const int64_t i1 = min(a.n_items, i0 + kLongChunk);
+  const bool plain = long_plain(a, fl, i0, i1);
+  uint32_t nf = 0, nt = 0;
+  int err = 0;
+  float4 sv[kLongIlp];
+  uint32_t fv[kLongIlp];
+  long_load4(sc, fl, i0, i1, sv, fv);
+#pragma unroll
+  for (int q = 0; q < kLongIlp; ++q) {
+    const int64_t ib = i0 + 4 * (q * kLongThreads + threadIdx.x);
+    if (ib >= i1) continue;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t key = 0;
+      const int cls = long_class4(a, plain, ib + e, quad_at(sv[q], e), fv[q], e, key, err);
+      bool fixed, tie;
+      long_decide(st, cls, key, fixed, tie);
+      nf += fixed;
+      nt += tie;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    nf += __shfl_xor_sync(kFull, nf, o);
+    nt += __shfl_xor_sync(kFull, nt, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&s_f, nf);
+    atomicAdd(&s_t, nt);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    w.fixed[static_cast<int64_t>(u) * w.chunks + blockIdx.x] = s_f;
+    w.ties[static_cast<int64_t>(u) * w.chunks + blockIdx.x] = s_t;
+  }
+}
+
+// Exclusive scan over the kLongThreads threads of the block; `total` gets the sum.
+__device__ __forceinline__ uint32_t long_block_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan(v, lane);
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t base = 0;
+  total = 0;
+#pragma unroll
+  for (int k = 0; k < kLongThreads / 32; ++k) {
+    if (k < warp) base += wsum[k];
+    total += wsum[k];
+  }
+  __syncthreads();
+  return base + incl - v;
+}
+
+// Write the kept items of chunk blockIdx.x of unit blockIdx.y in index order,
+// one 1,024-item slab at a time (a slab with nothing to keep and no tie is
+// skipped after one block-wide vote).
+__global__ void __launch_bounds__(kLongThreads) select_long_write4(const __grid_constant__ SelectArgs a) {
+  __shared__ uint32_t wsum[kLongThreads / 32];
+  const int u = blockIdx.y;
+  const LongWs w = long_ws(a.long_ws, a.U, a.n_items);
+  const LongState st = w.st[u];
+  if (st.phase == 3) return;
+  const int b = u / (a.L * a.Hkv);
+  const float* sc = a.scores + static_cast<int64_t>(u) * a.n_items;
+  const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * a.n_items : nullptr;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLongChunk;
+  const int64_t i1 = min(a.n_items, i0 + kLongChunk);
+  const bool plain = long_plain(a, fl, i0, i1);
+  uint32_t out = w.fixed[static_cast<int64_t>(u) * w.chunks + blockIdx.x];
+  const uint32_t ties_kept = w.ties[static_cast<int64_t>(u) * w.chunks + blockIdx.x];
+  uint32_t tie_run = 0;
+  const int P = a.page_size;
+  int32_t* dst = a.kept_idx + (static_cast<int64_t>(KVC_POOL_BF16) * a.U + u) * a.capacity;
+  int err = 0;
+  float4 sv[kLongIlp];
+  uint32_t fv[kLongIlp];
+  long_load4(sc, fl, i0, i1, sv, fv);
+#pragma unroll 1
+  for (int q = 0; q < kLongIlp; ++q) {
+    const int64_t ib = i0 + 4 * (q * kLongThreads + threadIdx.x);
+    uint32_t fixed_bits = 0, tie_bits = 0;
+    if (ib < i1) {
+      float4 v = sv[0];
+      uint32_t f4 = fv[0];
+#pragma unroll
+      for (int k = 1; k < kLongIlp; ++k)
+        if (q == k) {
+          v = sv[k];
+          f4 = fv[k];
+        }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t key = 0;
+        const int cls = long_class4(a, plain, ib + e, quad_at(v, e), f4, e, key, err);
+        bool fixed, tie;
+        long_decide(st, cls, key, fixed, tie);
+        fixed_bits |= static_cast<uint32_t>(fixed) << e;
+        tie_bits |= static_cast<uint32_t>(tie) << e;
+      }
+    }
+    if (!__syncthreads_or(fixed_bits | tie_bits)) continue;
+    // ranks of the ties in index order, then which of them the chunk keeps
+    uint32_t tie_total;
+    const uint32_t tie_before = tie_run + long_block_scan(__popc(tie_bits), wsum, tie_total);
+    uint32_t keep_bits = fixed_bits;
+    uint32_t tr = tie_before;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if ((tie_bits >> e) & 1u) {
+        if (tr < ties_kept) keep_bits |= 1u << e;
+        ++tr;
+      }
+    uint32_t keep_total;
+    uint32_t pos = out + long_block_scan(__popc(keep_bits), wsum, keep_total);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if ((keep_bits >> e) & 1u) {
+        const int64_t i = ib + e;
+        if (P == 1) {
+          dst[pos] = static_cast<int32_t>(i);
+        } else {
+          for (int j = 0; j < P; ++j) dst[static_cast<int64_t>(pos) * P + j] = static_cast<int32_t>(i * P + j);
+        }
+        ++pos;
+      }
+    out += keep_total;
+    tie_run += tie_total;
+  }
+}
+
 }  // namespace
 
 size_t select_long_ws_bytes(int64_t U, int64_t n_items) {
@@ -1108,13 +1341,19 @@ cudaError_t launch_select_long(const SelectArgs& a, cudaStream_t stream) {
                                     stream);
   if (err != cudaSuccess) return err;
   const dim3 grid(static_cast<unsigned>(w.chunks), static_cast<unsigned>(a.U));
+  // four items per load where every unit's scores (and flags) stay aligned
+  const bool vec4 = a.n_items % 4 == 0 && reinterpret_cast<uintptr_t>(a.scores) % 16 == 0 &&
+                    (a.flags == nullptr || reinterpret_cast<uintptr_t>(a.flags) % 4 == 0);
   for (int level = 0; level < 3; ++level) {
-    select_long_hist<<<grid, kLongThreads, 0, stream>>>(a, level);
+    if (vec4) select_long_hist4<<<grid, kLongThreads, 0, stream>>>(a, level);
+    else select_long_hist<<<grid, kLongThreads, 0, stream>>>(a, level);
     select_long_pick<<<a.U, kLongThreads, 0, stream>>>(a, level);
   }
-  select_long_count<<<grid, kLongThreads, 0, stream>>>(a);
+  if (vec4) select_long_count4<<<grid, kLongThreads, 0, stream>>>(a);
+  else select_long_count<<<grid, kLongThreads, 0, stream>>>(a);
   select_long_offsets<<<a.U, 32, 0, stream>>>(a);
-  select_long_write<<<grid, kLongThreads, 0, stream>>>(a);
+  if (vec4) select_long_write4<<<grid, kLongThreads, 0, stream>>>(a);
+  else select_long_write<<<grid, kLongThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -60,10 +60,13 @@ def _compare(kept_a, cnt_a, st_a, kept_b, cnt_b, st_b):
 
 @pytest.mark.parametrize("kind", ["random", "few_values", "all_equal", "special"])
 @pytest.mark.parametrize("budget", [2048, 40000])
-def test_long_selection_token_mode_matches(kvc, kind, budget):
+@pytest.mark.parametrize("n", [70001, 70000], ids=["one_item_loads", "four_item_loads"])
+def test_long_selection_token_mode_matches(kvc, kind, budget, n):
+    """n = 70,001: items loaded one at a time (a unit's scores are not 16-byte
+    aligned); n = 70,000: four at a time.  Both with a ragged last chunk."""
     g = torch.Generator(device="cuda")
     g.manual_seed(11)
-    U, n = 6, 70001                                   # a ragged last chunk
+    U = 6
     shape = kvc.make_shape(1, 3, 8, 2, 128, n)
     pol = kvc.Policy(budget_tokens=budget, n_sink=4, n_recent=128, capacity=budget, renumber=False)
     need = kvc.kvc_select_workspace_bytes(shape, pol)
