@@ -485,7 +485,6 @@ constexpr int kFastMaxItems = kThreads * kFastSlabs;
 
 __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_constant__ SelectArgs a) {
   __shared__ uint32_t hist_w[32 * 256];     // per-warp histograms
-  __shared__ unsigned long long wtot[32];
   __shared__ uint32_t scan_w[32];
   __shared__ uint32_t s_cnt[kFastSlabs * 32];
   __shared__ uint32_t s_red[4];
@@ -514,11 +513,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
   uint32_t forced_bits = 0;
   uint32_t n_forced = 0, n_cand = 0, kmin = 0xffffffffu, kmax = 0u;
   int err = 0;
+  // a slab with no sink or recent item, and no flags, holds only candidates
+  const int plain_lo = fl == nullptr ? (a.sink_items + kThreads - 1) / kThreads : kFastSlabs;
+  const int plain_hi = fl == nullptr ? (n - a.recent_items) / kThreads : 0;   // slabs [plain_lo, plain_hi)
 #pragma unroll
   for (int q = 0; q < kFastSlabs; ++q) {
     const int i = q * kThreads + tid;
     key[q] = 0;
-    if (i < n) {
+    if (q >= plain_lo && q < plain_hi) {
+      key[q] = order_key(v[q]);
+      ++n_cand;
+      kmin = min(kmin, key[q]);
+      kmax = max(kmax, key[q]);
+    } else if (i < n) {
       const bool window = i < a.sink_items || i >= n - a.recent_items;
       const bool protect = f[q] & KVC_FLAG_PROTECT;
       const bool exclude = f[q] & KVC_FLAG_EXCLUDE;
@@ -590,19 +597,22 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
       const uint32_t nb = 1u << width;
       for (int i = lane; i < 256; i += 32) whist[i] = 0;
       __syncwarp();
+      // the bits above hi must equal the prefix: one masked 32-bit compare
+      const uint32_t hmask = hi >= 31 ? 0u : ~((2u << hi) - 1u);
+      const uint32_t pmask = hi >= 31 ? 0u : static_cast<uint32_t>(pfx << (hi + 1));
 #pragma unroll
       for (int q = 0; q < kFastSlabs; ++q)
-        if (key[q] != 0 && (static_cast<uint64_t>(key[q]) >> (hi + 1)) == pfx)
+        if (key[q] != 0 && (key[q] & hmask) == pmask)
           atomicAdd(&whist[(key[q] >> shift) & (nb - 1)], 1u);
       if (tid == 0) s_bin = -1;
       __syncthreads();
-      unsigned long long local = 0;
+      uint32_t local = 0;
       if (tid < static_cast<int>(nb)) {
         const int bn = static_cast<int>(nb) - 1 - tid;
         for (int w = 0; w < 32; ++w) local += hist_w[w * 256 + bn];
       }
-      unsigned long long total;
-      const unsigned long long run = block_excl_scan<unsigned long long>(local, wtot, total);
+      uint32_t total;
+      const uint32_t run = block_excl_scan<uint32_t>(local, scan_w, total);
       if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
         s_bin = static_cast<int>(nb) - 1 - tid;
         s_above = run;
