@@ -491,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
   __shared__ uint32_t s_kmin, s_kmax;
   __shared__ int s_bin;
   __shared__ unsigned long long s_above;
+  __shared__ uint32_t s_bincnt;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = blockIdx.x;
@@ -586,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
   // (8-bit digits over the bits where candidate keys differ; t counts the
   // candidates still to place below the prefix)
   uint32_t tau = 0xffffffffu, take_ties = 0;
+  uint32_t n_tau = n_cand;                          // candidates whose key equals tau
   if (k > 0) {
     uint32_t t = k - 1;
     uint32_t* whist = hist_w + warp * 256;
@@ -616,10 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
       if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
         s_bin = static_cast<int>(nb) - 1 - tid;
         s_above = run;
+        s_bincnt = local;
       }
       __syncthreads();
       const int bn = s_bin;                      // always found: t < candidates under pfx
       t -= static_cast<uint32_t>(s_above);
+      n_tau = s_bincnt;
       pfx = (pfx << width) | static_cast<uint32_t>(bn);
       __syncthreads();
     }
@@ -627,28 +631,35 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
     take_ties = t + 1;
   }
 
-  // ---------------- ranks of the ties (key == tau) in index order
-  uint32_t tie_bits = 0;
-#pragma unroll
-  for (int q = 0; q < kFastSlabs; ++q) {
-    const bool tie = k > 0 && key[q] != 0 && key[q] == tau;
-    const unsigned m = __ballot_sync(kFull, tie);
-    if (tie) tie_bits |= 1u << q;
-    if (lane == 0) s_cnt[q * 32 + warp] = __popc(m);
-  }
-  __syncthreads();
-  uint32_t tot;
-  const uint32_t tie_off = block_excl_scan<uint32_t>(s_cnt[tid], scan_w, tot);
-  __syncthreads();
-  s_cnt[tid] = tie_off;                           // exclusive offset of (slab, warp) = tid
-  __syncthreads();
   uint32_t keep_bits = forced_bits;
+  if (k > 0 && n_tau == take_ties) {
+    // every candidate equal to tau is taken: no ranks needed (the common case)
 #pragma unroll
-  for (int q = 0; q < kFastSlabs; ++q) {
-    const unsigned m = __ballot_sync(kFull, (tie_bits >> q) & 1u);
-    const uint32_t rank = s_cnt[q * 32 + warp] + __popc(m & lt_mask);
-    const bool keep = (k > 0 && key[q] != 0 && key[q] > tau) || (((tie_bits >> q) & 1u) && rank < take_ties);
-    if (keep) keep_bits |= 1u << q;
+    for (int q = 0; q < kFastSlabs; ++q)
+      if (key[q] != 0 && key[q] >= tau) keep_bits |= 1u << q;
+  } else if (k > 0) {
+    // ---------------- ranks of the ties (key == tau) in index order
+    uint32_t tie_bits = 0;
+#pragma unroll
+    for (int q = 0; q < kFastSlabs; ++q) {
+      const bool tie = key[q] != 0 && key[q] == tau;
+      const unsigned m = __ballot_sync(kFull, tie);
+      if (tie) tie_bits |= 1u << q;
+      if (lane == 0) s_cnt[q * 32 + warp] = __popc(m);
+    }
+    __syncthreads();
+    uint32_t tot;
+    const uint32_t tie_off = block_excl_scan<uint32_t>(s_cnt[tid], scan_w, tot);
+    __syncthreads();
+    s_cnt[tid] = tie_off;                         // exclusive offset of (slab, warp) = tid
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kFastSlabs; ++q) {
+      const unsigned m = __ballot_sync(kFull, (tie_bits >> q) & 1u);
+      const uint32_t rank = s_cnt[q * 32 + warp] + __popc(m & lt_mask);
+      const bool keep = (key[q] != 0 && key[q] > tau) || (((tie_bits >> q) & 1u) && rank < take_ties);
+      if (keep) keep_bits |= 1u << q;
+    }
   }
   __syncthreads();
   // ---------------- output positions in index order, then the write

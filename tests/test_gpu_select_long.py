@@ -113,3 +113,24 @@ def test_long_selection_page_mode_flags_and_over_budget(kvc):
     kept, status = o.select_tokens(sc, T, 2048, 4, 64, flags[0].cpu().numpy(), P)
     assert status == o.UNIT_OK
     assert np.array_equal(long_[0][2, 0, :int(long_[1][2, 0])].cpu().numpy(), np.sort(kept))
+
+
+@pytest.mark.parametrize("kind", ["random", "few_values", "all_equal", "special"])
+@pytest.mark.parametrize("n", [32768, 20001])
+def test_one_cta_selection_matches_oracle(kvc, kind, n):
+    """Units of at most 32,768 items (one CTA each): every unit's kept list and
+    status against the oracle, with heavy ties (several candidates at the
+    threshold key), all-equal scores and special values, full and ragged slabs."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(12)
+    U = 6
+    shape = kvc.make_shape(1, 3, 8, 2, 128, n)
+    budget = 2048
+    pol = kvc.Policy(budget_tokens=budget, n_sink=4, n_recent=128, capacity=budget, renumber=False)
+    scores = _scores(kind, U, n, g)
+    kept, cnt, st = _run(kvc, shape, pol, scores, None)
+    for u in range(U):
+        sc = scores[u].cpu().numpy()
+        ref, status = o.select_tokens(sc, n, budget, 4, 128, None, 1)
+        assert status == int(st[u])
+        assert np.array_equal(kept[2, u, :int(cnt[2, u])].cpu().numpy(), np.sort(ref)), f"unit {u}"
