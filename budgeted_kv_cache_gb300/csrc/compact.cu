@@ -538,6 +538,12 @@ constexpr int kCopyRows = 1;          // rows per lane group and step
 constexpr int kCopyBatch = 256;       // rows staged per block and batch
 constexpr int kPieces = 6;            // key, value, cos(p), sin(p), cos(p'), sin(p')
 
+// The same through L1 (rotary-table pieces: many rows of a block and of the
+// blocks beside it on the SM share table rows).
+__device__ __forceinline__ void cp_async16_l1(uint32_t saddr, const void* src, uint64_t policy) {
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(saddr), "l"(src), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* src, uint64_t policy) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(saddr), "l"(src), "l"(policy)
                : "memory");
@@ -615,10 +621,10 @@ __global__ void __launch_bounds__(kThreads, 2) compact_copy_kernel(const Compact
           cp_async16(piece(stage, n, 1), reinterpret_cast<const uint4*>(a.v + r * d) + hl, stream);
           if ((f & kRotate) && lr.active) {
             const int64_t p = s_p[q], p2 = s_p2[q];
-            cp_async16(piece(stage, n, 2), a.cos + p * half + j0, keep);
-            cp_async16(piece(stage, n, 3), a.sin + p * half + j0, keep);
-            cp_async16(piece(stage, n, 4), a.cos + p2 * half + j0, keep);
-            cp_async16(piece(stage, n, 5), a.sin + p2 * half + j0, keep);
+            cp_async16_l1(piece(stage, n, 2), a.cos + p * half + j0, keep);
+            cp_async16_l1(piece(stage, n, 3), a.sin + p * half + j0, keep);
+            cp_async16_l1(piece(stage, n, 4), a.cos + p2 * half + j0, keep);
+            cp_async16_l1(piece(stage, n, 5), a.sin + p2 * half + j0, keep);
           }
         }
       }
