@@ -48,20 +48,21 @@ __device__ __forceinline__ V warp_incl_scan(V x, int lane) {
   return x;
 }
 
-// Exclusive scan over the 1024 threads of the block; `total` gets the sum.
-template <typename V>
+// Exclusive scan over the NW warps of the block (wtot: 32 entries); `total`
+// gets the sum.
+template <typename V, int NW = 32>
 __device__ __forceinline__ V block_excl_scan(V v, V* wtot, V& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const V incl = warp_incl_scan(v, lane);
   if (lane == 31) wtot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const V w = warp_incl_scan(wtot[lane], lane);
+    const V w = warp_incl_scan(lane < NW ? wtot[lane] : V(0), lane);
     wtot[lane] = w;
   }
   __syncthreads();
   const V base = warp ? wtot[warp - 1] : V(0);
-  total = wtot[31];
+  total = wtot[NW - 1];
   __syncthreads();
   return base + incl - v;
 }
@@ -116,8 +117,12 @@ __device__ __forceinline__ uint32_t item_weight(const Ctx& c, const Item& it) {
   return c.a->byte_mode ? c.cost[KVC_ACT_BF16] - c.cost[it.base] : 1u;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectArgs a) {
-  __shared__ uint32_t hist_w[32 * 256];     // per-warp histograms
+// NW warps per CTA: 32 for long units, 8 for units of at most 16,384 items
+// (byte mode at T = 8,192: four times as many CTAs per SM).
+template <int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 32 ? 1 : 1024 / (NW * 32)) select_kernel(const __grid_constant__ SelectArgs a) {
+  constexpr int kT = NW * 32;               // threads of the CTA
+  __shared__ uint32_t hist_w[NW * 256];     // per-warp histograms
   __shared__ unsigned long long wtot[32];
   __shared__ unsigned long long red[4];
   __shared__ int s_bin;
@@ -171,18 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   unsigned long long n_forced = 0, n_cand = 0, floor_bytes = 0;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
   int err = 0;
-  for (int64_t i0 = tid; i0 < c.n; i0 += 4 * kThreads) {
+  for (int64_t i0 = tid; i0 < c.n; i0 += 4 * kT) {
     Item it[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int64_t i = i0 + k * kThreads;
+      const int64_t i = i0 + k * kT;
       it[k].key = 0;
       it[k].base = KVC_ACT_RELEASE;
       if (i < c.n) it[k] = eval_item(c, i, err);
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int64_t i = i0 + k * kThreads;
+      const int64_t i = i0 + k * kT;
       if (i >= c.n) continue;
       if (a.cache_items) {
         ckey[i] = it[k].key;
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   uint32_t tau = 0;
   if (!sel_none && n_cand > 0) {
     const int warp = tid >> 5;
-    const int64_t per_w = (c.n + 32 * 32 - 1) / (32 * 32) * 32;
+    const int64_t per_w = (c.n + NW * 32 - 1) / (NW * 32) * 32;
     const int64_t w_lo = min(c.n, static_cast<int64_t>(warp) * per_w);
     const int64_t w_hi = min(c.n, w_lo + per_w);
     uint32_t* whist = hist_w + warp * 256;
@@ -288,10 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
       unsigned long long local = 0;
       if (tid < static_cast<int>(nb)) {
         const int bn = static_cast<int>(nb) - 1 - tid;
-        for (int w = 0; w < 32; ++w) local += hist_w[w * 256 + bn];
+        for (int w = 0; w < NW; ++w) local += hist_w[w * 256 + bn];
       }
       unsigned long long total;
-      const unsigned long long run = block_excl_scan<unsigned long long>(local, wtot, total);
+      const unsigned long long run = block_excl_scan<unsigned long long, NW>(local, wtot, total);
       if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
         s_bin = static_cast<int>(nb) - 1 - tid;
         s_above = run;
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   __shared__ uint32_t s_pool[KVC_N_POOLS][32];
   const int warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int64_t per_w = (c.n + 32 * 32 - 1) / (32 * 32) * 32;
+  const int64_t per_w = (c.n + NW * 32 - 1) / (NW * 32) * 32;
   const int64_t w_lo = min(c.n, static_cast<int64_t>(warp) * per_w);
   const int64_t w_hi = min(c.n, w_lo + per_w);
   const unsigned long long tie_slack = a.byte_mode ? 0ull : 1ull;
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   if (lane == 0) s_tie[warp] = a.byte_mode ? tie_w : tie_n;
   __syncthreads();
   if (warp == 0) {
-    const unsigned long long v = s_tie[lane];
+    const unsigned long long v = lane < NW ? s_tie[lane] : 0ull;
     s_tie[lane] = warp_incl_scan(v, lane) - v;     // exclusive offsets
   }
   __syncthreads();
@@ -429,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_consta
   if (warp == 0) {
 #pragma unroll
     for (int q = 0; q < KVC_N_POOLS; ++q) {
-      const uint32_t v = s_pool[q][lane];
+      const uint32_t v = lane < NW ? s_pool[q][lane] : 0u;
       s_pool[q][lane] = warp_incl_scan(v, lane);        // inclusive: entry 31 is the total
     }
   }
@@ -700,16 +705,18 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
 }  // namespace
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes) {
-  if (smem_bytes > 0) {
-    cudaError_t err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem_bytes));
-    if (err != cudaSuccess) return err;
-  }
   if (!a.byte_mode && a.n_items <= kFastMaxItems) {
     select_fast_kernel<<<a.U, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
   }
-  select_kernel<<<a.U, kThreads, smem_bytes, stream>>>(a);
+  const bool small = a.n_items <= 16384;
+  void (*kern)(const SelectArgs) = small ? select_kernel<8> : select_kernel<32>;
+  if (smem_bytes > 0) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem_bytes));
+    if (err != cudaSuccess) return err;
+  }
+  kern<<<a.U, small ? 256 : kThreads, smem_bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
