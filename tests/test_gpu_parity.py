@@ -123,7 +123,9 @@ def small_workloads():
                        budget_bytes=(2000 * 256) // 3)
     c2w32 = c2.replace(name="qwen_small_w32", window=32, n_tokens=3001, renumber=False,
                        bonus_spans=0)
-    return [c1, c1r, c2, c2w32, c3, c3row, c4]
+    # byte mode with renumbering: kept keys re-rotated, then quantised to int8 / int4
+    c3ren = c3.replace(name="pask_small_renumber", renumber=True)
+    return [c1, c1r, c2, c2w32, c3, c3row, c3ren, c4]
 
 
 @pytest.mark.parametrize("w", small_workloads(), ids=lambda w: w.name)
