@@ -810,6 +810,12 @@ def run_gpu(args, w, world, rank, local):
                           "t_exp_ms": 1e3 * wr.n_units * wr.rows_per_unit * wr.n_tokens
                                       / (30.0 * torch.cuda.get_device_properties(dev).multi_processor_count
                                          * ((clocks or {}).get("sm_mhz") or 2070.0) * 1e6)},
+        # every stage on its own algorithmic bytes (HBM-bound stages)
+        "stage_rooflines": {
+            k: {"algorithmic_bytes": ab[k], "gbs": ab[k] / (t * 1e-3) / 1e9,
+                "frac": ab[k] / (t * 1e-3) / 1e9 / hbm}
+            for k, t in (("score", score_ms), ("select", statistics.mean(t_select)),
+                         ("compact", statistics.mean(t_compact)))},
         "graph_ms_per_step": graph_ms,
         "configs": configs,
         "cpu_baseline": cpu, "e2e": e2e,
