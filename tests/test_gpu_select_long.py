@@ -134,3 +134,25 @@ def test_one_cta_selection_matches_oracle(kvc, kind, n):
         ref, status = o.select_tokens(sc, n, budget, 4, 128, None, 1)
         assert status == int(st[u])
         assert np.array_equal(kept[2, u, :int(cnt[2, u])].cpu().numpy(), np.sort(ref)), f"unit {u}"
+
+
+@pytest.mark.parametrize("kind", ["random", "few_values", "all_equal", "special"])
+@pytest.mark.parametrize("n", [32768, 20001, 9000])
+def test_many_units_selection_matches_oracle(kvc, kind, n):
+    """More units than SMs (304, two waves of CTAs): every unit's kept list and
+    status against the oracle, with heavy ties, all-equal scores and special
+    values, full, ragged and short units."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(13)
+    shape = kvc.make_shape(1, 38, 32, 8, 128, n)
+    U = 304
+    budget = 2048
+    pol = kvc.Policy(budget_tokens=budget, n_sink=4, n_recent=128, capacity=budget, renumber=False)
+    scores = _scores(kind, U, n, g)
+    kept, cnt, st = _run(kvc, shape, pol, scores, None)
+    sc_all = scores.cpu().numpy()
+    cnt_h, kept_h, st_h = cnt.cpu().numpy(), kept.cpu().numpy(), st.cpu().numpy()
+    for u in range(U):
+        ref, status = o.select_tokens(sc_all[u], n, budget, 4, 128, None, 1)
+        assert status == int(st_h[u])
+        assert np.array_equal(kept_h[2, u, :int(cnt_h[2, u])], np.sort(ref)), f"unit {u}"
