@@ -478,25 +478,33 @@ __global__ void __launch_bounds__(NW * 32, NW == 32 ? 1 : 1024 / (NW * 32)) sele
 
 // ----------------------------------------------------------------------------
 // Token / page mode with at most 32,768 items per unit.  Item q * 1024 + t
-// (q < 32) belongs to thread t, so every load is coalesced, all 32 of a
-// thread's scores and flags are requested before any is used, and the keys
-// stay in registers through the radix passes.  In index order the items of
-// slab q come thread by thread, so the write-out needs one ballot per slab
-// and one block scan over the 1,024 (slab, warp) counts.  Same rule and
-// same results as select_kernel (forced items, then the top k candidates by
-// (score descending, index ascending)).
+// (q < 32) belongs to thread t, and the keys stay in registers through the
+// radix passes.  With kBulk (the unit's scores 16-byte aligned and a
+// multiple of 16 bytes long) the scores come into shared memory through
+// bulk copies issued by one warp, which bring the unit's 128 KB in several
+// times faster than 32 rounds of 4-byte loads by every thread; otherwise
+// every thread requests its 32 scores before it uses any.  In index order
+// the items of slab q come thread by thread, so the write-out needs one
+// ballot per slab and one block scan over the 1,024 (slab, warp) counts.
+// Same rule and same results as select_kernel (forced items, then the top k
+// candidates by (score descending, index ascending)).
 constexpr int kFastSlabs = 32;
 constexpr int kFastMaxItems = kThreads * kFastSlabs;
+constexpr uint32_t kFastCopyChunk = 16384;        // bytes per bulk copy (one per lane of warp 0)
 
+template <bool kBulk>
 __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_constant__ SelectArgs a) {
+  extern __shared__ __align__(16) float s_sc[];   // kBulk: the unit's scores
   __shared__ uint32_t hist_w[32 * 256];     // per-warp histograms
   __shared__ uint32_t scan_w[32];
   __shared__ uint32_t s_cnt[kFastSlabs * 32];
   __shared__ uint32_t s_red[4];
   __shared__ uint32_t s_kmin, s_kmax;
+  __shared__ uint32_t s_w8[8];              // bin-scan totals of warps 0-7
   __shared__ int s_bin;
-  __shared__ unsigned long long s_above;
-  __shared__ uint32_t s_bincnt;
+  __shared__ uint32_t s_above, s_bincnt;
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = blockIdx.x;
@@ -505,16 +513,60 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
   const float* sc = a.scores + static_cast<int64_t>(u) * n;
   const uint8_t* fl = a.flags ? a.flags + static_cast<int64_t>(b) * n : nullptr;
   const unsigned lt_mask = (1u << lane) - 1u;
+  int32_t* cnt = a.kept_count;
 
   // ---------------- classify
   float v[kFastSlabs];
   uint8_t f[kFastSlabs];
+  if constexpr (kBulk) {
+    const uint32_t bar = smem_u32(&s_bar);
+    const uint32_t bytes = static_cast<uint32_t>(n) * 4u;
+    if (warp == 0) {
+      if (lane == 0) {
+        s_abort = 0;
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        mbar_arrive_expect_tx(bar, bytes);
+      }
+      __syncwarp();
+      const uint32_t off = static_cast<uint32_t>(lane) * kFastCopyChunk;
+      if (off < bytes)
+        bulk_copy_g2s(smem_u32(s_sc) + off, reinterpret_cast<const char*>(sc) + off,
+                      min(kFastCopyChunk, bytes - off), bar);
+    }
 #pragma unroll
-  for (int q = 0; q < kFastSlabs; ++q) {
-    const int i = q * kThreads + tid;
-    v[q] = i < n ? __ldg(sc + i) : 0.f;
-    f[q] = (fl != nullptr && i < n) ? __ldg(fl + i) : 0;
+    for (int q = 0; q < kFastSlabs; ++q) {
+      const int i = q * kThreads + tid;
+      f[q] = (fl != nullptr && i < n) ? __ldg(fl + i) : 0;
+    }
+    __syncthreads();                              // the barrier is initialised
+    const bool landed = mbar_wait(bar, 0, &s_abort);
+    if (__syncthreads_or(!landed)) {
+      // the copy did not land within the wait bound: wait for it (bounded)
+      // before the block leaves, and report the unit
+      if (tid == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+        a.unit_status[u] = KVC_UNIT_TIMEOUT;
+        if (a.floor_excess) a.floor_excess[u] = 0;
+      }
+      if (tid < KVC_N_POOLS) cnt[tid * a.U + u] = 0;
+      return;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < kFastSlabs; ++q) {
+      const int i = q * kThreads + tid;
+      v[q] = i < n ? __ldg(sc + i) : 0.f;
+      f[q] = (fl != nullptr && i < n) ? __ldg(fl + i) : 0;
+    }
   }
+  // item i < n of slab q (read from shared memory as it is classified)
+  auto score = [&](int q, int i) -> float {
+    if constexpr (kBulk) return s_sc[i];
+    else return v[q];
+  };
   uint32_t key[kFastSlabs];
   uint32_t forced_bits = 0;
   uint32_t n_forced = 0, n_cand = 0, kmin = 0xffffffffu, kmax = 0u;
@@ -527,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
     const int i = q * kThreads + tid;
     key[q] = 0;
     if (q >= plain_lo && q < plain_hi) {
-      key[q] = order_key(v[q]);
+      key[q] = order_key(score(q, i));
       ++n_cand;
       kmin = min(kmin, key[q]);
       kmax = max(kmax, key[q]);
@@ -542,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
         forced_bits |= 1u << q;
         ++n_forced;
       } else if (!excluded) {
-        key[q] = order_key(v[q]);
+        key[q] = order_key(score(q, i));
         ++n_cand;
         kmin = min(kmin, key[q]);
         kmax = max(kmax, key[q]);
@@ -577,7 +629,6 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
   kmin = s_kmin;
   kmax = s_kmax;
 
-  int32_t* cnt = a.kept_count;
   if (err || n_forced > static_cast<uint32_t>(a.budget_items)) {
     if (tid < KVC_N_POOLS) cnt[tid * a.U + u] = 0;
     if (tid == 0) {
@@ -592,16 +643,20 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
   // (8-bit digits over the bits where candidate keys differ; t counts the
   // candidates still to place below the prefix)
   uint32_t tau = 0xffffffffu, take_ties = 0;
-  uint32_t n_tau = n_cand;                          // candidates whose key equals tau
+  uint32_t n_tau = n_cand;                          // candidates at the threshold (key tau, or
+                                                    // in tau's bin after an early exit)
   if (k > 0) {
     uint32_t t = k - 1;
     uint32_t* whist = hist_w + warp * 256;
     const int top = (kmin == kmax) ? -1 : 31 - __clz(kmin ^ kmax);
     uint64_t pfx = static_cast<uint64_t>(kmax) >> (top + 1);
+    int low = 0;                                    // bits below the prefix still open
     for (int hi = top; hi >= 0; hi -= 8) {
       const int shift = max(0, hi - 7);
       const int width = hi - shift + 1;
       const uint32_t nb = 1u << width;
+      // (every read of this warp's histogram and of the level's results by
+      // the level before came ahead of that level's second barrier)
       for (int i = lane; i < 256; i += 32) whist[i] = 0;
       __syncwarp();
       // the bits above hi must equal the prefix: one masked 32-bit compare
@@ -611,28 +666,37 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
       for (int q = 0; q < kFastSlabs; ++q)
         if (key[q] != 0 && (key[q] & hmask) == pmask)
           atomicAdd(&whist[(key[q] >> shift) & (nb - 1)], 1u);
-      if (tid == 0) s_bin = -1;
       __syncthreads();
-      uint32_t local = 0;
-      if (tid < static_cast<int>(nb)) {
-        const int bn = static_cast<int>(nb) - 1 - tid;
-        for (int w = 0; w < 32; ++w) local += hist_w[w * 256 + bn];
-      }
-      uint32_t total;
-      const uint32_t run = block_excl_scan<uint32_t>(local, scan_w, total);
-      if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
-        s_bin = static_cast<int>(nb) - 1 - tid;
-        s_above = run;
-        s_bincnt = local;
+      // the scan over the (at most 256) bins, highest first: warps 0-7 only
+      if (tid < 256) {
+        uint32_t local = 0;
+        if (tid < static_cast<int>(nb)) {
+          const int bn = static_cast<int>(nb) - 1 - tid;
+#pragma unroll 8
+          for (int w = 0; w < 32; ++w) local += hist_w[w * 256 + bn];
+        }
+        const uint32_t incl = warp_incl_scan(local, lane);
+        if (lane == 31) s_w8[warp] = incl;
+        named_bar_sync(1, 256);
+        uint32_t run = incl - local;
+        for (int w = 0; w < warp; ++w) run += s_w8[w];
+        if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
+          s_bin = static_cast<int>(nb) - 1 - tid;
+          s_above = run;
+          s_bincnt = local;
+        }
       }
       __syncthreads();
       const int bn = s_bin;                      // always found: t < candidates under pfx
-      t -= static_cast<uint32_t>(s_above);
+      t -= s_above;
       n_tau = s_bincnt;
       pfx = (pfx << width) | static_cast<uint32_t>(bn);
-      __syncthreads();
+      low = shift;
+      // every candidate of the bin is taken: its lower edge is the threshold
+      // and no candidate sits below it in the bin (uniform: shared values)
+      if (t + 1 == n_tau) break;
     }
-    tau = static_cast<uint32_t>(pfx);
+    tau = static_cast<uint32_t>(pfx << low);
     take_ties = t + 1;
   }
 
@@ -706,7 +770,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t stream, size_t smem_bytes) {
   if (!a.byte_mode && a.n_items <= kFastMaxItems) {
-    select_fast_kernel<<<a.U, kThreads, 0, stream>>>(a);
+    // bulk copies need 16-byte aligned rows of whole 16-byte pieces
+    const bool bulk = a.n_items > 0 && a.n_items % 4 == 0 && reinterpret_cast<uintptr_t>(a.scores) % 16 == 0;
+    if (bulk) {
+      const int smem = static_cast<int>(a.n_items * sizeof(float));
+      cudaError_t err = cudaFuncSetAttribute(select_fast_kernel<true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (err != cudaSuccess) return err;
+      select_fast_kernel<true><<<a.U, kThreads, smem, stream>>>(a);
+    } else {
+      select_fast_kernel<false><<<a.U, kThreads, 0, stream>>>(a);
+    }
     return cudaGetLastError();
   }
   const bool small = a.n_items <= 16384;

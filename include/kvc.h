@@ -226,7 +226,9 @@ typedef struct {
  * kept_idx     int32 [KVC_N_POOLS][U][capacity]: kept token indices of each
  *              pool, ascending; entries past kept_count are not written.
  * kept_count   int32 [KVC_N_POOLS][U].
- * unit_status  int32 [U], always written (KVC_UNIT_OK or an error code).
+ * unit_status  int32 [U], always written (KVC_UNIT_OK or an error code;
+ *              KVC_UNIT_TIMEOUT, with nothing kept, if a unit's scores did
+ *              not reach shared memory within the bounded device wait).
  * floor_excess optional int64 [U] (byte mode; 0 otherwise).
  * workspace    optional: in token and page mode with more than 32,768 items
  *              per unit, a workspace of kvc_select_workspace_bytes (256-byte

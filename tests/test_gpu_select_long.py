@@ -116,11 +116,13 @@ def test_long_selection_page_mode_flags_and_over_budget(kvc):
 
 
 @pytest.mark.parametrize("kind", ["random", "few_values", "all_equal", "special"])
-@pytest.mark.parametrize("n", [32768, 20001])
+@pytest.mark.parametrize("n", [32768, 20001, 20000])
 def test_one_cta_selection_matches_oracle(kvc, kind, n):
     """Units of at most 32,768 items (one CTA each): every unit's kept list and
     status against the oracle, with heavy ties (several candidates at the
-    threshold key), all-equal scores and special values, full and ragged slabs."""
+    threshold key), all-equal scores and special values, full and ragged slabs;
+    20,000 items take the bulk-copy load with a short last copy, 20,001 the
+    per-thread loads."""
     g = torch.Generator(device="cuda")
     g.manual_seed(12)
     U = 6
