@@ -529,11 +529,14 @@ __global__ void __launch_bounds__(kThreads, 4) compact_kernel(const CompactArgs 
 // as above).  Each lane copies its 16-byte pieces of a row -- key, value and,
 // for a key that changes position, the four rotary-table pieces it needs --
 // into shared memory with asynchronous copies, kCopyStages - 1 steps ahead
-// of the step it is working on; no registers are held by the copies in flight,
-// so a block keeps several rows per lane group in flight.  A lane reads back
-// only the pieces it copied itself, so no block-wide barrier separates the
-// copy and the use.
-constexpr int kCopyStages = 4;
+// of the step it is working on; no registers are held by the copies in flight.
+// A lane reads back only the pieces it copied itself, so no block-wide barrier
+// separates the copy and the use.  Two stages and three blocks per SM: the
+// 48 KB of stages per block leave most of the SM's on-chip memory to L1,
+// where table rows are shared between rows and blocks, and 24 warps per SM
+// hide the re-rotation arithmetic (four stages with two blocks, or two stages
+// with two or four blocks, are 6-19% slower).
+constexpr int kCopyStages = 2;
 constexpr int kCopyRows = 1;          // rows per lane group and step
 constexpr int kCopyBatch = 256;       // rows staged per block and batch
 constexpr int kPieces = 6;            // key, value, cos(p), sin(p), cos(p'), sin(p')
@@ -561,7 +564,7 @@ size_t compact_copy_smem_bytes() {
   return static_cast<size_t>(kCopyStages) * kCopyRows * kPieces * kThreads * 16;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) compact_copy_kernel(const CompactArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) compact_copy_kernel(const CompactArgs a) {
   extern __shared__ uint4 s_pieces[];   // [stage][row n][piece][thread]
   __shared__ int32_t s_t[kCopyBatch], s_p[kCopyBatch], s_p2[kCopyBatch];
   __shared__ uint8_t s_f[kCopyBatch];

@@ -672,14 +672,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
         uint32_t local = 0;
         if (tid < static_cast<int>(nb)) {
           const int bn = static_cast<int>(nb) - 1 - tid;
-#pragma unroll 8
+#pragma unroll
           for (int w = 0; w < 32; ++w) local += hist_w[w * 256 + bn];
         }
         const uint32_t incl = warp_incl_scan(local, lane);
         if (lane == 31) s_w8[warp] = incl;
         named_bar_sync(1, 256);
-        uint32_t run = incl - local;
-        for (int w = 0; w < warp; ++w) run += s_w8[w];
+        // candidates in the bins of the warps before this one (lanes 0-7 add
+        // up the totals of warps below this one)
+        uint32_t wl = lane < warp ? s_w8[lane & 7] : 0u;
+        wl += __shfl_xor_sync(kFull, wl, 1);
+        wl += __shfl_xor_sync(kFull, wl, 2);
+        wl += __shfl_xor_sync(kFull, wl, 4);
+        const uint32_t run = incl - local + __shfl_sync(kFull, wl, 0);
         if (tid < static_cast<int>(nb) && run <= t && t < run + local) {
           s_bin = static_cast<int>(nb) - 1 - tid;
           s_above = run;
