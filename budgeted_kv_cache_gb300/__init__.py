@@ -79,7 +79,8 @@ class kvc_effect_record(ctypes.Structure):
 class kvc_overrides(ctypes.Structure):
     """Launch-plan overrides of kvc_set_overrides (tuning and failure tests)."""
     _fields_ = [(n, ctypes.c_int32) for n in ("score_chunk_tiles", "decode_splits",
-                                              "effect_chunk_tiles", "score_stall_unit")]
+                                              "effect_chunk_tiles", "score_stall_unit",
+                                              "select_stall_unit")]
 
 
 class kvc_commit_thresholds(ctypes.Structure):
@@ -234,12 +235,14 @@ class Pools:
 # ----------------------------------------------------------------------------- entry points
 
 def kvc_set_overrides(score_chunk_tiles: int = 0, decode_splits: int = 0,
-                      effect_chunk_tiles: int = 0, score_stall_unit: int = -1, reset: bool = False):
+                      effect_chunk_tiles: int = 0, score_stall_unit: int = -1,
+                      select_stall_unit: int = -1, reset: bool = False):
     """Process-wide launch-plan overrides (tuning sweeps, failure tests); reset=True restores defaults."""
     if reset:
         _check("kvc_set_overrides", library().kvc_set_overrides(None))
         return
-    o = kvc_overrides(score_chunk_tiles, decode_splits, effect_chunk_tiles, score_stall_unit)
+    o = kvc_overrides(score_chunk_tiles, decode_splits, effect_chunk_tiles, score_stall_unit,
+                      select_stall_unit)
     _check("kvc_set_overrides", library().kvc_set_overrides(ctypes.byref(o)))
 
 

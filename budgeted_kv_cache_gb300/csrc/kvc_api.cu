@@ -20,6 +20,7 @@ std::atomic<int32_t> g_score_chunk_tiles{0};
 std::atomic<int32_t> g_decode_splits{0};
 std::atomic<int32_t> g_effect_chunk_tiles{0};
 std::atomic<int32_t> g_score_stall_unit{-1};
+std::atomic<int32_t> g_select_stall_unit{-1};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -377,12 +378,13 @@ extern "C" {
 kvc_status kvc_set_overrides(const kvc_overrides* o) {
   if (o && (o->score_chunk_tiles < 0 || o->score_chunk_tiles > (1 << 20) || o->decode_splits < 0 ||
             o->decode_splits > 32 || o->effect_chunk_tiles < 0 || o->effect_chunk_tiles > (1 << 20) ||
-            o->score_stall_unit < -1))
+            o->score_stall_unit < -1 || o->select_stall_unit < -1))
     return KVC_ERR_INVALID_ARG;
   g_score_chunk_tiles.store(o ? o->score_chunk_tiles : 0);
   g_decode_splits.store(o ? o->decode_splits : 0);
   g_effect_chunk_tiles.store(o ? o->effect_chunk_tiles : 0);
   g_score_stall_unit.store(o ? o->score_stall_unit : -1);
+  g_select_stall_unit.store(o ? o->select_stall_unit : -1);
   return KVC_OK;
 }
 
@@ -584,6 +586,7 @@ kvc_status kvc_select(const kvc_shape* shape, const kvc_policy* policy, const fl
   a.kept_count = kept_count;
   a.unit_status = unit_status;
   a.floor_excess = floor_excess;
+  a.stall_unit = g_select_stall_unit.load(std::memory_order_relaxed);   // failure test hook (-1: none)
   // token / page mode with long units: the multi-CTA selection when the
   // caller gave its workspace (else the one-CTA-per-unit kernel, same result)
   const size_t long_bytes = kvc_select_workspace_bytes(shape, policy);

@@ -69,6 +69,7 @@ struct SelectArgs {
   int64_t* floor_excess;
   int32_t cache_items;         // 1: item keys staged in shared memory
   void* long_ws;               // multi-CTA selection of long units (token / page mode), or null
+  int32_t stall_unit;          // test hook (-1 = none): this unit's wait for its scores never completes
 };
 
 // Workspace of the multi-CTA selection of long units (token / page mode).

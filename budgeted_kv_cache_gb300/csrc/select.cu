@@ -526,7 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
         s_abort = 0;
         mbar_init(bar, 1);
         fence_barrier_init();
-        mbar_arrive_expect_tx(bar, bytes);
+        // (a.stall_unit: a test waits for 16 bytes more than the copy brings)
+        mbar_arrive_expect_tx(bar, bytes + (u == a.stall_unit ? 16u : 0u));
       }
       __syncwarp();
       const uint32_t off = static_cast<uint32_t>(lane) * kFastCopyChunk;

@@ -608,6 +608,12 @@ kvc_status kvc_commit_flags(int32_t batch, int64_t n_tokens, int32_t n_pages,
  *                       of this unit never completes, so after the bounded
  *                       wait (2 s) that unit and every unit its CTA leaves
  *                       unscored report KVC_UNIT_TIMEOUT.
+ *   select_stall_unit   -1 = off.  Test hook: in kvc_select (token and page
+ *                       mode, units of at most 32,768 items whose scores
+ *                       are copied to shared memory in bulk) this unit waits
+ *                       for 16 bytes more than its copy brings, so after
+ *                       the bounded wait (2 s, then 2 s more for the copy)
+ *                       it reports KVC_UNIT_TIMEOUT and keeps nothing.
  * NULL restores every default.  Values out of range return
  * KVC_ERR_INVALID_ARG and change nothing.  A call affects calls issued
  * after it from any host thread; it does not synchronise with them.
@@ -617,6 +623,7 @@ typedef struct {
   int32_t decode_splits;
   int32_t effect_chunk_tiles;
   int32_t score_stall_unit;
+  int32_t select_stall_unit;
 } kvc_overrides;
 kvc_status kvc_set_overrides(const kvc_overrides* overrides);
 

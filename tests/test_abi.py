@@ -84,6 +84,20 @@ def test_argument_errors_return_before_any_launch(lib):
                                     None, None, None, 0, None) == 1
 
 
+def test_overrides_check_their_ranges(lib):
+    """kvc_set_overrides is host-only: out-of-range fields are refused and change nothing."""
+    import budgeted_kv_cache_gb300 as kvc
+    kvc.library()
+    bad = [kvc.kvc_overrides(-1, 0, 0, -1, -1), kvc.kvc_overrides(0, 33, 0, -1, -1),
+           kvc.kvc_overrides(0, 0, -1, -1, -1), kvc.kvc_overrides(0, 0, 0, -2, -1),
+           kvc.kvc_overrides(0, 0, 0, -1, -2)]
+    for o in bad:
+        assert kvc.library().kvc_set_overrides(ctypes.byref(o)) == 1
+    ok = kvc.kvc_overrides(0, 8, 0, -1, 3)
+    assert kvc.library().kvc_set_overrides(ctypes.byref(ok)) == 0
+    assert kvc.library().kvc_set_overrides(None) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import budgeted_kv_cache_gb300 as kvc
     monkeypatch.setattr(kvc, "_LIB", None)

@@ -60,6 +60,40 @@ def test_a_wait_that_cannot_complete_reports_timeout(kvc):
     assert int(p.score_status.abs().sum()) == 0
 
 
+def test_a_selection_wait_that_cannot_complete_reports_timeout(kvc):
+    """The selection's wait for a unit's scores (bulk copies into shared
+    memory, completing on an mbarrier) gives up after its bound: the test hook
+    makes unit 1 wait for 16 bytes more than its copy brings.  That unit
+    reports KVC_UNIT_TIMEOUT and keeps nothing; unit 0's kept list equals the
+    oracle's; the next call without the hook selects both units."""
+    w = wl.tiny()                                      # 2 units of 1,024 items: bulk-copied scores
+    p, x = _pass(w)
+    p.score(x["k_cache"], x["q_window"], x.get("bonus"))
+    torch.cuda.synchronize()
+    p.kept_count.fill_(-7)
+    kvc.kvc_set_overrides(select_stall_unit=1)
+    try:
+        p.select()
+        torch.cuda.synchronize()
+    finally:
+        kvc.kvc_set_overrides(reset=True)
+    st = p.unit_status.cpu().numpy()
+    cnt = p.kept_count.cpu().numpy()
+    assert st[1] == kvc.UNIT_TIMEOUT and st[0] == kvc.UNIT_OK
+    assert (cnt[:, 1] == 0).all()
+    sc = p.scores.cpu().numpy()
+    ref, status = o.select_tokens(sc[0], w.n_tokens, w.budget_tokens, w.n_sink, w.n_recent, None, 1)
+    assert status == o.UNIT_OK
+    assert np.array_equal(p.kept_idx[2, 0, :int(cnt[2, 0])].cpu().numpy(), np.sort(ref))
+    # the context is still usable: the same call without the hook selects both units
+    p.select()
+    torch.cuda.synchronize()
+    assert int(p.unit_status.abs().sum()) == 0
+    cnt = p.kept_count.cpu().numpy()
+    ref1, _ = o.select_tokens(sc[1], w.n_tokens, w.budget_tokens, w.n_sink, w.n_recent, None, 1)
+    assert np.array_equal(p.kept_idx[2, 1, :int(cnt[2, 1])].cpu().numpy(), np.sort(ref1))
+
+
 def test_kept_index_out_of_range_marks_its_unit(kvc):
     w = wl.tiny()
     p, x = _pass(w)
