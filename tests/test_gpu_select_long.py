@@ -158,3 +158,35 @@ def test_many_units_selection_matches_oracle(kvc, kind, n):
         ref, status = o.select_tokens(sc_all[u], n, budget, 4, 128, None, 1)
         assert status == int(st_h[u])
         assert np.array_equal(kept_h[2, u, :int(cnt_h[2, u])], np.sort(ref)), f"unit {u}"
+
+
+@pytest.mark.parametrize("extra", [0, 1, -1], ids=["bin_taken_whole", "one_more_in_bin", "one_fewer_in_bin"])
+@pytest.mark.parametrize("n", [32768, 20000])
+def test_threshold_bin_boundaries_match_oracle(kvc, extra, n):
+    """Scores in two binades: the candidates still to take (budget minus the
+    forced sink and recent items), plus `extra`, lie in [2, 4) and the rest in
+    [0.5, 1).  With extra = 0 the first radix level's threshold bin holds
+    exactly the candidates to take, so the levels stop there and its lower
+    edge is the threshold; with one more the search goes on inside the bin;
+    with one fewer the last kept candidate is the largest of the lower bin."""
+    rng = np.random.default_rng(14)
+    U = 4
+    n_sink, n_recent, budget = 4, 128, 2048
+    shape = kvc.make_shape(1, 2, 8, 2, 128, n)
+    pol = kvc.Policy(budget_tokens=budget, n_sink=n_sink, n_recent=n_recent, capacity=budget,
+                     renumber=False)
+    need = budget - n_sink - n_recent + extra
+    host = rng.uniform(0.5, 0.99, size=(U, n)).astype(np.float32)
+    for u in range(U):
+        cand = n_sink + rng.permutation(n - n_sink - n_recent)[:need]
+        host[u, cand] = rng.uniform(2.0, 3.99, size=need).astype(np.float32)
+    scores = torch.from_numpy(host).cuda()
+    kept, cnt, st = _run(kvc, shape, pol, scores, None)
+    for u in range(U):
+        sc = scores[u].cpu().numpy()
+        ref, status = o.select_tokens(sc, n, budget, n_sink, n_recent, None, 1)
+        assert status == int(st[u])
+        got = kept[2, u, :int(cnt[2, u])].cpu().numpy()
+        assert np.array_equal(got, np.sort(ref)), f"unit {u}"
+        if extra == 0:                       # exactly the high-binade candidates and the forced items
+            assert np.all(sc[got[(got >= n_sink) & (got < n - n_recent)]] >= 2.0)
