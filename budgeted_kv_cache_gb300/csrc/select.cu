@@ -1,4 +1,6 @@
-// Deterministic budgeted selection, one CTA of 1024 threads per unit.
+// Deterministic budgeted selection, one CTA per unit (1,024 threads; 256 for
+// the general kernel on units of at most 16,384 items), and a multi-CTA form
+// for token / page mode units of more than 32,768 items (end of the file).
 //
 // Token / page mode: the kept set is the forced items plus the k best
 // eligible items in the order (score descending, index ascending) -- the
@@ -12,7 +14,8 @@
 // token mode, the upgrade cost in byte mode): four 8-bit digit passes each
 // build per-warp shared-memory histograms of the items still matching the
 // key prefix and locate, with a block scan, the bin where the running weight
-// crosses the target.  Items above the final
+// crosses the target (the register-resident token / page kernel stops at
+// the first level whose threshold bin is taken whole).  Items above the final
 // key are taken; items equal to it are taken in index order while the
 // running weight still fits.  A last phase writes the kept indices in index
 // order: each warp owns a contiguous range of items and the warps' offsets
@@ -481,8 +484,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 32 ? 1 : 1024 / (NW * 32)) sele
 // (q < 32) belongs to thread t, and the keys stay in registers through the
 // radix passes.  With kBulk (the unit's scores 16-byte aligned and a
 // multiple of 16 bytes long) the scores come into shared memory through
-// bulk copies issued by one warp, which bring the unit's 128 KB in several
-// times faster than 32 rounds of 4-byte loads by every thread; otherwise
+// bulk copies issued by one warp, which bring the unit's 128 KB in about
+// half the time of 32 rounds of 4-byte loads by every thread; otherwise
 // every thread requests its 32 scores before it uses any.  In index order
 // the items of slab q come thread by thread, so the write-out needs one
 // ballot per slab and one block scan over the 1,024 (slab, warp) counts.
@@ -698,8 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_fast_kernel(const __grid_c
       n_tau = s_bincnt;
       pfx = (pfx << width) | static_cast<uint32_t>(bn);
       low = shift;
-      // every candidate of the bin is taken: its lower edge is the threshold
-      // and no candidate sits below it in the bin (uniform: shared values)
+      // every candidate of this bin is taken: the bin's lower edge serves as
+      // the threshold (uniform: t and n_tau come from shared memory)
       if (t + 1 == n_tau) break;
     }
     tau = static_cast<uint32_t>(pfx << low);
