@@ -33,6 +33,20 @@ def renumber_due(next_pos: int, limit: int, headroom: int) -> bool:
     return next_pos > limit - headroom
 
 
+def cycle_schedule(next_pos: int, budget: int, chunk: int, limit: int):
+    """Positions of one cycle whose chunk starts at physical position
+    `next_pos`: (renumber, end, next) -- whether the compaction renumbers,
+    the position one past the cache's last row, and where the following
+    chunk starts (the kept rows end with the cache's last row, which the
+    recent window always keeps; after a renumber they sit at 0..budget-1).
+    Raises ValueError if positions would pass the limit unrenumbered."""
+    end = next_pos + chunk
+    ren = renumber_due(end, limit, chunk)
+    if not ren and end > limit:
+        raise ValueError("positions would pass the limit without renumbering")
+    return ren, end, (budget if ren else end)
+
+
 class BoundedSession:
     """Compaction cycles of a session of B sequences x L layers x H_kv heads.
 
@@ -117,18 +131,13 @@ class BoundedSession:
         buffer; returns whether the kept rows were renumbered."""
         B, L, H, d = self.dims
         src, dst = self._buf(self.cur), self.passes[1 - self.cur]
-        end = self.next_pos + self.chunk          # position after the cache's last row
-        ren = renumber_due(end, self.limit, self.chunk)
-        if not ren and end > self.limit:
-            raise ValueError("positions would pass the limit without renumbering")
+        ren, end, nxt = cycle_schedule(self.next_pos, self.budget, self.chunk, self.limit)
         dst.policy.renumber = ren
         k = src.k_bf16.view(B, L, H, self.T, d)
         v = src.v_bf16.view(B, L, H, self.T, d)
         dst.run(k, v, q_window, src.pos_out[POOL_BF16], rope_cos, rope_sin, bonus, stream=stream)
         self.cur = 1 - self.cur
-        # the recent rows (the end of the chunk) are always kept: the last kept
-        # row is the cache's last row
-        self.next_pos = self.budget if ren else end
+        self.next_pos = nxt
         self.renumbered.append(ren)
         return ren
 

@@ -122,3 +122,42 @@ def test_attention_logits_depend_only_on_relative_position_across_cycles():
                     for i, p in enumerate(s["pos"])])
     scale = np.linalg.norm(qpre) * np.linalg.norm(s["pre"], axis=1)
     assert np.all(np.abs(got - exp) <= 0.05 * scale)
+
+
+@pytest.mark.parametrize("limit", [64, 128, 256, 1 << 20])
+def test_session_schedule_follows_the_oracle(limit):
+    """The library session's host-side schedule (`cycle_schedule`: where each
+    chunk starts and whether its compaction renumbers) against the oracle's
+    session run cycle by cycle: the same renumber decisions, and the next
+    chunk starts one past the largest resident position the oracle keeps.
+    Limits that renumber every cycle, every few cycles and never."""
+    from budgeted_kv_cache_gb300.session import cycle_schedule
+    steps = _session(limit, cycles=24, seed=3)
+    next_pos = B                                       # the resident rows start at 0..B-1
+    for s in steps:
+        ren, end, nxt = cycle_schedule(next_pos, B, H, limit)
+        renumbered = not np.array_equal(s["pos"], s["orig"])
+        assert ren == renumbered or (ren and np.array_equal(s["orig"], np.arange(B)))
+        assert end == next_pos + H and s["pos"].max() < limit
+        assert nxt == int(s["pos"].max()) + 1
+        next_pos = nxt
+
+
+def test_session_schedule_keeps_positions_below_the_limit():
+    """From resident rows at 0..budget-1, the schedule's caches never hold a
+    position at or past the limit, for every limit that holds one cache
+    (budget + chunk <= L), and it renumbers exactly when the next chunk would
+    otherwise reach the limit."""
+    from budgeted_kv_cache_gb300.session import cycle_schedule
+    # the next cache would end exactly at L (allowed) or one past it (renumber)
+    assert cycle_schedule(B, B, H, B + 2 * H) == (False, B + H, B + H)
+    assert cycle_schedule(B, B, H, B + 2 * H - 1) == (True, B + H, B)
+    assert cycle_schedule(B + H, B, H, B + 3 * H) == (False, B + 2 * H, B + 2 * H)
+    assert cycle_schedule(B + H, B, H, B + 3 * H - 1) == (True, B + 2 * H, B)
+    for limit in range(B + H, B + 12 * H + 1, 7):
+        next_pos = B
+        for _ in range(50):
+            ren, end, nxt = cycle_schedule(next_pos, B, H, limit)
+            assert end <= limit                          # the cache's rows sit below L
+            assert ren == (end + H > limit)              # the next chunk would pass L
+            next_pos = nxt
