@@ -84,6 +84,45 @@ def test_argument_errors_return_before_any_launch(lib):
                                     None, None, None, 0, None) == 1
 
 
+def test_compaction_decode_and_variant_arguments_are_checked_first(lib):
+    """Null, misaligned and out-of-range arguments of the compaction, decode and
+    score-pooling calls return KVC_ERR_INVALID_ARG (or KVC_ERR_UNSUPPORTED)
+    before the library looks for a device.  Every call below is refused by a
+    host check, so the stand-in pointers are never dereferenced and no kernel
+    is launched, on a machine with or without a GPU."""
+    import budgeted_kv_cache_gb300 as kvc
+    L = kvc.library()
+    A = 1 << 20                                       # a 16-byte aligned stand-in pointer
+    shape = kvc.make_shape(1, 1, 4, 2, 64, 100)
+    ren = kvc.Policy(budget_tokens=10, capacity=10, renumber=True).c()
+    pools = kvc.kvc_pools(A, A, None, None, None, None, None, None, None, None, A, None)
+    SH, PO, PL = ctypes.byref(shape), ctypes.byref(ren), ctypes.byref(pools)
+
+    def compact(k=A, v=A, pos=A, idx=A, cnt=A, cos=A, sin=A, max_pos=100, pol=PO, pl=PL):
+        return L.kvc_compact_rerotate_quant(SH, pol, k, v, pos, idx, cnt, cos, sin, max_pos, pl,
+                                            None, None)
+    assert compact(k=None) == 1 and compact(idx=None) == 1 and compact(cnt=None) == 1
+    assert compact(k=A + 8) == 1                                # caches 16-byte aligned
+    assert compact(cos=None) == 1 and compact(sin=A + 4) == 1   # renumbering needs the tables
+    assert compact(max_pos=5) == 1                              # tables shorter than the capacity
+    no_pos = kvc.kvc_pools(A, A, None, None, None, None, None, None, None, None, None, None)
+    assert compact(pl=ctypes.byref(no_pos)) == 1                # positions out are required
+    byte = kvc.Policy(budget_bytes=4096, capacity=100).c()
+    assert compact(pol=ctypes.byref(byte)) == 1                 # byte mode needs every pool
+
+    def decode(q=A, pl=PL, cnt=A, out=A):
+        return L.kvc_decode_attn(SH, PO, q, pl, cnt, 0.0, out, None, 0, None)
+    assert decode(q=None) == 1 and decode(cnt=None) == 1 and decode(out=None) == 1
+    wide = kvc.make_shape(1, 1, 32, 2, 64, 100)                 # 16 query heads per KV head
+    assert L.kvc_decode_attn(ctypes.byref(wide), PO, A, PL, A, 0.0, A, None, 0, None) == 2
+
+    B2 = 2 * A
+    assert L.kvc_pool_scores(4, 100, A, B2, 4, 0, None) == 1    # kernel sizes 1, 3, 5, 7
+    assert L.kvc_pool_scores(4, 100, A, B2, 3, 9, None) == 1    # average or maximum
+    assert L.kvc_pool_scores(4, 100, A, A, 3, 0, None) == 1     # not in place
+    assert L.kvc_pool_scores(65536, 100, A, B2, 3, 0, None) == 1  # rows within a grid dimension
+
+
 def test_overrides_check_their_ranges(lib):
     """kvc_set_overrides is host-only: out-of-range fields are refused and change nothing."""
     import budgeted_kv_cache_gb300 as kvc
