@@ -133,8 +133,10 @@ def test_overrides_check_their_ranges(lib):
     for o in bad:
         assert kvc.library().kvc_set_overrides(ctypes.byref(o)) == 1
     ok = kvc.kvc_overrides(0, 8, 0, -1, 3)
-    assert kvc.library().kvc_set_overrides(ctypes.byref(ok)) == 0
-    assert kvc.library().kvc_set_overrides(None) == 0
+    try:
+        assert kvc.library().kvc_set_overrides(ctypes.byref(ok)) == 0
+    finally:
+        assert kvc.library().kvc_set_overrides(None) == 0   # defaults for every later call
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
